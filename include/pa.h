@@ -1,0 +1,212 @@
+/*
+ * pa.h -- C ABI of libpa.so: paged attention over a block-table-addressed
+ * KV cache on GB300 (sm_103a).
+ *
+ * The method: keys and values live in fixed-size physical blocks of 16
+ * tokens; a per-sequence block table maps logical positions to physical
+ * blocks, like virtual memory; blocks may be shared between sequences with
+ * refcounts and copied on write ("03 - Engines Papers", section 2, Efficient
+ * Memory Management for LLM Serving with PagedAttention (vLLM): Key trick and
+ * What to extract; "The LLM inference engine playbook: tricks in vLLM and
+ * SGLang", Theme 3).  The attention kernel gathers K/V from those
+ * non-contiguous blocks (same section), tiles them through on-chip memory with
+ * an online softmax (FlashAttention and Milakov & Gimelshein, "References"
+ * page), splits long contexts over KV partitions and reduces the partial
+ * softmaxes by log-sum-exp ("The LLM inference engine playbook", Theme 4;
+ * "03 - Engines Papers", section 12 Cascade Inference), and serves the
+ * prefill chunks of a Sarathi hybrid batch next to the decodes
+ * ("03 - Engines Papers", section 3 Sarathi / Sarathi-Serve).
+ *
+ * Common conventions
+ *  - Every pointer argument named *device* below is a CUDA device pointer the
+ *    caller owns; the library never frees, retains or allocates memory.
+ *    Every call is asynchronous on `stream` (a cudaStream_t passed as void*;
+ *    NULL = the legacy default stream).
+ *  - bf16 tensors are row-major and contiguous unless a stride is given:
+ *      q        [num_q_tokens, num_q_heads, head_dim]
+ *      out      [num_q_tokens, num_q_heads, head_dim]
+ *      k_cache, v_cache [num_blocks, block_size, num_kv_heads, head_dim]
+ *      block_tables int32 [num_seqs, max_blocks_per_seq]
+ *      seq_lens     int32 [num_seqs]
+ *      slot_mapping int64 [num_tokens], slot = block * block_size + offset
+ *  - GQA: query head h reads kv head h / (num_q_heads / num_kv_heads).
+ *  - block_size must be 16 and head_dim 64 or 128; num_q_heads /
+ *    num_kv_heads must be an integer in [1, 8] (PA_ERR_UNSUPPORTED otherwise).
+ *  - Scores are scale * <q, k>; lse outputs are natural-log log-sum-exp of
+ *    the scaled scores, fp32.  A sequence with seq_len == 0 yields out = 0 and
+ *    lse = -inf.
+ *  - Arguments are checked on the host before anything is launched; a
+ *    failing check returns PA_ERR_INVALID / PA_ERR_UNSUPPORTED /
+ *    PA_ERR_WORKSPACE and touches nothing.  A launch failure returns
+ *    PA_ERR_CUDA.  Device-side checks (block id or slot out of range, a
+ *    length beyond the table) never fault: the offending access is skipped or
+ *    clamped and a bit is set in the device error word (pa_device_error_flags).
+ *    No call aborts, exits or traps.
+ */
+#ifndef PA_H_
+#define PA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum pa_status {
+  PA_OK = 0,
+  PA_ERR_INVALID = -1,     /* bad pointer, size or metadata */
+  PA_ERR_UNSUPPORTED = -2, /* valid but not implemented (head_dim, group, block_size) */
+  PA_ERR_CUDA = -3,        /* a CUDA runtime call or launch failed */
+  PA_ERR_WORKSPACE = -4    /* workspace missing, too small or misaligned */
+} pa_status;
+
+/* Bits of the device error word. */
+#define PA_DEVERR_BLOCK_ID 1u  /* block-table entry outside [0, num_blocks) */
+#define PA_DEVERR_SEQ_LEN 2u   /* seq_len < 0 or > max_blocks_per_seq * block_size */
+#define PA_DEVERR_SLOT 4u      /* slot >= num_blocks * block_size (skipped) */
+#define PA_DEVERR_TIMEOUT 8u   /* a pipeline wait ran past its iteration limit */
+#define PA_DEVERR_CHUNK 16u    /* prefill chunk metadata inconsistent (skipped) */
+
+/* Human-readable name of a pa_status value.  Never NULL. */
+const char *pa_status_string(int status);
+
+/* ABI version, (major << 16) | minor. */
+int pa_version(void);
+
+/*
+ * Slot scatter ("reshape and cache"): for every new token t with
+ * slot_mapping[t] >= 0,
+ *   k_cache[slot / block_size][slot % block_size][h][:] = key[t][h][:]
+ *   v_cache[...same...]                                 = value[t][h][:]
+ * for all kv heads h -- a bit-exact copy.  A negative slot is padding and is
+ * skipped.  The paged layout it writes is the one the block table addresses
+ * ("03 - Engines Papers", section 2, Key trick).
+ *   key, value        device, bf16, row t at key + t * key_token_stride
+ *                     (strides in elements, multiples of 8; head h at + h*head_dim)
+ *   k_cache, v_cache  device, bf16 [num_blocks, block_size, num_kv_heads, head_dim]
+ *   slot_mapping      device, int64 [num_tokens]
+ * Duplicate non-negative slots are invalid input (the surviving value is
+ * unspecified); pa_validate_metadata detects them.
+ */
+int pa_reshape_and_cache(const void *key, const void *value, int64_t key_token_stride,
+                         int64_t value_token_stride, void *k_cache, void *v_cache,
+                         const int64_t *slot_mapping, int num_tokens, int num_kv_heads,
+                         int head_dim, int block_size, int64_t num_blocks, void *stream);
+
+/*
+ * Copy-on-write support: copy whole physical blocks of both pools,
+ * k_cache[dst] = k_cache[src], v_cache[dst] = v_cache[src], bit-exact, for
+ * every pair (src, dst) in block_pairs (device, int64 [num_pairs, 2]).  A
+ * sequence about to write into a block whose refcount is above one is given
+ * a private copy first ("03 - Engines Papers", section 2, copy-on-write with
+ * refcounts).  Destinations must be distinct and must not be sources.
+ */
+int pa_copy_blocks(void *k_cache, void *v_cache, const int64_t *block_pairs, int num_pairs,
+                   int num_kv_heads, int head_dim, int block_size, int64_t num_blocks,
+                   void *stream);
+
+/*
+ * Bytes of workspace pa_decode needs for these sizes and partition_tokens,
+ * on the current device.  0 when no workspace is needed.  Returns 0 and sets
+ * nothing on invalid sizes (pa_decode then reports the error).
+ */
+size_t pa_decode_workspace_size(int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
+                                int max_blocks_per_seq, int block_size, int partition_tokens);
+
+/*
+ * Paged decode attention: one query per sequence, attending over positions
+ * [0, seq_lens[s]) of its paged KV (this step's new token included, so the
+ * scatter runs first):
+ *   out[s][h] = sum_j softmax_j(scale * <q[s][h], K_s[j]>) V_s[j],
+ *   K_s[j] = k_cache[block_tables[s][j / 16]][j % 16][h / group]
+ * ("03 - Engines Papers", section 2, the PagedAttention kernel gathering K/V
+ * from non-contiguous blocks; online softmax per "References", Milakov &
+ * Gimelshein).
+ *   out        device bf16 [num_seqs, num_q_heads, head_dim]
+ *   q          device bf16 [num_seqs, num_q_heads, head_dim]
+ *   out_lse    device fp32 [num_seqs, num_q_heads] or NULL
+ * partition_tokens selects how the KV is split across the GPU:
+ *   < 0  single pass: each (sequence, kv head) is one work item; no workspace.
+ *   = 0  balanced: the total KV is cut into equal contiguous ranges, one per
+ *        persistent CTA; pieces of a sequence that straddle ranges are merged
+ *        by log-sum-exp inside the same launch.  Needs workspace, which must
+ *        be zero-filled before its first use (the kernel leaves it zeroed).
+ *   > 0  split-KV with fixed partitions of partition_tokens tokens (a multiple
+ *        of block_size): partition p covers [p * P, (p + 1) * P) and writes a
+ *        partial (o_p, lse_p) to the workspace, laid out exactly as
+ *        pa_merge_partials reads it; a merge kernel then combines them
+ *        (partial buffers first: part_out [S, Hq, P_max, D] fp32, then part_lse
+ *        [S, Hq, P_max] fp32, P_max = ceil(max_blocks_per_seq * 16 / P)).
+ * A workspace may not be shared by two calls in flight at the same time.
+ */
+int pa_decode(void *out, const void *q, const void *k_cache, const void *v_cache,
+              const int32_t *block_tables, int max_blocks_per_seq, const int32_t *seq_lens,
+              int num_seqs, int num_q_heads, int num_kv_heads, int head_dim, int block_size,
+              int64_t num_blocks, float scale, int partition_tokens, float *out_lse,
+              void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * Log-sum-exp merge of partial attentions ("03 - Engines Papers", section 12
+ * Cascade Inference, merged via LSE; split-K softmax reduction, "The LLM
+ * inference engine playbook", Theme 4):
+ *   L = max_p lse_p,  w_p = exp(lse_p - L),
+ *   out = sum_p w_p o_p / sum_p w_p,  lse = L + ln sum_p w_p
+ * over p < num_parts[s].  Parts with lse = -inf have weight 0; if every part
+ * is -inf the output is 0 and lse -inf.
+ *   part_out  device fp32 [num_seqs, num_q_heads, max_parts, head_dim]
+ *   part_lse  device fp32 [num_seqs, num_q_heads, max_parts]
+ *   num_parts device int32 [num_seqs], each in [0, max_parts]
+ *   out       device bf16 [num_seqs, num_q_heads, head_dim]; out_lse fp32 or NULL
+ */
+int pa_merge_partials(void *out, float *out_lse, const float *part_out, const float *part_lse,
+                      const int32_t *num_parts, int num_seqs, int num_q_heads, int head_dim,
+                      int max_parts, void *stream);
+
+/*
+ * Causal prefill chunks of a hybrid batch ("03 - Engines Papers", section 3
+ * Sarathi / Sarathi-Serve: long prefills split into chunks co-scheduled with
+ * decodes; a chunk's queries see the K/V of earlier positions and of the chunk
+ * itself, not of later chunks).  Chunk c owns query rows
+ * [cu_q_lens[c], cu_q_lens[c + 1]); row i sits at absolute position
+ * q_start_pos[c] + i and attends over keys 0 .. that position of sequence c
+ * (block table row c), which holds seq_lens[c] >= q_start_pos[c] + q_len
+ * tokens (the chunk's own K/V already scattered).  Runs on tcgen05 tensor
+ * cores with fp32 accumulation in tensor memory.
+ *   q, out     device bf16 [total_q_tokens, num_q_heads, head_dim]
+ *   cu_q_lens  device int32 [num_chunks + 1]; q_start_pos, seq_lens int32 [num_chunks]
+ *   max_q_len  host int, an upper bound of every chunk's query count
+ *   out_lse    device fp32 [total_q_tokens, num_q_heads] or NULL
+ * head_dim must be 128 for this call.
+ */
+int pa_prefill_chunk(void *out, const void *q, const void *k_cache, const void *v_cache,
+                     const int32_t *block_tables, int max_blocks_per_seq,
+                     const int32_t *cu_q_lens, const int32_t *q_start_pos,
+                     const int32_t *seq_lens, int num_chunks, int total_q_tokens, int max_q_len,
+                     int num_q_heads, int num_kv_heads, int head_dim, int block_size,
+                     int64_t num_blocks, float scale, float *out_lse, void *stream);
+
+/*
+ * Host-side metadata check (host pointers; any of block_tables / slot_mapping
+ * / refcount may be NULL to skip that part).  Returns PA_OK or PA_ERR_INVALID:
+ * table entries of every used block in [0, num_blocks); 0 <= seq_len <=
+ * max_blocks_per_seq * block_size; slots in range and pairwise distinct; with
+ * a refcount array, no slot targets a block whose refcount is above one (the
+ * copy-on-write rule).
+ */
+int pa_validate_metadata(const int32_t *block_tables, int max_blocks_per_seq,
+                         const int32_t *seq_lens, int num_seqs, const int64_t *slot_mapping,
+                         int num_slots, const int32_t *refcount, int64_t num_blocks,
+                         int block_size);
+
+/*
+ * Read (and with reset != 0, clear) the device error word of the current
+ * device into *flags (PA_DEVERR_* bits).  Synchronizes with the device.
+ */
+int pa_device_error_flags(unsigned int *flags, int reset);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PA_H_ */

@@ -1,0 +1,538 @@
+// pa_api.cu -- the C ABI of libpa.so (declared in include/pa.h): argument
+// checks, TMA descriptor setup, launch selection, and the small kernels
+// (slot scatter, block copy, log-sum-exp merge).
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <math.h>
+#include <stdint.h>
+#include <string.h>
+
+#include <mutex>
+#include <unordered_set>
+
+#include "../../include/pa.h"
+#include "pa_internal.h"
+
+namespace pa {
+namespace {
+
+// Device error word (PA_DEVERR_* bits), one per device that loads the library.
+__device__ unsigned int g_device_error;
+
+constexpr int kMaxDevices = 64;
+
+struct DeviceInfo {
+  bool ready = false;
+  int num_sms = 0;
+  unsigned int* err = nullptr;
+};
+
+std::mutex g_mu;
+DeviceInfo g_dev[kMaxDevices];
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+int current_device_info(DeviceInfo** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return PA_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(g_mu);
+  DeviceInfo& d = g_dev[dev];
+  if (!d.ready) {
+    if (cudaDeviceGetAttribute(&d.num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      return PA_ERR_CUDA;
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_device_error) != cudaSuccess) return PA_ERR_CUDA;
+    d.err = static_cast<unsigned int*>(p);
+    d.ready = true;
+  }
+  if (!g_encode) {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) !=
+            cudaSuccess ||
+        q != cudaDriverEntryPointSuccess || fn == nullptr)
+      return PA_ERR_CUDA;
+    g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  }
+  *out = &d;
+  return PA_OK;
+}
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+// Paged pool [num_blocks * 16 tokens, Hkv, D] as a 3-D tensor; box = 64
+// columns x 1 head x `rows` tokens, 128-byte swizzle.
+int encode_pool_map(CUtensorMap* m, const void* pool, int64_t num_blocks, int Hkv, int D,
+                    int rows) {
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(Hkv),
+                        static_cast<cuuint64_t>(num_blocks) * kBlockSize};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(D) * 2, static_cast<cuuint64_t>(Hkv) * D * 2};
+  cuuint32_t box[3] = {64, 1, static_cast<cuuint32_t>(rows)};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(pool), dims,
+                        strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? PA_OK : PA_ERR_CUDA;
+}
+
+// q [T, Hq, D] as a 3-D tensor; box = 64 columns x `heads` heads x `rows` tokens.
+int encode_q_map(CUtensorMap* m, const void* q, int64_t T, int Hq, int D, int heads, int rows) {
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(Hq),
+                        static_cast<cuuint64_t>(T)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(D) * 2, static_cast<cuuint64_t>(Hq) * D * 2};
+  cuuint32_t box[3] = {64, static_cast<cuuint32_t>(heads), static_cast<cuuint32_t>(rows)};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(q), dims,
+                        strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? PA_OK : PA_ERR_CUDA;
+}
+
+int check_shape(int Hq, int Hkv, int D, int block_size) {
+  if (Hq <= 0 || Hkv <= 0 || D <= 0 || block_size <= 0) return PA_ERR_INVALID;
+  if (Hq % Hkv != 0) return PA_ERR_INVALID;
+  if (block_size != kBlockSize) return PA_ERR_UNSUPPORTED;
+  if (D != 64 && D != 128) return PA_ERR_UNSUPPORTED;
+  if (Hq / Hkv > kMaxGroup) return PA_ERR_UNSUPPORTED;
+  return PA_OK;
+}
+
+// ------------------------------------------------------------------ kernels
+
+// One thread copies 16 bytes (8 bf16) of K and of V for one (token, head).
+__global__ void reshape_and_cache_kernel(const uint4* __restrict__ key,
+                                         const uint4* __restrict__ value, int64_t key_stride16,
+                                         int64_t value_stride16, uint4* __restrict__ k_cache,
+                                         uint4* __restrict__ v_cache,
+                                         const int64_t* __restrict__ slots, int num_tokens,
+                                         int vec_per_token, int64_t num_slots,
+                                         unsigned int* err) {
+  const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (i >= static_cast<int64_t>(num_tokens) * vec_per_token) return;
+  const int t = static_cast<int>(i / vec_per_token);
+  const int c = static_cast<int>(i % vec_per_token);
+  const int64_t slot = slots[t];
+  if (slot < 0) return;
+  if (slot >= num_slots) {
+    if (c == 0) atomicOr(err, PA_DEVERR_SLOT);
+    return;
+  }
+  k_cache[slot * vec_per_token + c] = key[t * key_stride16 + c];
+  v_cache[slot * vec_per_token + c] = value[t * value_stride16 + c];
+}
+
+__global__ void copy_blocks_kernel(uint4* __restrict__ k_cache, uint4* __restrict__ v_cache,
+                                   const int64_t* __restrict__ pairs, int64_t vec_per_block,
+                                   int64_t num_blocks, unsigned int* err) {
+  const int p = blockIdx.y;
+  const int64_t src = pairs[2 * p], dst = pairs[2 * p + 1];
+  if (src < 0 || src >= num_blocks || dst < 0 || dst >= num_blocks) {
+    if (blockIdx.x == 0 && threadIdx.x == 0) atomicOr(err, PA_DEVERR_BLOCK_ID);
+    return;
+  }
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < vec_per_block;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    k_cache[dst * vec_per_block + i] = k_cache[src * vec_per_block + i];
+    v_cache[dst * vec_per_block + i] = v_cache[src * vec_per_block + i];
+  }
+}
+
+// Log-sum-exp merge: one CTA of 128 threads per (sequence, q head); warp w
+// takes parts w, w+4, ...; each lane holds head_dim/32 output columns.
+template <int D>
+__global__ void __launch_bounds__(128) merge_kernel(const MergeArgs a) {
+  constexpr int V = D / 32;
+  const int s = blockIdx.x / a.num_q_heads;
+  const int h = blockIdx.x % a.num_q_heads;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  int np;
+  if (a.num_parts) {
+    np = a.num_parts[s];
+    np = np < 0 ? 0 : (np > a.max_parts ? a.max_parts : np);
+  } else {
+    int len = a.seq_lens[s];
+    const int cap = a.max_blocks * kBlockSize;
+    len = len < 0 ? 0 : (len > cap ? cap : len);
+    const int nb = (len + kBlockSize - 1) / kBlockSize;
+    np = nb == 0 ? 1 : (nb + a.part_blocks - 1) / a.part_blocks;
+    if (a.skip_single && np == 1) return;
+  }
+  const int64_t row = static_cast<int64_t>(s) * a.num_q_heads + h;
+  const float* lse = a.part_lse + row * a.max_parts;
+  const float* po = a.part_o + row * a.max_parts * D;
+  __shared__ float red[4];
+  __shared__ float acc_s[4][D];
+  __shared__ float wsum_s[4];
+  float L = -INFINITY;
+  for (int p = threadIdx.x; p < np; p += 128) L = fmaxf(L, lse[p]);
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) L = fmaxf(L, __shfl_xor_sync(0xffffffffu, L, off));
+  if (lane == 0) red[warp] = L;
+  __syncthreads();
+  L = fmaxf(fmaxf(red[0], red[1]), fmaxf(red[2], red[3]));
+  float acc[V];
+#pragma unroll
+  for (int v = 0; v < V; ++v) acc[v] = 0.f;
+  float wsum = 0.f;
+  if (L != -INFINITY) {
+    for (int p = warp; p < np; p += 4) {
+      const float w = __expf(lse[p] - L);
+      wsum += w;
+      const float* src = po + static_cast<int64_t>(p) * D + lane * V;
+      if constexpr (V == 4) {
+        const float4 x = *reinterpret_cast<const float4*>(src);
+        acc[0] += w * x.x;
+        acc[1] += w * x.y;
+        acc[2] += w * x.z;
+        acc[3] += w * x.w;
+      } else {
+        const float2 x = *reinterpret_cast<const float2*>(src);
+        acc[0] += w * x.x;
+        acc[1] += w * x.y;
+      }
+    }
+  }
+#pragma unroll
+  for (int v = 0; v < V; ++v) acc_s[warp][lane * V + v] = acc[v];
+  if (lane == 0) wsum_s[warp] = wsum;
+  __syncthreads();
+  const float W = wsum_s[0] + wsum_s[1] + wsum_s[2] + wsum_s[3];
+  for (int d = threadIdx.x; d < D; d += 128) {
+    const float o = acc_s[0][d] + acc_s[1][d] + acc_s[2][d] + acc_s[3][d];
+    a.out[row * a.head_dim + d] = __float2bfloat16(W > 0.f ? o / W : 0.f);
+  }
+  if (threadIdx.x == 0 && a.out_lse) a.out_lse[row] = W > 0.f ? L + __logf(W) : -INFINITY;
+}
+
+}  // namespace
+
+cudaError_t launch_merge(const MergeArgs& a, cudaStream_t stream) {
+  const int grid = a.num_seqs * a.num_q_heads;
+  if (grid == 0) return cudaSuccess;
+  if (a.head_dim == 128)
+    merge_kernel<128><<<grid, 128, 0, stream>>>(a);
+  else
+    merge_kernel<64><<<grid, 128, 0, stream>>>(a);
+  return cudaGetLastError();
+}
+
+}  // namespace pa
+
+using namespace pa;
+
+extern "C" {
+
+const char* pa_status_string(int status) {
+  switch (status) {
+    case PA_OK: return "PA_OK";
+    case PA_ERR_INVALID: return "PA_ERR_INVALID";
+    case PA_ERR_UNSUPPORTED: return "PA_ERR_UNSUPPORTED";
+    case PA_ERR_CUDA: return "PA_ERR_CUDA";
+    case PA_ERR_WORKSPACE: return "PA_ERR_WORKSPACE";
+    default: return "PA_ERR_UNKNOWN";
+  }
+}
+
+int pa_version(void) { return (1 << 16) | 0; }
+
+int pa_reshape_and_cache(const void* key, const void* value, int64_t key_token_stride,
+                         int64_t value_token_stride, void* k_cache, void* v_cache,
+                         const int64_t* slot_mapping, int num_tokens, int num_kv_heads,
+                         int head_dim, int block_size, int64_t num_blocks, void* stream) {
+  if (num_tokens < 0 || num_kv_heads <= 0 || head_dim <= 0 || num_blocks <= 0) return PA_ERR_INVALID;
+  if (block_size != kBlockSize) return PA_ERR_UNSUPPORTED;
+  if (head_dim % 8 != 0) return PA_ERR_UNSUPPORTED;
+  if (num_tokens == 0) return PA_OK;
+  if (!key || !value || !k_cache || !v_cache || !slot_mapping) return PA_ERR_INVALID;
+  const int64_t row = static_cast<int64_t>(num_kv_heads) * head_dim;
+  if (key_token_stride < row || value_token_stride < row || key_token_stride % 8 ||
+      value_token_stride % 8)
+    return PA_ERR_INVALID;
+  if (!aligned(key, 16) || !aligned(value, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) ||
+      !aligned(slot_mapping, 8))
+    return PA_ERR_INVALID;
+  DeviceInfo* d;
+  if (int rc = current_device_info(&d)) return rc;
+  const int vec = static_cast<int>(row / 8);
+  const int64_t total = static_cast<int64_t>(num_tokens) * vec;
+  const int threads = 256;
+  const int64_t blocks = (total + threads - 1) / threads;
+  reshape_and_cache_kernel<<<static_cast<unsigned>(blocks), threads, 0,
+                             static_cast<cudaStream_t>(stream)>>>(
+      static_cast<const uint4*>(key), static_cast<const uint4*>(value), key_token_stride / 8,
+      value_token_stride / 8, static_cast<uint4*>(k_cache), static_cast<uint4*>(v_cache),
+      slot_mapping, num_tokens, vec, num_blocks * block_size, d->err);
+  return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+
+int pa_copy_blocks(void* k_cache, void* v_cache, const int64_t* block_pairs, int num_pairs,
+                   int num_kv_heads, int head_dim, int block_size, int64_t num_blocks,
+                   void* stream) {
+  if (num_pairs < 0 || num_kv_heads <= 0 || head_dim <= 0 || num_blocks <= 0) return PA_ERR_INVALID;
+  if (block_size != kBlockSize) return PA_ERR_UNSUPPORTED;
+  if (head_dim % 8 != 0) return PA_ERR_UNSUPPORTED;
+  if (num_pairs == 0) return PA_OK;
+  if (num_pairs > 65535) return PA_ERR_UNSUPPORTED;
+  if (!k_cache || !v_cache || !block_pairs) return PA_ERR_INVALID;
+  if (!aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(block_pairs, 8))
+    return PA_ERR_INVALID;
+  DeviceInfo* d;
+  if (int rc = current_device_info(&d)) return rc;
+  const int64_t vec = static_cast<int64_t>(block_size) * num_kv_heads * head_dim / 8;
+  dim3 grid(static_cast<unsigned>((vec + 255) / 256 < 64 ? (vec + 255) / 256 : 64), num_pairs);
+  copy_blocks_kernel<<<grid, 256, 0, static_cast<cudaStream_t>(stream)>>>(
+      static_cast<uint4*>(k_cache), static_cast<uint4*>(v_cache), block_pairs, vec, num_blocks,
+      d->err);
+  return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+
+static int decode_mode(int partition_tokens) {
+  return partition_tokens < 0 ? kModeSinglePass
+                              : (partition_tokens == 0 ? kModeBalanced : kModeFixedSplit);
+}
+
+static size_t fixed_workspace_bytes(int num_seqs, int Hq, int D, int max_parts) {
+  const size_t rows = static_cast<size_t>(num_seqs) * Hq * max_parts;
+  const size_t o = (rows * D * 4 + 255) / 256 * 256;
+  return o + (rows * 4 + 255) / 256 * 256;
+}
+
+size_t pa_decode_workspace_size(int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
+                                int max_blocks_per_seq, int block_size, int partition_tokens) {
+  if (num_seqs < 0 || max_blocks_per_seq <= 0) return 0;
+  if (check_shape(num_q_heads, num_kv_heads, head_dim, block_size) != PA_OK) return 0;
+  const int mode = decode_mode(partition_tokens);
+  if (mode == kModeSinglePass) return 0;
+  if (mode == kModeFixedSplit) {
+    if (partition_tokens % block_size) return 0;
+    const int pb = partition_tokens / block_size;
+    const int max_parts = (max_blocks_per_seq + pb - 1) / pb;
+    return fixed_workspace_bytes(num_seqs, num_q_heads, head_dim, max_parts);
+  }
+  int num_sms = 0, dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+      num_sms <= 0) {
+    cudaGetLastError();
+    num_sms = 1024;  // no device visible: an upper bound
+  }
+  return balanced_workspace_bytes(decode_grid(num_sms, kModeBalanced), num_q_heads / num_kv_heads,
+                                  head_dim);
+}
+
+int pa_decode(void* out, const void* q, const void* k_cache, const void* v_cache,
+              const int32_t* block_tables, int max_blocks_per_seq, const int32_t* seq_lens,
+              int num_seqs, int num_q_heads, int num_kv_heads, int head_dim, int block_size,
+              int64_t num_blocks, float scale, int partition_tokens, float* out_lse,
+              void* workspace, size_t workspace_bytes, void* stream) {
+  if (int rc = check_shape(num_q_heads, num_kv_heads, head_dim, block_size)) return rc;
+  if (num_seqs < 0 || max_blocks_per_seq <= 0 || num_blocks <= 0) return PA_ERR_INVALID;
+  if (num_blocks * kBlockSize > (int64_t)INT32_MAX) return PA_ERR_UNSUPPORTED;
+  if (!(scale > 0.f) || !isfinite(scale)) return PA_ERR_INVALID;
+  if (num_seqs == 0) return PA_OK;
+  if (!out || !q || !k_cache || !v_cache || !block_tables || !seq_lens) return PA_ERR_INVALID;
+  if (!aligned(out, 16) || !aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) ||
+      !aligned(block_tables, 4) || !aligned(seq_lens, 4) || (out_lse && !aligned(out_lse, 4)))
+    return PA_ERR_INVALID;
+  const int mode = decode_mode(partition_tokens);
+  if (mode == kModeFixedSplit && partition_tokens % block_size) return PA_ERR_INVALID;
+  if (mode == kModeBalanced && num_seqs > kMaxSeqsBalanced) return PA_ERR_UNSUPPORTED;
+  DeviceInfo* d;
+  if (int rc = current_device_info(&d)) return rc;
+
+  DecodeArgs a{};
+  a.out = static_cast<__nv_bfloat16*>(out);
+  a.q = static_cast<const __nv_bfloat16*>(q);
+  a.block_tables = block_tables;
+  a.seq_lens = seq_lens;
+  a.out_lse = out_lse;
+  a.err = d->err;
+  a.num_blocks = num_blocks;
+  a.max_blocks = max_blocks_per_seq;
+  a.num_seqs = num_seqs;
+  a.num_q_heads = num_q_heads;
+  a.num_kv_heads = num_kv_heads;
+  a.group = num_q_heads / num_kv_heads;
+  a.scale_log2 = scale * 1.4426950408889634f;
+  a.mode = mode;
+  int grid = decode_grid(d->num_sms, mode);
+  if (mode == kModeSinglePass) {
+    a.part_blocks = max_blocks_per_seq;
+    a.max_parts = 1;
+    const int64_t units = static_cast<int64_t>(num_seqs) * num_kv_heads;
+    if (units < grid) grid = static_cast<int>(units);
+  } else if (mode == kModeFixedSplit) {
+    a.part_blocks = partition_tokens / block_size;
+    a.max_parts = (max_blocks_per_seq + a.part_blocks - 1) / a.part_blocks;
+    const size_t need = fixed_workspace_bytes(num_seqs, num_q_heads, head_dim, a.max_parts);
+    if (!workspace || workspace_bytes < need || !aligned(workspace, 256)) return PA_ERR_WORKSPACE;
+    const size_t rows = static_cast<size_t>(num_seqs) * num_q_heads * a.max_parts;
+    a.part_o = static_cast<float*>(workspace);
+    a.part_lse = reinterpret_cast<float*>(static_cast<char*>(workspace) +
+                                          (rows * head_dim * 4 + 255) / 256 * 256);
+    const int64_t units = static_cast<int64_t>(num_seqs) * a.max_parts * num_kv_heads;
+    if (units < grid) grid = static_cast<int>(units);
+  } else {
+    const size_t need = balanced_workspace_bytes(grid, a.group, head_dim);
+    if (!workspace || workspace_bytes < need || !aligned(workspace, 256)) return PA_ERR_WORKSPACE;
+    a.counters = static_cast<int*>(workspace);
+    a.part_o = reinterpret_cast<float*>(static_cast<char*>(workspace) +
+                                        (static_cast<size_t>(grid) * 4 + 255) / 256 * 256);
+    a.slot_floats = static_cast<int>(balanced_slot_floats(a.group, head_dim));
+  }
+
+  CUtensorMap tm_k, tm_v;
+  if (encode_pool_map(&tm_k, k_cache, num_blocks, num_kv_heads, head_dim, kBlockSize) ||
+      encode_pool_map(&tm_v, v_cache, num_blocks, num_kv_heads, head_dim, kBlockSize))
+    return PA_ERR_CUDA;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (launch_decode(a, &tm_k, &tm_v, head_dim, grid, st) != cudaSuccess) return PA_ERR_CUDA;
+  if (mode == kModeFixedSplit) {
+    MergeArgs m{};
+    m.out = a.out;
+    m.out_lse = out_lse;
+    m.part_o = a.part_o;
+    m.part_lse = a.part_lse;
+    m.num_parts = nullptr;
+    m.seq_lens = seq_lens;
+    m.part_blocks = a.part_blocks;
+    m.max_blocks = max_blocks_per_seq;
+    m.skip_single = 1;
+    m.num_seqs = num_seqs;
+    m.num_q_heads = num_q_heads;
+    m.head_dim = head_dim;
+    m.max_parts = a.max_parts;
+    if (launch_merge(m, st) != cudaSuccess) return PA_ERR_CUDA;
+  }
+  return PA_OK;
+}
+
+int pa_merge_partials(void* out, float* out_lse, const float* part_out, const float* part_lse,
+                      const int32_t* num_parts, int num_seqs, int num_q_heads, int head_dim,
+                      int max_parts, void* stream) {
+  if (num_seqs < 0 || num_q_heads <= 0 || max_parts <= 0) return PA_ERR_INVALID;
+  if (head_dim != 64 && head_dim != 128) return PA_ERR_UNSUPPORTED;
+  if (static_cast<int64_t>(num_seqs) * num_q_heads > INT32_MAX) return PA_ERR_UNSUPPORTED;
+  if (num_seqs == 0) return PA_OK;
+  if (!out || !part_out || !part_lse || !num_parts) return PA_ERR_INVALID;
+  if (!aligned(part_out, 16) || !aligned(part_lse, 4) || !aligned(num_parts, 4) ||
+      !aligned(out, 4) || (out_lse && !aligned(out_lse, 4)))
+    return PA_ERR_INVALID;
+  DeviceInfo* d;
+  if (int rc = current_device_info(&d)) return rc;
+  MergeArgs m{};
+  m.out = static_cast<__nv_bfloat16*>(out);
+  m.out_lse = out_lse;
+  m.part_o = part_out;
+  m.part_lse = part_lse;
+  m.num_parts = num_parts;
+  m.num_seqs = num_seqs;
+  m.num_q_heads = num_q_heads;
+  m.head_dim = head_dim;
+  m.max_parts = max_parts;
+  return launch_merge(m, static_cast<cudaStream_t>(stream)) == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+
+int pa_prefill_chunk(void* out, const void* q, const void* k_cache, const void* v_cache,
+                     const int32_t* block_tables, int max_blocks_per_seq,
+                     const int32_t* cu_q_lens, const int32_t* q_start_pos,
+                     const int32_t* seq_lens, int num_chunks, int total_q_tokens, int max_q_len,
+                     int num_q_heads, int num_kv_heads, int head_dim, int block_size,
+                     int64_t num_blocks, float scale, float* out_lse, void* stream) {
+  if (int rc = check_shape(num_q_heads, num_kv_heads, head_dim, block_size)) return rc;
+  if (head_dim != 128) return PA_ERR_UNSUPPORTED;
+  const int group = num_q_heads / num_kv_heads;
+  if (128 % group != 0) return PA_ERR_UNSUPPORTED;
+  if (num_chunks < 0 || total_q_tokens < 0 || max_q_len < 0 || max_blocks_per_seq <= 0 ||
+      num_blocks <= 0)
+    return PA_ERR_INVALID;
+  if (num_blocks * kBlockSize > (int64_t)INT32_MAX) return PA_ERR_UNSUPPORTED;
+  if (!(scale > 0.f) || !isfinite(scale)) return PA_ERR_INVALID;
+  if (num_chunks == 0 || total_q_tokens == 0 || max_q_len == 0) return PA_OK;
+  if (!out || !q || !k_cache || !v_cache || !block_tables || !cu_q_lens || !q_start_pos ||
+      !seq_lens)
+    return PA_ERR_INVALID;
+  if (!aligned(out, 16) || !aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16))
+    return PA_ERR_INVALID;
+  DeviceInfo* d;
+  if (int rc = current_device_info(&d)) return rc;
+  PrefillArgs a{};
+  a.out = static_cast<__nv_bfloat16*>(out);
+  a.block_tables = block_tables;
+  a.cu_q_lens = cu_q_lens;
+  a.q_start_pos = q_start_pos;
+  a.seq_lens = seq_lens;
+  a.out_lse = out_lse;
+  a.err = d->err;
+  a.num_blocks = num_blocks;
+  a.max_blocks = max_blocks_per_seq;
+  a.num_chunks = num_chunks;
+  a.num_q_heads = num_q_heads;
+  a.num_kv_heads = num_kv_heads;
+  a.group = group;
+  const int tokens_per_tile = 128 / group;
+  a.tiles_per_chunk = (max_q_len + tokens_per_tile - 1) / tokens_per_tile;
+  a.scale_log2 = scale * 1.4426950408889634f;
+  CUtensorMap tm_q, tm_k, tm_v;
+  if (encode_q_map(&tm_q, q, total_q_tokens, num_q_heads, head_dim, group, tokens_per_tile) ||
+      encode_pool_map(&tm_k, k_cache, num_blocks, num_kv_heads, head_dim, kBlockSize) ||
+      encode_pool_map(&tm_v, v_cache, num_blocks, num_kv_heads, head_dim, kBlockSize))
+    return PA_ERR_CUDA;
+  const int64_t tiles = static_cast<int64_t>(a.tiles_per_chunk) * num_chunks * num_kv_heads;
+  if (tiles > INT32_MAX) return PA_ERR_UNSUPPORTED;
+  return launch_prefill(a, &tm_q, &tm_k, &tm_v, static_cast<int>(tiles),
+                        static_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? PA_OK
+             : PA_ERR_CUDA;
+}
+
+int pa_validate_metadata(const int32_t* block_tables, int max_blocks_per_seq,
+                         const int32_t* seq_lens, int num_seqs, const int64_t* slot_mapping,
+                         int num_slots, const int32_t* refcount, int64_t num_blocks,
+                         int block_size) {
+  if (num_seqs < 0 || num_slots < 0 || num_blocks <= 0 || block_size <= 0) return PA_ERR_INVALID;
+  if (num_seqs > 0 && !seq_lens) return PA_ERR_INVALID;
+  for (int s = 0; s < num_seqs; ++s) {
+    const int64_t n = seq_lens[s];
+    if (n < 0 || n > static_cast<int64_t>(max_blocks_per_seq) * block_size) return PA_ERR_INVALID;
+    if (block_tables) {
+      const int64_t nb = (n + block_size - 1) / block_size;
+      for (int64_t j = 0; j < nb; ++j) {
+        const int64_t b = block_tables[static_cast<int64_t>(s) * max_blocks_per_seq + j];
+        if (b < 0 || b >= num_blocks) return PA_ERR_INVALID;
+      }
+    }
+  }
+  if (slot_mapping && num_slots > 0) {
+    std::unordered_set<int64_t> seen;
+    seen.reserve(static_cast<size_t>(num_slots) * 2);
+    for (int t = 0; t < num_slots; ++t) {
+      const int64_t slot = slot_mapping[t];
+      if (slot < 0) continue;
+      if (slot >= num_blocks * block_size) return PA_ERR_INVALID;
+      if (!seen.insert(slot).second) return PA_ERR_INVALID;
+      if (refcount && refcount[slot / block_size] > 1) return PA_ERR_INVALID;
+    }
+  }
+  return PA_OK;
+}
+
+int pa_device_error_flags(unsigned int* flags, int reset) {
+  if (!flags) return PA_ERR_INVALID;
+  DeviceInfo* d;
+  if (int rc = current_device_info(&d)) return rc;
+  if (cudaDeviceSynchronize() != cudaSuccess) return PA_ERR_CUDA;
+  unsigned int v = 0;
+  if (cudaMemcpy(&v, d->err, sizeof v, cudaMemcpyDeviceToHost) != cudaSuccess) return PA_ERR_CUDA;
+  *flags = v;
+  if (reset) {
+    const unsigned int z = 0;
+    if (cudaMemcpy(d->err, &z, sizeof z, cudaMemcpyHostToDevice) != cudaSuccess) return PA_ERR_CUDA;
+  }
+  return PA_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,93 @@
+// pa_internal.h -- launch parameters shared between the C-ABI front end
+// (pa_api.cu) and the kernel translation units.  Not part of the public ABI.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace pa {
+
+constexpr int kBlockSize = 16;
+constexpr int kMaxGroup = 8;            // q heads per kv head handled by one MMA column tile
+constexpr int kMaxSeqsBalanced = 16000; // per-CTA prefix of block counts lives in shared memory
+
+enum DecodeMode : int {
+  kModeSinglePass = 0,  // one work item per (sequence, kv head)
+  kModeFixedSplit = 1,  // fixed partitions of part_blocks blocks, partials + merge kernel
+  kModeBalanced = 2,    // equal contiguous block ranges per CTA, merged in-kernel
+};
+
+struct DecodeArgs {
+  __nv_bfloat16* out;           // [S, Hq, D]
+  const __nv_bfloat16* q;       // [S, Hq, D]
+  const int32_t* block_tables;  // [S, max_blocks]
+  const int32_t* seq_lens;      // [S]
+  float* out_lse;               // [S, Hq] or null
+  float* part_o;                // fixed: [S, Hq, P_max, D]; balanced: slots
+  float* part_lse;              // fixed: [S, Hq, P_max]
+  int* counters;                // balanced: [grid] merge tickets (self-resetting)
+  unsigned int* err;            // device error word
+  int64_t num_blocks;
+  int max_blocks;
+  int num_seqs;
+  int num_q_heads;
+  int num_kv_heads;
+  int group;
+  float scale_log2;  // scale * log2(e)
+  int mode;
+  int part_blocks;   // fixed split / single pass: blocks per partition
+  int max_parts;     // fixed split: P_max
+  int slot_floats;   // balanced: floats per partial slot
+};
+
+struct MergeArgs {
+  __nv_bfloat16* out;
+  float* out_lse;
+  const float* part_o;
+  const float* part_lse;
+  const int32_t* num_parts;  // explicit counts, or null to derive from seq_lens
+  const int32_t* seq_lens;   // with part_blocks: parts = max(1, ceil(ceil(len/16)/part_blocks))
+  int part_blocks;
+  int max_blocks;
+  int skip_single;           // parts == 1 were written final by the decode kernel
+  int num_seqs;
+  int num_q_heads;
+  int head_dim;
+  int max_parts;
+};
+
+struct PrefillArgs {
+  __nv_bfloat16* out;
+  const int32_t* block_tables;
+  const int32_t* cu_q_lens;
+  const int32_t* q_start_pos;
+  const int32_t* seq_lens;
+  float* out_lse;
+  unsigned int* err;
+  int64_t num_blocks;
+  int max_blocks;
+  int num_chunks;
+  int num_q_heads;
+  int num_kv_heads;
+  int group;
+  int tiles_per_chunk;  // M tiles of 128 rows per (chunk, kv head)
+  float scale_log2;
+};
+
+// Balanced-mode workspace layout (shared by the size query and the launch).
+size_t balanced_slot_floats(int group, int head_dim);
+size_t balanced_workspace_bytes(int grid, int group, int head_dim);
+
+// Kernel launchers (return cudaError_t of the launch).
+cudaError_t launch_decode(const DecodeArgs& a, const CUtensorMap* tm_k, const CUtensorMap* tm_v,
+                          int head_dim, int grid, cudaStream_t stream);
+int decode_grid(int num_sms, int mode);
+size_t decode_smem_bytes(int head_dim, int mode, int num_seqs);
+cudaError_t launch_merge(const MergeArgs& a, cudaStream_t stream);
+cudaError_t launch_prefill(const PrefillArgs& a, const CUtensorMap* tm_q, const CUtensorMap* tm_k,
+                           const CUtensorMap* tm_v, int grid_tiles, cudaStream_t stream);
+size_t prefill_smem_bytes();
+
+}  // namespace pa
