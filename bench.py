@@ -1,0 +1,496 @@
+"""Benchmark: paged decode KV-read GB/s (and decode tokens/s) on GB300.
+
+Default workload: one Llama-3-8B-shaped decode layer -- 64 sequences with
+lengths uniform[128, 2048], 32 q / 8 kv heads, head_dim 128, 16-token blocks
+drawn at random from a pool 1.25x the need, bf16 N(0, 1) data (seeded,
+synthetic).  One step = the slot scatter of the 64 new tokens followed by
+balanced paged decode over every sequence (the whole decode hot path), on
+one of 8 independent copies of the KV pool in rotation so that the working
+set (~2.7 GB) is far above the 129 MB L2.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+                    [--config llama3_8b_decode_layer|long_context_split_kv|
+                              cow_prefix_mix|sarathi_hybrid]
+
+Prints one JSON line (rank 0).  Under torchrun each rank runs an independent
+replica of the workload on its own GPU (the decode path needs no exchange);
+value = all ranks' KV bytes / the slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "paged decode KV-read GB/s & % of GB300 HBM peak; decode tokens/s at batch"
+FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
+NOMINAL_HBM_GBS = 8000.0
+
+CONFIG_TEXT = {
+    "llama3_8b_decode_layer": "Llama-3-8B-shaped decode layer: 64 seqs, seq_lens U[128,2048], "
+                              "32 q / 8 kv heads, head_dim 128, block 16, bf16 N(0,1)",
+    "long_context_split_kv": "long-context decode: 8 seqs, seq_lens U[32768,131072], 32 q / 8 kv "
+                             "heads, head_dim 128, block 16, bf16 N(0,1)",
+    "cow_prefix_mix": "continuous-batching mix: 256 seqs, lognormal(median 512, sigma 1) lengths "
+                      "in [1,8192], 64 q / 8 kv heads, head_dim 128, groups of 4 alias a "
+                      "256-token prefix with copy-on-write",
+    "sarathi_hybrid": "Sarathi hybrid batch: prefill chunk of 512 queries at positions "
+                      "1536-2047 + 128 decodes with seq_lens U[256,4096], 32 q / 8 kv heads, "
+                      "head_dim 128, token budget 640",
+}
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), float(p["bf16_tflops"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS, "fallback"
+
+
+def profile_traffic(kernel_file: str, summary: str):
+    """Per-launch DRAM bytes recorded by an ncu capture in profiles/, valid only
+    while the kernel source still has the hash the summary was taken at."""
+    try:
+        src = open(os.path.join(ROOT, "paged_kv_cache_218_gb300", "csrc", kernel_file), "rb").read()
+        sha = hashlib.sha256(src).hexdigest()[:16]
+        fields = {}
+        for line in open(os.path.join(ROOT, "profiles", summary)):
+            if ":" in line and line.strip().startswith("- "):
+                k, v = line.strip()[2:].split(":", 1)
+                fields[k.strip()] = v.strip().strip("`")
+        if fields.get("source_sha256_16") != sha:
+            return None
+        return float(fields["traffic_bytes_per_launch"])
+    except Exception:
+        return None
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason samples every 200 ms."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.idx = device_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        import tempfile
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.idx), f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        sms, maxs, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sms.append(float(parts[1]))
+                maxs.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        os.unlink(self.path)
+        return {"sm_mhz": statistics.median(sms) if sms else None,
+                "sm_max_mhz": max(maxs) if maxs else None,
+                "samples": len(sms), "reasons": sorted(reasons)}
+
+
+# ----------------------------------------------------------------------------- workload
+
+def make_workload(name):
+    from paged_kv_cache_218_gb300 import workload as W
+    return {"llama3_8b_decode_layer": W.llama3_8b_layer, "long_context_split_kv": W.long_context_split,
+            "cow_prefix_mix": W.cow_mix, "sarathi_hybrid": W.sarathi_hybrid}[name]()
+
+
+class Replica:
+    """One device-resident copy of the step's state (KV pools, tables, inputs)."""
+
+    def __init__(self, w, dev, src=None):
+        import numpy as np
+        import torch
+
+        def bits(a):
+            return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).to(dev)
+
+        if src is None:
+            self.k_cache = bits(w.k_cache)
+            self.v_cache = bits(w.v_cache)
+        else:
+            self.k_cache = src.k_cache.clone()
+            self.v_cache = src.v_cache.clone()
+        self.q = bits(w.q)
+        self.key = bits(w.key)
+        self.value = bits(w.value)
+        self.block_tables = torch.from_numpy(w.block_tables).to(dev)
+        self.seq_lens = torch.from_numpy(w.seq_lens).to(dev)
+        self.slot_mapping = torch.from_numpy(w.slot_mapping).to(dev)
+        S, Hq, D = w.num_decode_seqs, w.num_q_heads, w.head_dim
+        self.out = torch.empty((S, Hq, D), dtype=torch.bfloat16, device=dev)
+        C = w.num_chunks
+        if C:
+            T = int(w.cu_q_lens[C])
+            self.out_chunk = torch.empty((T, Hq, D), dtype=torch.bfloat16, device=dev)
+            self.cu = torch.from_numpy(w.cu_q_lens).to(dev)
+            self.qs = torch.from_numpy(w.q_start_pos).to(dev)
+
+
+def decode_args(w, r):
+    s0, q0, S = w.decode_seq0, w.q_decode_row0, w.num_decode_seqs
+    return (r.out, r.q[q0:q0 + S], r.k_cache, r.v_cache, r.block_tables[s0:], r.seq_lens[s0:])
+
+
+def kv_bytes_decode(w):
+    from paged_kv_cache_218_gb300 import workload as W
+    return W.logical_kv_bytes(w.decode_seq_lens, w.num_kv_heads, w.head_dim)
+
+
+def decode_algorithmic_bytes(w):
+    """Minimal bytes one decode launch must move: every K/V token once, the
+    queries, the outputs, the used block-table entries and the lengths."""
+    S, Hq, D = w.num_decode_seqs, w.num_q_heads, w.head_dim
+    nb = sum((int(n) + 15) // 16 for n in w.decode_seq_lens)
+    return kv_bytes_decode(w) + 2 * S * Hq * D * 2 + nb * 4 + S * 4
+
+
+def chunk_flops(w):
+    """Causal (q, k) pairs of the prefill chunk x heads x 4 x head_dim
+    (QK^T and PV, 2 flops per multiply-add)."""
+    pairs = 0
+    for c in range(w.num_chunks):
+        n = int(w.cu_q_lens[c + 1] - w.cu_q_lens[c])
+        p0 = int(w.q_start_pos[c])
+        pairs += n * p0 + n * (n + 1) // 2
+    return 4.0 * pairs * w.num_q_heads * w.head_dim
+
+
+# ----------------------------------------------------------------------------- arms
+
+def run_gpu(args, rank, world, local_rank):
+    import torch
+
+    from paged_kv_cache_218_gb300 import binding as pa
+
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    w = make_workload(args.config)
+    R = args.replicas
+    reps = [Replica(w, dev)]
+    for _ in range(R - 1):
+        reps.append(Replica(w, dev, src=reps[0]))
+    S, Hq, D = w.num_decode_seqs, w.num_q_heads, w.head_dim
+    P = args.partition_tokens
+    ws = [pa.alloc_workspace(pa.pa_decode_workspace_size(S, Hq, w.num_kv_heads, D,
+                                                         w.max_blocks_per_seq, 16, P), dev)
+          for _ in range(R)]
+    hybrid = w.num_chunks > 0
+    max_q = int(max(w.cu_q_lens[1:] - w.cu_q_lens[:-1])) if hybrid else 0
+    T = int(w.cu_q_lens[w.num_chunks]) if hybrid else 0
+    main = torch.cuda.current_stream()
+    s_chunk = torch.cuda.Stream(device=dev) if hybrid else None
+    launches_per_step = 2 + (1 if P > 0 else 0) + (1 if hybrid else 0)
+
+    def step(i, ev=None, cev=None):
+        r = reps[i % R]
+        pa.pa_reshape_and_cache(r.key, r.value, r.k_cache, r.v_cache, r.slot_mapping)
+        if hybrid:
+            s_chunk.wait_stream(main)
+            if cev is not None:
+                cev[0].record(s_chunk)
+            pa.pa_prefill_chunk(r.out_chunk, r.q[:T], r.k_cache, r.v_cache,
+                                r.block_tables[:w.num_chunks], r.cu, r.qs,
+                                r.seq_lens[:w.num_chunks], max_q, w.scale, stream=s_chunk)
+            if cev is not None:
+                cev[1].record(s_chunk)
+        if ev is not None:
+            ev[0].record(main)
+        pa.pa_decode(*decode_args(w, r), w.scale, partition_tokens=P, workspace=ws[i % R])
+        if ev is not None:
+            ev[1].record(main)
+        if hybrid:
+            main.wait_stream(s_chunk)
+
+    for i in range(args.warmup):
+        step(i)
+    torch.cuda.synchronize()
+    if pa.pa_device_error_flags() != 0:
+        raise RuntimeError("device error flags set during warm-up")
+
+    dist = world > 1
+    if dist:
+        import torch.distributed as tdist
+    K = args.steps
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(K)]
+    cevs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+            for _ in range(K)] if hybrid else [None] * K
+    sampler = ClockSampler(dev.index if dev.index is not None else 0)
+    sampler.start()
+    time.sleep(0.6)
+    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if dist:
+        tdist.barrier()
+    torch.cuda.synchronize()
+    t_start.record(main)
+    for i in range(K):
+        step(i, evs[i], cevs[i])
+    t_end.record(main)
+    torch.cuda.synchronize()
+    if dist:
+        tdist.barrier()
+    clocks = sampler.stop()
+    elapsed_ms = t_start.elapsed_time(t_end)
+    if dist:
+        t = torch.tensor([elapsed_ms], dtype=torch.float64, device=dev)
+        tdist.all_reduce(t, op=tdist.ReduceOp.MAX)
+        elapsed_ms = float(t.item())
+    dec_ms = sum(a.elapsed_time(b) for a, b in evs) / K
+    chunk_ms = sum(a.elapsed_time(b) for a, b in cevs) / K if hybrid else None
+    flags = pa.pa_device_error_flags()
+    if flags:
+        raise RuntimeError(f"device error flags {flags} after the timed region")
+
+    e2e = run_e2e(args, w, reps, ws, dev, pa, dist)
+    return dict(w=w, elapsed_ms=elapsed_ms, dec_ms=dec_ms, chunk_ms=chunk_ms, clocks=clocks,
+                e2e=e2e, launches=launches_per_step * K)
+
+
+def run_e2e(args, w, reps, ws, dev, pa, dist):
+    """Same metric through the public API with host buffers: every step copies
+    its inputs (queries, new K/V, slots, block tables, lengths) from pinned
+    host memory, runs scatter + decode, and reads the output back."""
+    import torch
+
+    K = max(args.warmup + 1, min(args.steps, args.e2e_steps))
+    r = reps[0]
+    s0, q0, S = w.decode_seq0, w.q_decode_row0, w.num_decode_seqs
+    host = {n: getattr(r, n).cpu().pin_memory() for n in
+            ("q", "key", "value", "slot_mapping", "block_tables", "seq_lens")}
+    out_h = torch.empty(r.out.shape, dtype=r.out.dtype).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    d2h = out_h.numel() * out_h.element_size()
+    P = args.partition_tokens
+    main = torch.cuda.current_stream()
+
+    def step(i):
+        rr = reps[i % len(reps)]
+        for n, t in host.items():
+            getattr(rr, n).copy_(t, non_blocking=True)
+        pa.pa_reshape_and_cache(rr.key, rr.value, rr.k_cache, rr.v_cache, rr.slot_mapping)
+        pa.pa_decode(*decode_args(w, rr), w.scale, partition_tokens=P, workspace=ws[i % len(reps)])
+        out_h.copy_(rr.out, non_blocking=True)
+
+    for i in range(args.warmup):
+        step(i)
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if dist:
+        import torch.distributed as tdist
+        tdist.barrier()
+    torch.cuda.synchronize()
+    a.record(main)
+    for i in range(K):
+        step(i)
+    b.record(main)
+    torch.cuda.synchronize()
+    ms = a.elapsed_time(b)
+    if dist:
+        t = torch.tensor([ms], dtype=torch.float64, device=dev)
+        tdist.all_reduce(t, op=tdist.ReduceOp.MAX)
+        ms = float(t.item())
+    return dict(ms=ms, steps=K, h2d=h2d, d2h=d2h)
+
+
+def run_oracle(w, min_seconds):
+    """The fp64 CPU oracle as it stands, on the host cores: decode attention
+    over the whole batch (its KV already holding the new tokens), repeated
+    until at least `min_seconds` of CPU time; returns (seconds per pass,
+    passes, threads, kv bytes per pass)."""
+    import oracle
+    kc, vc = oracle.copy_blocks(w.k_cache, w.v_cache, w.cow_pairs)
+    kc, vc = oracle.reshape_and_cache(w.key, w.value, kc, vc, w.slot_mapping)
+    passes, t0 = 0, time.perf_counter()
+    while True:
+        oracle.decode(w.decode_q, kc, vc, w.decode_block_tables, w.decode_seq_lens, w.scale)
+        passes += 1
+        el = time.perf_counter() - t0
+        if el >= min_seconds or passes >= 1000:
+            break
+    return el / passes, passes, oracle.num_threads(), kv_bytes_decode(w)
+
+
+def cpu_baseline_obj(w, min_seconds):
+    sec, passes, cores, kvb = run_oracle(w, min_seconds)
+    return {"value": kvb / sec / 1e9, "unit": "GB/s", "cores": cores, "kind": "oracle",
+            "sample": f"fp64 oracle decode over the whole batch ({w.num_decode_seqs} seqs, "
+                      f"{kvb / 1e6:.1f} MB of bf16 KV), repeated {passes}x in {sec * passes:.1f} s; "
+                      f"slot scatter excluded", "tokens_per_s": w.num_decode_seqs / sec}
+
+
+def reference_arm(args):
+    """K timed steps of the oracle, each a bounded sample of the workload: a
+    rotating subset of the sequences sized so that warm-up + K steps take
+    about --cpu-seconds in total."""
+    import numpy as np
+
+    import oracle
+    from paged_kv_cache_218_gb300 import workload as W
+    w = make_workload(args.config)
+    kc, vc = oracle.copy_blocks(w.k_cache, w.v_cache, w.cow_pairs)
+    kc, vc = oracle.reshape_and_cache(w.key, w.value, kc, vc, w.slot_mapping)
+    q, bt, sl = w.decode_q, w.decode_block_tables, w.decode_seq_lens
+    S = w.num_decode_seqs
+    t0 = time.perf_counter()
+    oracle.decode(q, kc, vc, bt, sl, w.scale)
+    full = time.perf_counter() - t0
+    per_step = args.cpu_seconds / (args.steps + args.warmup)
+    n = int(max(1, min(S, round(S * per_step / full))))
+
+    def step(i):
+        idx = (np.arange(n) + i * n) % S
+        oracle.decode(q[idx], kc, vc, bt[idx], sl[idx], w.scale)
+        return W.logical_kv_bytes(sl[idx], w.num_kv_heads, w.head_dim)
+
+    for i in range(args.warmup):
+        step(i)
+    kvb = 0
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        kvb += step(args.warmup + i)
+    el = time.perf_counter() - t0
+    value = kvb / el / 1e9
+    cores = oracle.num_threads()
+    sample = (f"each step: fp64 oracle decode of {n} of the {S} sequences (rotating), "
+              f"KV already holding the new tokens; slot scatter excluded")
+    return {"impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": el / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": CONFIG_TEXT[args.config], "name": args.config},
+            "tokens_per_s": n * args.steps / el,
+            "cpu_baseline": {"value": value, "unit": "GB/s", "cores": cores, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10000)
+    ap.add_argument("--warmup", type=int, default=50)
+    ap.add_argument("--impl", default="native", choices=["native", "reference"])
+    ap.add_argument("--config", default="llama3_8b_decode_layer", choices=sorted(CONFIG_TEXT))
+    ap.add_argument("--partition-tokens", type=int, default=None,
+                    help="decode split mode (0 balanced, >0 fixed partitions, <0 single pass)")
+    ap.add_argument("--replicas", type=int, default=8)
+    ap.add_argument("--e2e-steps", type=int, default=2000)
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    if args.partition_tokens is None:
+        args.partition_tokens = 0
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    hbm, bf16, peak_src = load_peaks()
+
+    if args.impl == "reference":
+        # the reference arm is the fp64 oracle on the host cores; rank 0 only
+        if rank != 0:
+            return
+        print(json.dumps(reference_arm(args)), flush=True)
+        return
+
+    if world > 1:
+        import torch
+        import torch.distributed as tdist
+        torch.cuda.set_device(local_rank)
+        tdist.init_process_group("nccl")
+    res = run_gpu(args, rank, world, local_rank)
+    w = res["w"]
+    K = args.steps
+    kvb = kv_bytes_decode(w)
+    step_ms = res["elapsed_ms"] / K
+    value = kvb * world * K / (res["elapsed_ms"] * 1e-3) / 1e9
+    alg = decode_algorithmic_bytes(w)
+    achieved = alg / (res["dec_ms"] * 1e-3) / 1e9
+    traffic = profile_traffic("pa_decode.cu", "decode_kernel_llama3_8b_decode_layer.md") \
+        if args.config == "llama3_8b_decode_layer" else None
+    e = res["e2e"]
+    line = {
+        "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": K,
+        "warmup": args.warmup, "ms_per_step": step_ms, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": CONFIG_TEXT[args.config], "name": args.config,
+                   "partition_tokens": args.partition_tokens,
+                   "accumulate": "fp32",
+                   "l2": f"{args.replicas} independent KV pools in rotation "
+                         f"({args.replicas * 2 * w.k_cache.nbytes / 1e9:.2f} GB) >> 129 MB L2",
+                   "parallelism": f"replicas x{world}"},
+        "tokens_per_s": w.num_decode_seqs * world * K / (res["elapsed_ms"] * 1e-3),
+        "pct_of_nominal_8tbps": 100.0 * value / world / NOMINAL_HBM_GBS,
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
+                     "frac": achieved / hbm, "traffic": traffic,
+                     "kernel": "decode_kernel<128>", "peak_source": f"{peak_src} (hbm_gbs)",
+                     "bytes_per_launch": alg, "launch_ms": res["dec_ms"]},
+        "e2e": {"value": kvb * world * e["steps"] / (e["ms"] * 1e-3) / 1e9, "unit": "GB/s",
+                "h2d_bytes_per_step": e["h2d"], "d2h_bytes_per_step": e["d2h"],
+                "steps": e["steps"], "ms_per_step": e["ms"] / e["steps"]},
+        "gpu_launches": res["launches"],
+        "clocks": res["clocks"],
+    }
+    if res["chunk_ms"] is not None:
+        fl = chunk_flops(w)
+        line["prefill_chunk"] = {"tflops": fl / (res["chunk_ms"] * 1e-3) / 1e12,
+                                 "frac_of_bf16_peak": fl / (res["chunk_ms"] * 1e-3) / 1e12 / bf16,
+                                 "peak": bf16, "gflop": fl / 1e9, "launch_ms": res["chunk_ms"],
+                                 "peak_source": f"{peak_src} (bf16_tflops)"}
+    if rank == 0:
+        line["cpu_baseline"] = cpu_baseline_obj(w, args.cpu_seconds)
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as tdist
+        tdist.barrier()
+        tdist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

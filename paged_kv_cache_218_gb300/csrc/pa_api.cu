@@ -319,8 +319,7 @@ size_t pa_decode_workspace_size(int num_seqs, int num_q_heads, int num_kv_heads,
     cudaGetLastError();
     num_sms = 1024;  // no device visible: an upper bound
   }
-  return balanced_workspace_bytes(decode_grid(num_sms, kModeBalanced), num_q_heads / num_kv_heads,
-                                  head_dim);
+  return balanced_workspace_bytes(decode_grid(num_sms, kModeBalanced), num_q_heads, head_dim);
 }
 
 int pa_decode(void* out, const void* q, const void* k_cache, const void* v_cache,
@@ -340,6 +339,7 @@ int pa_decode(void* out, const void* q, const void* k_cache, const void* v_cache
   const int mode = decode_mode(partition_tokens);
   if (mode == kModeFixedSplit && partition_tokens % block_size) return PA_ERR_INVALID;
   if (mode == kModeBalanced && num_seqs > kMaxSeqsBalanced) return PA_ERR_UNSUPPORTED;
+  if (!decode_supported(head_dim, num_kv_heads, mode, num_seqs)) return PA_ERR_UNSUPPORTED;
   DeviceInfo* d;
   if (int rc = current_device_info(&d)) return rc;
 
@@ -362,8 +362,7 @@ int pa_decode(void* out, const void* q, const void* k_cache, const void* v_cache
   if (mode == kModeSinglePass) {
     a.part_blocks = max_blocks_per_seq;
     a.max_parts = 1;
-    const int64_t units = static_cast<int64_t>(num_seqs) * num_kv_heads;
-    if (units < grid) grid = static_cast<int>(units);
+    if (num_seqs < grid) grid = num_seqs;
   } else if (mode == kModeFixedSplit) {
     a.part_blocks = partition_tokens / block_size;
     a.max_parts = (max_blocks_per_seq + a.part_blocks - 1) / a.part_blocks;
@@ -373,15 +372,15 @@ int pa_decode(void* out, const void* q, const void* k_cache, const void* v_cache
     a.part_o = static_cast<float*>(workspace);
     a.part_lse = reinterpret_cast<float*>(static_cast<char*>(workspace) +
                                           (rows * head_dim * 4 + 255) / 256 * 256);
-    const int64_t units = static_cast<int64_t>(num_seqs) * a.max_parts * num_kv_heads;
+    const int64_t units = static_cast<int64_t>(num_seqs) * a.max_parts;
     if (units < grid) grid = static_cast<int>(units);
   } else {
-    const size_t need = balanced_workspace_bytes(grid, a.group, head_dim);
+    const size_t need = balanced_workspace_bytes(grid, num_q_heads, head_dim);
     if (!workspace || workspace_bytes < need || !aligned(workspace, 256)) return PA_ERR_WORKSPACE;
     a.counters = static_cast<int*>(workspace);
     a.part_o = reinterpret_cast<float*>(static_cast<char*>(workspace) +
                                         (static_cast<size_t>(grid) * 4 + 255) / 256 * 256);
-    a.slot_floats = static_cast<int>(balanced_slot_floats(a.group, head_dim));
+    a.slot_floats = static_cast<int>(balanced_slot_floats(num_q_heads, head_dim));
   }
 
   CUtensorMap tm_k, tm_v;

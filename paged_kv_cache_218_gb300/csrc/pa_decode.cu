@@ -4,27 +4,31 @@
 // section 2 PagedAttention: the kernel gathers K/V from non-contiguous
 // 16-token blocks named by the block table).  Design:
 //
-//  * Persistent CTAs, one per SM: 4 consumer warps + 1 producer warp.
-//  * The producer walks the CTA's work (a list of block ranges of
-//    (sequence, kv head) segments), prefetches block-table rows 32 entries at
-//    a time, and streams each 16-token block of one kv head into a ring of
-//    shared-memory stages with TMA tensor loads (two 64-column boxes per
-//    row of 128 bf16, 128-byte swizzled), signalling an mbarrier per stage.
-//  * Consumer warp w takes every 4th stage.  GQA: the group's q heads are the
-//    N=8 columns of a warp MMA, so each K/V byte loaded is used by every q
-//    head of its group: S^T[16 tokens x 8 heads] = K[16 x D] Q^T[D x 8]
-//    (mma.m16n8k16, bf16 in, fp32 accumulate), online softmax over the
-//    block's 16 scores per head with warp-shuffle max reductions (Milakov &
-//    Gimelshein recurrence, "References" page), then O^T[D x 8] += V^T P^T.
-//  * At the end of a segment piece the 4 warps' running (m, l, O) are merged
-//    through shared memory and the result is written: final bf16 output, a
+//  * Persistent CTAs, one per SM: 8 consumer warps + 1 producer warp.
+//  * Work is a list of (sequence, block range) pieces covering *all* kv heads
+//    of each block, so one physical block -- 16 tokens x Hkv heads x D,
+//    contiguous in the pool -- is streamed as a whole (DRAM-page friendly).
+//  * The producer walks the CTA's pieces, prefetches block-table rows 32
+//    entries at a time, and lands each block in a ring of shared-memory
+//    stages with TMA tensor loads: per kv head, K and V as 64-column boxes of
+//    16 token rows, 128-byte swizzled so warp-level matrix loads are
+//    bank-conflict free.  One mbarrier per stage counts the bytes in.
+//  * Consumer warps map to kv heads (with Hkv < 8, several warps share a head
+//    and split its blocks).  GQA: the group's q heads are the N=8 columns of
+//    a warp MMA, so each K/V byte loaded serves every q head of its group:
+//    S^T[16 tok x 8 heads] = K[16 x D] Q^T (mma.m16n8k16, bf16 in, fp32
+//    accumulate), a per-head online softmax over the block's 16 scores with
+//    warp-shuffle max reductions (the Milakov & Gimelshein recurrence,
+//    "References" page), then O^T[D x 8] += V^T P^T.
+//  * At the end of a piece the result is written: final bf16 output, a
 //    fixed-partition partial for the LSE merge kernel, or (balanced mode) a
-//    partial that the last-arriving CTA of that segment merges in place by
+//    partial that the last-arriving CTA of that sequence merges in place by
 //    log-sum-exp ("03 - Engines Papers", section 12 Cascade Inference;
 //    split-K reduction of "The LLM inference engine playbook", Theme 4).
 //
-// No wait is unbounded: every mbarrier spin gives up after kWaitLimit tries,
-// sets PA_DEVERR_TIMEOUT and stops the CTA's work.
+// No wait is unbounded: every mbarrier spin gives up after a two-second limit,
+// sets PA_DEVERR_TIMEOUT, and the CTA then skips the rest of its work while
+// still meeting its named barriers.
 #include <math.h>
 
 #include "../../include/pa.h"
@@ -34,41 +38,50 @@
 namespace pa {
 namespace {
 
-constexpr int kConsumerWarps = 4;
-constexpr int kThreads = (kConsumerWarps + 1) * 32;
+constexpr int kConsumerWarps = 8;
+constexpr int kConsumerThreads = kConsumerWarps * 32;
+constexpr int kThreads = kConsumerThreads + 32;
 constexpr int kBoxBytes = 16 * 128;  // one TMA box: 16 token rows x 64 bf16
+constexpr int kMaxStages = 16;
 constexpr float kLn2 = 0.6931471805599453f;
-
-template <int D>
-struct Cfg {
-  static constexpr int kStages = D == 128 ? 16 : 24;
-  static constexpr int kHalves = D / 64;
-  static constexpr int kKBytes = kHalves * kBoxBytes;  // K of one block, one kv head
-  static constexpr int kStageBytes = 2 * kKBytes;      // K + V
-  static constexpr int kObufStride = D + 4;            // padded head row (bank spread)
-  static constexpr int kObufFloats = kConsumerWarps * kMaxGroup * kObufStride;
-  static constexpr int kStageOff = 0;
-  static constexpr int kObufOff = kStages * kStageBytes;
-  static constexpr int kMlOff = kObufOff + kObufFloats * 4;
-  static constexpr int kLseOff = kMlOff + kConsumerWarps * kMaxGroup * 2 * 4;
-  static constexpr int kBarOff = kLseOff + kMaxGroup * 2 * 4;
-  static constexpr int kMiscOff = kBarOff + kStages * 2 * 8;
-  static constexpr int kPreOff = kMiscOff + 64;
-};
 
 enum PieceKind : int { kFinal = 0, kPartialFixed = 1, kPartialBalanced = 2 };
 
 struct Piece {
-  int s, kvh, j0, j1, len, nb, kind, part, which;
+  int s, j0, j1, len, nb, kind, part, which;
   long long seg_start;
 };
 
 struct Cursor {
-  long long u, U;          // fixed / single-pass unit walk
-  long long idx, lo, hi;   // balanced block range [lo, hi)
-  long long W;             // balanced: total blocks
-  int C;                   // balanced: CTAs that own a non-empty range
+  long long u, U;         // fixed / single-pass unit walk
+  long long idx, lo, hi;  // balanced block range [lo, hi)
+  long long W;            // balanced: total blocks
+  int C;                  // balanced: CTAs that own a non-empty range
 };
+
+// Shared-memory carve-up (byte offsets from a 1024-aligned base).
+struct Layout {
+  int head_bytes;   // K (or V) of one block, one kv head
+  int stage_bytes;  // K + V of one block, all kv heads
+  int stages;
+  int obuf_off, ml_off, bar_off, misc_off, pre_off, total;
+};
+
+__host__ __device__ inline Layout make_layout(int D, int Hkv, int wph, int stages,
+                                              int pre_ints) {
+  Layout L;
+  L.head_bytes = (D / 64) * kBoxBytes;
+  L.stage_bytes = 2 * Hkv * L.head_bytes;
+  L.stages = stages;
+  L.obuf_off = stages * L.stage_bytes;
+  const int obuf = wph > 1 ? kConsumerWarps * kMaxGroup * (D + 4) * 4 : 0;
+  L.ml_off = L.obuf_off + obuf;
+  L.bar_off = L.ml_off + kConsumerWarps * kMaxGroup * 2 * 4;
+  L.misc_off = L.bar_off + kMaxStages * 2 * 8;
+  L.pre_off = L.misc_off + 64;
+  L.total = L.pre_off + pre_ints * 4;
+  return L;
+}
 
 __device__ __forceinline__ int load_len(const DecodeArgs& a, int s, bool report) {
   int len = a.seq_lens[s];
@@ -89,27 +102,22 @@ __device__ bool next_piece(const DecodeArgs& a, const int* pre, Cursor& c, Piece
                            bool report) {
   if (a.mode == kModeBalanced) {
     if (c.idx >= c.hi) return false;
-    const long long Hkv = a.num_kv_heads;
-    int lo = 0, hi = a.num_seqs - 1;  // largest s with Hkv*pre[s] <= idx
+    int lo = 0, hi = a.num_seqs - 1;  // largest s with pre[s] <= idx
     while (lo < hi) {
-      int mid = (lo + hi + 1) >> 1;
-      if (Hkv * pre[mid] <= c.idx) lo = mid; else hi = mid - 1;
+      const int mid = (lo + hi + 1) >> 1;
+      if (pre[mid] <= c.idx) lo = mid; else hi = mid - 1;
     }
     const int s = lo;
-    const int nb = pre[s + 1] - pre[s];
-    const long long base = Hkv * pre[s];
-    const long long r = c.idx - base;
     p.s = s;
-    p.nb = nb;
-    p.kvh = static_cast<int>(r / nb);
-    p.j0 = static_cast<int>(r % nb);
-    p.seg_start = base + static_cast<long long>(p.kvh) * nb;
-    const long long seg_end = p.seg_start + nb;
+    p.nb = pre[s + 1] - pre[s];
+    p.seg_start = pre[s];
+    p.j0 = static_cast<int>(c.idx - p.seg_start);
+    const long long seg_end = p.seg_start + p.nb;
     const long long end = c.hi < seg_end ? c.hi : seg_end;
     p.j1 = p.j0 + static_cast<int>(end - c.idx);
     c.idx = end;
     p.len = load_len(a, s, false);
-    p.kind = (p.j0 == 0 && p.j1 == nb) ? kFinal : kPartialBalanced;
+    p.kind = (p.j0 == 0 && p.j1 == p.nb) ? kFinal : kPartialBalanced;
     p.which = p.seg_start < c.lo ? 0 : 1;
     p.part = 0;
     return true;
@@ -117,16 +125,13 @@ __device__ bool next_piece(const DecodeArgs& a, const int* pre, Cursor& c, Piece
   while (c.u < c.U) {
     const long long u = c.u;
     c.u += gridDim.x;
-    const int kvh = static_cast<int>(u % a.num_kv_heads);
-    const long long t = u / a.num_kv_heads;
-    const int part = static_cast<int>(t % a.max_parts);
-    const int s = static_cast<int>(t / a.max_parts);
-    const int len = load_len(a, s, report && part == 0 && kvh == 0);
+    const int part = static_cast<int>(u % a.max_parts);
+    const int s = static_cast<int>(u / a.max_parts);
+    const int len = load_len(a, s, report && part == 0);
     const int nb = (len + kBlockSize - 1) / kBlockSize;
     const int nparts = nb == 0 ? 1 : (nb + a.part_blocks - 1) / a.part_blocks;
     if (part >= nparts) continue;
     p.s = s;
-    p.kvh = kvh;
     p.len = len;
     p.nb = nb;
     p.j0 = part * a.part_blocks;
@@ -149,11 +154,10 @@ struct ChunkIter {
 };
 
 __device__ __forceinline__ bool next_chunk(const DecodeArgs& a, const int* pre, ChunkIter& it,
-                                           int& s, int& kvh, int& jb, int& n) {
+                                           int& s, int& jb, int& n) {
   while (true) {
     if (it.valid && it.jb < it.pc.j1) {
       s = it.pc.s;
-      kvh = it.pc.kvh;
       jb = it.jb;
       n = min(32, it.pc.j1 - it.jb);
       it.jb += n;
@@ -177,8 +181,8 @@ __device__ __forceinline__ int load_ids(const DecodeArgs& a, int s, int jb, int 
   return id;
 }
 
-// Address of the 16-byte chunk `chunk` (8 bf16) of token row `tok` in a
-// block staged as kHalves 128-byte-swizzled boxes of 16 rows.
+// Address of the 16-byte chunk `chunk` (8 bf16) of token row `tok` in one
+// head's block, staged as 128-byte-swizzled boxes of 16 rows x 64 columns.
 __device__ __forceinline__ uint32_t swz(uint32_t base, int tok, int chunk) {
   return base + (chunk >> 3) * kBoxBytes + tok * 128 + (((chunk & 7) ^ (tok & 7)) << 4);
 }
@@ -191,21 +195,24 @@ __device__ __forceinline__ void attend_block(uint32_t kbase, uint32_t vbase,
                                              int lane) {
   constexpr int KS = D / 16;
   const int i = lane >> 3, r = lane & 7;
-  float sacc[4] = {0.f, 0.f, 0.f, 0.f};
+  // two independent accumulation chains halve the dependent MMA latency
+  float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb[4] = {0.f, 0.f, 0.f, 0.f};
   const int ktok = r + ((i & 1) << 3);
 #pragma unroll
-  for (int ks = 0; ks < KS; ++ks) {
-    uint32_t a[4];
-    ldsm_x4(swz(kbase, ktok, ks * 2 + (i >> 1)), a);
-    mma_bf16_16816(sacc, a, qf[ks][0], qf[ks][1]);
+  for (int ks = 0; ks < KS; ks += 2) {
+    uint32_t a0[4], a1[4];
+    ldsm_x4(swz(kbase, ktok, ks * 2 + (i >> 1)), a0);
+    ldsm_x4(swz(kbase, ktok, (ks + 1) * 2 + (i >> 1)), a1);
+    mma_bf16_16816(sa, a0, qf[ks][0], qf[ks][1]);
+    mma_bf16_16816(sb, a1, qf[ks + 1][0], qf[ks + 1][1]);
   }
-  // sacc: [token lane/4][heads 2q, 2q+1], [token lane/4 + 8][same heads]
+  // S^T: [token lane/4][heads 2q, 2q+1], [token lane/4 + 8][same heads]
   const int t0 = lane >> 2;
   const bool v0 = t0 < valid, v1 = t0 + 8 < valid;
-  const float x0 = v0 ? sacc[0] * scale_log2 : -INFINITY;
-  const float x1 = v0 ? sacc[1] * scale_log2 : -INFINITY;
-  const float x2 = v1 ? sacc[2] * scale_log2 : -INFINITY;
-  const float x3 = v1 ? sacc[3] * scale_log2 : -INFINITY;
+  const float x0 = v0 ? (sa[0] + sb[0]) * scale_log2 : -INFINITY;
+  const float x1 = v0 ? (sa[1] + sb[1]) * scale_log2 : -INFINITY;
+  const float x2 = v1 ? (sa[2] + sb[2]) * scale_log2 : -INFINITY;
+  const float x3 = v1 ? (sa[3] + sb[3]) * scale_log2 : -INFINITY;
   float mxa = fmaxf(x0, x2), mxb = fmaxf(x1, x3);
 #pragma unroll
   for (int off = 4; off < 32; off <<= 1) {
@@ -253,26 +260,29 @@ template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
     decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                   const DecodeArgs a) {
-  using C = Cfg<D>;
+  constexpr int KS = D / 16;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_u32(smem_raw);
   uint8_t* smem = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
   const uint32_t sbase = smem_u32(smem);
-  float* obuf = reinterpret_cast<float*>(smem + C::kObufOff);
-  float* mlbuf = reinterpret_cast<float*>(smem + C::kMlOff);
-  float* lsebuf = reinterpret_cast<float*>(smem + C::kLseOff);
-  int* misc = reinterpret_cast<int*>(smem + C::kMiscOff);
-  int* pre = reinterpret_cast<int*>(smem + C::kPreOff);
-  const uint32_t bar_full = sbase + C::kBarOff;
-  const uint32_t bar_empty = bar_full + C::kStages * 8;
+
+  const int Hkv = a.num_kv_heads, G = a.group;
+  const int wph = a.warps_per_head;
+  const Layout L = make_layout(D, Hkv, wph, a.stages, 0);
+  float* obuf = reinterpret_cast<float*>(smem + L.obuf_off);
+  float* mlbuf = reinterpret_cast<float*>(smem + L.ml_off);
+  int* misc = reinterpret_cast<int*>(smem + L.misc_off);
+  int* pre = reinterpret_cast<int*>(smem + L.pre_off);
+  const uint32_t bar_full = sbase + L.bar_off;
+  const uint32_t bar_empty = bar_full + kMaxStages * 8;
+  const int NS = L.stages;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int G = a.group;
 
   if (tid == 0) {
-    for (int st = 0; st < C::kStages; ++st) {
+    for (int st = 0; st < NS; ++st) {
       mbar_init(bar_full + st * 8, 1);
-      mbar_init(bar_empty + st * 8, 1);
+      mbar_init(bar_empty + st * 8, Hkv);  // one arrival per kv head's warp
     }
     misc[0] = 0;  // abort flag
     fence_mbar_init();
@@ -289,21 +299,20 @@ __global__ void __launch_bounds__(kThreads, 1)
     int incl = local;
 #pragma unroll
     for (int off = 1; off < 32; off <<= 1) {
-      int v = __shfl_up_sync(0xffffffffu, incl, off);
+      const int v = __shfl_up_sync(0xffffffffu, incl, off);
       if (lane >= off) incl += v;
     }
-    if (lane == 31) misc[8 + warp] = incl;
+    if (lane == 31) misc[4 + warp] = incl;
     __syncthreads();
-    int warp_base = 0;
-    for (int w = 0; w < warp; ++w) warp_base += misc[8 + w];
-    int run = warp_base + incl - local;
+    int run = incl - local;
+    for (int w = 0; w < warp; ++w) run += misc[4 + w];
     for (int s = s0; s < s1; ++s) {
       pre[s] = run;
       run += (load_len(a, s, false) + kBlockSize - 1) / kBlockSize;
     }
     if (tid == kThreads - 1) pre[S] = run;
     __syncthreads();
-    cur.W = static_cast<long long>(a.num_kv_heads) * pre[S];
+    cur.W = pre[S];
     cur.C = static_cast<int>(cur.W < gridDim.x ? cur.W : gridDim.x);
     if (static_cast<int>(blockIdx.x) < cur.C) {
       cur.lo = static_cast<long long>(blockIdx.x) * cur.W / cur.C;
@@ -314,7 +323,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     cur.idx = cur.lo;
   } else {
     cur.u = blockIdx.x;
-    cur.U = static_cast<long long>(a.num_seqs) * a.max_parts * a.num_kv_heads;
+    cur.U = static_cast<long long>(a.num_seqs) * a.max_parts;
     __syncthreads();
   }
 
@@ -326,42 +335,41 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     const uint64_t pol = l2_policy_evict_first();
     ChunkIter it{cur, Piece{}, 0, false};
-    int s, kvh, jb, n;
-    bool have = next_chunk(a, pre, it, s, kvh, jb, n);
+    int s, jb, n;
+    bool have = next_chunk(a, pre, it, s, jb, n);
     int ids = have ? load_ids(a, s, jb, n, lane) : 0;
     uint32_t g = 0;
     bool ok = true;
     while (have && ok) {
-      int s2, kvh2, jb2, n2;
-      const bool have2 = next_chunk(a, pre, it, s2, kvh2, jb2, n2);
+      int s2, jb2, n2;
+      const bool have2 = next_chunk(a, pre, it, s2, jb2, n2);
       const int ids2 = have2 ? load_ids(a, s2, jb2, n2, lane) : 0;
       for (int i = 0; i < n; ++i, ++g) {
         const int blk = __shfl_sync(0xffffffffu, ids, i);
-        if (lane == 0 && ok) {
-          const uint32_t st = g % C::kStages;
-          if (g >= static_cast<uint32_t>(C::kStages) &&
-              !mbar_wait(bar_empty + st * 8, ((g / C::kStages) - 1) & 1)) {
+        const uint32_t st = g % NS;
+        const uint32_t fb = bar_full + st * 8;
+        if (lane == 0) {
+          if (g >= static_cast<uint32_t>(NS) && !mbar_wait(bar_empty + st * 8, ((g / NS) - 1) & 1)) {
             atomicOr(a.err, PA_DEVERR_TIMEOUT);
-            *reinterpret_cast<volatile int*>(misc) = 1;
             ok = false;
           } else {
-            const uint32_t fb = bar_full + st * 8;
-            mbar_arrive_expect_tx(fb, C::kStageBytes);
-            const uint32_t kdst = sbase + C::kStageOff + st * C::kStageBytes;
-            const uint32_t vdst = kdst + C::kKBytes;
-            const int z = blk * kBlockSize;
-#pragma unroll
-            for (int h = 0; h < C::kHalves; ++h) {
-              tma_load_3d(kdst + h * kBoxBytes, &tm_k, h * 64, kvh, z, fb, pol);
-              tma_load_3d(vdst + h * kBoxBytes, &tm_v, h * 64, kvh, z, fb, pol);
-            }
+            mbar_arrive_expect_tx(fb, L.stage_bytes);
           }
         }
         ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
         if (!ok) break;
+        if (lane < Hkv) {
+          const uint32_t kdst = sbase + st * L.stage_bytes + lane * L.head_bytes;
+          const uint32_t vdst = kdst + Hkv * L.head_bytes;
+          const int z = blk * kBlockSize;
+#pragma unroll
+          for (int h = 0; h < D / 64; ++h) {
+            tma_load_3d(kdst + h * kBoxBytes, &tm_k, h * 64, lane, z, fb, pol);
+            tma_load_3d(vdst + h * kBoxBytes, &tm_v, h * 64, lane, z, fb, pol);
+          }
+        }
       }
       s = s2;
-      kvh = kvh2;
       jb = jb2;
       n = n2;
       ids = ids2;
@@ -371,36 +379,37 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 
   // -------------------------------------------------------------- consumers
-  constexpr int KS = D / 16;
-  const int ctid = tid;  // 0..127
+  const int ctid = tid;  // 0..255
   if (a.mode == kModeBalanced) {
     // sequences without tokens produce out = 0, lse = -inf
     for (int s = blockIdx.x; s < a.num_seqs; s += gridDim.x) {
       if (load_len(a, s, ctid == 0) != 0) continue;
-      for (int e = ctid; e < a.num_q_heads * D; e += kConsumerWarps * 32)
+      for (int e = ctid; e < a.num_q_heads * D; e += kConsumerThreads)
         a.out[static_cast<long long>(s) * a.num_q_heads * D + e] = __float2bfloat16(0.f);
       if (a.out_lse)
-        for (int h = ctid; h < a.num_q_heads; h += kConsumerWarps * 32)
+        for (int h = ctid; h < a.num_q_heads; h += kConsumerThreads)
           a.out_lse[static_cast<long long>(s) * a.num_q_heads + h] = -INFINITY;
     }
   }
 
-  // After a timeout every consumer warp keeps walking its pieces (skipping
-  // the waits and the math) so that all of them still meet at each named
-  // barrier; nothing waits without a bound.
+  const bool active = warp < Hkv * wph;
+  const int hw = warp % Hkv;  // this warp's kv head
+  const int sub = warp / Hkv; // which of the head's warps
+  const int q4 = lane & 3;
+  const int d0 = lane >> 2;
   volatile int* abort_flag = misc;
   Piece pc;
   uint32_t g = 0;
   while (next_piece(a, pre, cur, pc, ctid == 0)) {
     // query fragments of the group: B operand (k = dim, n = head)
     uint32_t qf[KS][2];
-    {
-      const int hq = lane >> 2;
-      const __nv_bfloat16* qrow =
-          a.q + (static_cast<long long>(pc.s) * a.num_q_heads + pc.kvh * G + hq) * D;
+    const int hq = lane >> 2;
+    const long long head0 = static_cast<long long>(pc.s) * a.num_q_heads + hw * G;
+    if (active) {
+      const __nv_bfloat16* qrow = a.q + (head0 + hq) * D;
 #pragma unroll
       for (int ks = 0; ks < KS; ++ks) {
-        const int c = ks * 16 + (lane & 3) * 2;
+        const int c = ks * 16 + q4 * 2;
         qf[ks][0] = hq < G ? *reinterpret_cast<const uint32_t*>(qrow + c) : 0u;
         qf[ks][1] = hq < G ? *reinterpret_cast<const uint32_t*>(qrow + c + 8) : 0u;
       }
@@ -410,148 +419,266 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int mt = 0; mt < KS; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
     float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
 
-    for (int j = pc.j0; j < pc.j1; ++j, ++g) {
-      if (static_cast<int>(g & (kConsumerWarps - 1)) != warp) continue;
-      if (*abort_flag) continue;
-      const uint32_t st = g % C::kStages;
-      if (!mbar_wait(bar_full + st * 8, (g / C::kStages) & 1)) {
-        atomicOr(a.err, PA_DEVERR_TIMEOUT);
-        *abort_flag = 1;
-        continue;
+    if (active) {
+      for (int j = pc.j0; j < pc.j1; ++j, ++g) {
+        if (static_cast<int>(g % wph) != sub) continue;
+        if (*abort_flag) continue;
+        const uint32_t st = g % NS;
+        if (!mbar_wait(bar_full + st * 8, (g / NS) & 1)) {
+          atomicOr(a.err, PA_DEVERR_TIMEOUT);
+          *abort_flag = 1;
+          continue;
+        }
+        const int valid = min(kBlockSize, pc.len - j * kBlockSize);
+        const uint32_t kb = sbase + st * L.stage_bytes + hw * L.head_bytes;
+        attend_block<D>(kb, kb + Hkv * L.head_bytes, qf, o, m0, m1, l0, l1, valid,
+                        a.scale_log2, lane);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar_empty + st * 8);
       }
-      const int valid = min(kBlockSize, pc.len - j * kBlockSize);
-      const uint32_t kb = sbase + C::kStageOff + st * C::kStageBytes;
-      attend_block<D>(kb, kb + C::kKBytes, qf, o, m0, m1, l0, l1, valid, a.scale_log2, lane);
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar_empty + st * 8);
+    } else {
+      g += pc.j1 - pc.j0;
     }
 
-    // ---- merge the 4 warps' running states
+    // ---- per-head result of this piece: normalized o and lse (log2 units)
 #pragma unroll
     for (int off = 4; off < 32; off <<= 1) {
       l0 += __shfl_xor_sync(0xffffffffu, l0, off);
       l1 += __shfl_xor_sync(0xffffffffu, l1, off);
     }
-    const int q4 = lane & 3;
-    if (lane < 4) {
-      mlbuf[(warp * kMaxGroup + 2 * q4) * 2 + 0] = m0;
-      mlbuf[(warp * kMaxGroup + 2 * q4) * 2 + 1] = l0;
-      mlbuf[(warp * kMaxGroup + 2 * q4 + 1) * 2 + 0] = m1;
-      mlbuf[(warp * kMaxGroup + 2 * q4 + 1) * 2 + 1] = l1;
-    }
-    named_barrier(1, kConsumerWarps * 32);
-    float fa, fb;
-    {
-      float f[2];
+    float fa, fb, lsea, lseb;  // scale applied to this warp's O, and the head's lse
+    if (wph > 1) {
+      // several warps share the head: merge their (m, l, O) through smem
+      if (active && lane < 4) {
+        mlbuf[(warp * kMaxGroup + 2 * q4) * 2 + 0] = m0;
+        mlbuf[(warp * kMaxGroup + 2 * q4) * 2 + 1] = l0;
+        mlbuf[(warp * kMaxGroup + 2 * q4 + 1) * 2 + 0] = m1;
+        mlbuf[(warp * kMaxGroup + 2 * q4 + 1) * 2 + 1] = l1;
+      }
+      named_barrier(1, kConsumerThreads);
+      float f[2], ls[2];
 #pragma unroll
       for (int k = 0; k < 2; ++k) {
         const int h = 2 * q4 + k;
         float M = -INFINITY;
-#pragma unroll
-        for (int w = 0; w < kConsumerWarps; ++w) M = fmaxf(M, mlbuf[(w * kMaxGroup + h) * 2]);
-        float L = 0.f;
-        if (M != -INFINITY) {
-#pragma unroll
-          for (int w = 0; w < kConsumerWarps; ++w)
-            L += mlbuf[(w * kMaxGroup + h) * 2 + 1] *
-                 fast_exp2(mlbuf[(w * kMaxGroup + h) * 2] - M);
-        }
+        for (int w2 = 0; w2 < wph; ++w2)
+          M = fmaxf(M, mlbuf[((w2 * Hkv + hw) * kMaxGroup + h) * 2]);
+        float Ls = 0.f;
+        if (M != -INFINITY)
+          for (int w2 = 0; w2 < wph; ++w2)
+            Ls += mlbuf[((w2 * Hkv + hw) * kMaxGroup + h) * 2 + 1] *
+                  fast_exp2(mlbuf[((w2 * Hkv + hw) * kMaxGroup + h) * 2] - M);
         const float mine = k == 0 ? m0 : m1;
-        f[k] = L > 0.f ? fast_exp2(mine - M) / L : 0.f;
-        if (warp == 0 && lane < 4)
-          lsebuf[h] = L > 0.f ? (M + __log2f(L)) * kLn2 : -INFINITY;
+        f[k] = Ls > 0.f ? fast_exp2(mine - M) / Ls : 0.f;
+        ls[k] = Ls > 0.f ? (M + __log2f(Ls)) * kLn2 : -INFINITY;
       }
       fa = f[0];
       fb = f[1];
-    }
-    {
-      const int d0 = lane >> 2;
-      float* ob = obuf + warp * kMaxGroup * C::kObufStride;
+      lsea = ls[0];
+      lseb = ls[1];
+      if (active) {
+        float* ob = obuf + warp * kMaxGroup * (D + 4);
+#pragma unroll
+        for (int mt = 0; mt < KS; ++mt) {
+          const int d = mt * 16 + d0;
+          ob[(2 * q4) * (D + 4) + d] = o[mt][0] * fa;
+          ob[(2 * q4 + 1) * (D + 4) + d] = o[mt][1] * fb;
+          ob[(2 * q4) * (D + 4) + d + 8] = o[mt][2] * fa;
+          ob[(2 * q4 + 1) * (D + 4) + d + 8] = o[mt][3] * fb;
+        }
+      }
+      named_barrier(1, kConsumerThreads);
+      // the head's first warp sums its partners' contributions into registers
+      if (active && sub == 0) {
+#pragma unroll
+        for (int mt = 0; mt < KS; ++mt) {
+          const int d = mt * 16 + d0;
+          float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
+          for (int w2 = 0; w2 < wph; ++w2) {
+            const float* ob = obuf + (w2 * Hkv + hw) * kMaxGroup * (D + 4);
+            s0 += ob[(2 * q4) * (D + 4) + d];
+            s1 += ob[(2 * q4 + 1) * (D + 4) + d];
+            s2 += ob[(2 * q4) * (D + 4) + d + 8];
+            s3 += ob[(2 * q4 + 1) * (D + 4) + d + 8];
+          }
+          o[mt][0] = s0;
+          o[mt][1] = s1;
+          o[mt][2] = s2;
+          o[mt][3] = s3;
+        }
+      }
+      named_barrier(1, kConsumerThreads);
+    } else {
+      fa = l0 > 0.f ? 1.f / l0 : 0.f;
+      fb = l1 > 0.f ? 1.f / l1 : 0.f;
+      lsea = l0 > 0.f ? (m0 + __log2f(l0)) * kLn2 : -INFINITY;
+      lseb = l1 > 0.f ? (m1 + __log2f(l1)) * kLn2 : -INFINITY;
 #pragma unroll
       for (int mt = 0; mt < KS; ++mt) {
-        const int d = mt * 16 + d0;
-        ob[(2 * q4) * C::kObufStride + d] = o[mt][0] * fa;
-        ob[(2 * q4 + 1) * C::kObufStride + d] = o[mt][1] * fb;
-        ob[(2 * q4) * C::kObufStride + d + 8] = o[mt][2] * fa;
-        ob[(2 * q4 + 1) * C::kObufStride + d + 8] = o[mt][3] * fb;
+        o[mt][0] *= fa;
+        o[mt][1] *= fb;
+        o[mt][2] *= fa;
+        o[mt][3] *= fb;
       }
     }
-    named_barrier(1, kConsumerWarps * 32);
-
-    const long long head0 = static_cast<long long>(pc.s) * a.num_q_heads + pc.kvh * G;
-    if (pc.kind == kFinal || pc.kind == kPartialFixed) {
-      for (int e = ctid; e < G * D; e += kConsumerWarps * 32) {
-        const int h = e / D, d = e % D;
-        float v = 0.f;
+    // lanes own o^T[d = mt*16 + d0 (+8)][head 2*q4 (+1)] of kv head hw
+    const bool writer = active && sub == 0;
+    const int ha = 2 * q4, hb = 2 * q4 + 1;
+    if (pc.kind == kFinal) {
+      if (writer) {
 #pragma unroll
-        for (int w = 0; w < kConsumerWarps; ++w)
-          v += obuf[(w * kMaxGroup + h) * C::kObufStride + d];
-        if (pc.kind == kFinal) {
-          a.out[(head0 + h) * D + d] = __float2bfloat16(v);
-          if (d == 0 && a.out_lse) a.out_lse[head0 + h] = lsebuf[h];
-        } else {
-          const long long row = (head0 + h) * a.max_parts + pc.part;
-          a.part_o[row * D + d] = v;
-          if (d == 0) a.part_lse[row] = lsebuf[h];
+        for (int mt = 0; mt < KS; ++mt) {
+          const int d = mt * 16 + d0;
+          if (ha < G) {
+            a.out[(head0 + ha) * D + d] = __float2bfloat16(o[mt][0]);
+            a.out[(head0 + ha) * D + d + 8] = __float2bfloat16(o[mt][2]);
+          }
+          if (hb < G) {
+            a.out[(head0 + hb) * D + d] = __float2bfloat16(o[mt][1]);
+            a.out[(head0 + hb) * D + d + 8] = __float2bfloat16(o[mt][3]);
+          }
+        }
+        if (a.out_lse && d0 == 0) {
+          if (ha < G) a.out_lse[head0 + ha] = lsea;
+          if (hb < G) a.out_lse[head0 + hb] = lseb;
+        }
+      }
+    } else if (pc.kind == kPartialFixed) {
+      if (writer) {
+#pragma unroll
+        for (int mt = 0; mt < KS; ++mt) {
+          const int d = mt * 16 + d0;
+          if (ha < G) {
+            const long long row = (head0 + ha) * a.max_parts + pc.part;
+            a.part_o[row * D + d] = o[mt][0];
+            a.part_o[row * D + d + 8] = o[mt][2];
+            if (mt == 0 && d0 == 0) a.part_lse[row] = lsea;
+          }
+          if (hb < G) {
+            const long long row = (head0 + hb) * a.max_parts + pc.part;
+            a.part_o[row * D + d] = o[mt][1];
+            a.part_o[row * D + d + 8] = o[mt][3];
+            if (mt == 0 && d0 == 0) a.part_lse[row] = lseb;
+          }
         }
       }
     } else {
-      // balanced partial: publish to this CTA's slot, then the last of the
-      // segment's pieces merges them all
+      // balanced partial: publish to this CTA's slot [Hq][D] + lse[Hq], then the
+      // last of the sequence's pieces merges them all
+      const int Hq = a.num_q_heads;
       float* slot = a.part_o + (static_cast<long long>(blockIdx.x) * 2 + pc.which) * a.slot_floats;
-      for (int e = ctid; e < G * D; e += kConsumerWarps * 32) {
-        const int h = e / D, d = e % D;
-        float v = 0.f;
+      if (writer) {
+        const int hga = hw * G + ha, hgb = hw * G + hb;
 #pragma unroll
-        for (int w = 0; w < kConsumerWarps; ++w)
-          v += obuf[(w * kMaxGroup + h) * C::kObufStride + d];
-        slot[e] = v;
-        if (d == 0) slot[G * D + h] = lsebuf[h];
+        for (int mt = 0; mt < KS; ++mt) {
+          const int d = mt * 16 + d0;
+          if (ha < G) {
+            slot[hga * D + d] = o[mt][0];
+            slot[hga * D + d + 8] = o[mt][2];
+          }
+          if (hb < G) {
+            slot[hgb * D + d] = o[mt][1];
+            slot[hgb * D + d + 8] = o[mt][3];
+          }
+        }
+        if (d0 == 0) {
+          if (ha < G) slot[Hq * D + hga] = lsea;
+          if (hb < G) slot[Hq * D + hgb] = lseb;
+        }
       }
       __threadfence();
-      named_barrier(1, kConsumerWarps * 32);
+      named_barrier(1, kConsumerThreads);
       const long long c_first = cta_of(pc.seg_start, cur.W, cur.C);
       const long long c_last = cta_of(pc.seg_start + pc.nb - 1, cur.W, cur.C);
       const int npieces = static_cast<int>(c_last - c_first + 1);
       if (ctid == 0) misc[1] = atomicAdd(a.counters + c_first, 1);
-      named_barrier(1, kConsumerWarps * 32);
+      named_barrier(1, kConsumerThreads);
       if (misc[1] == npieces - 1) {
         __threadfence();
-        for (int e = ctid; e < G * D; e += kConsumerWarps * 32) {
-          const int h = e / D, d = e % D;
-          float L = -INFINITY;
+        // a running log-sum-exp per float4 group over the pieces; a thread's
+        // loads of one piece are independent, so each piece costs about one
+        // L2 round trip per batch of groups
+        constexpr int kNI = 4;  // float4 groups per thread per batch
+        const int nf = Hq * D / 4;  // float4 groups of the sequence's output
+        const long long row0 = static_cast<long long>(pc.s) * Hq;
+        for (int fb0 = 0; fb0 < nf; fb0 += kNI * kConsumerThreads) {
+          float4 acc[kNI];
+          float mrun[kNI], wsum[kNI];
+#pragma unroll
+          for (int i = 0; i < kNI; ++i) {
+            acc[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+            mrun[i] = -INFINITY;
+            wsum[i] = 0.f;
+          }
+#pragma unroll 1
           for (int k = 0; k < npieces; ++k) {
             const float* sl = a.part_o + ((c_first + k) * 2 + (k == 0 ? 1 : 0)) * a.slot_floats;
-            L = fmaxf(L, __ldcg(sl + G * D + h));
-          }
-          float wsum = 0.f, acc = 0.f;
-          if (L != -INFINITY) {
-            for (int k = 0; k < npieces; ++k) {
-              const float* sl = a.part_o + ((c_first + k) * 2 + (k == 0 ? 1 : 0)) * a.slot_floats;
-              const float w = __expf(__ldcg(sl + G * D + h) - L);
-              wsum += w;
-              acc += w * __ldcg(sl + e);
+            float lk[kNI];
+            float4 ok[kNI];
+#pragma unroll
+            for (int i = 0; i < kNI; ++i) {
+              const int f = fb0 + ctid + i * kConsumerThreads;
+              if (f < nf) {
+                lk[i] = __ldcg(sl + Hq * D + (f * 4) / D);
+                ok[i] = __ldcg(reinterpret_cast<const float4*>(sl) + f);
+              }
+            }
+#pragma unroll
+            for (int i = 0; i < kNI; ++i) {
+              const int f = fb0 + ctid + i * kConsumerThreads;
+              if (f < nf && lk[i] != -INFINITY) {
+                const float mn = fmaxf(mrun[i], lk[i]);
+                const float sc = __expf(mrun[i] - mn), w = __expf(lk[i] - mn);
+                acc[i].x = acc[i].x * sc + w * ok[i].x;
+                acc[i].y = acc[i].y * sc + w * ok[i].y;
+                acc[i].z = acc[i].z * sc + w * ok[i].z;
+                acc[i].w = acc[i].w * sc + w * ok[i].w;
+                wsum[i] = wsum[i] * sc + w;
+                mrun[i] = mn;
+              }
             }
           }
-          a.out[(head0 + h) * D + d] = __float2bfloat16(wsum > 0.f ? acc / wsum : 0.f);
-          if (d == 0 && a.out_lse) a.out_lse[head0 + h] = wsum > 0.f ? L + __logf(wsum) : -INFINITY;
+#pragma unroll
+          for (int i = 0; i < kNI; ++i) {
+            const int f = fb0 + ctid + i * kConsumerThreads;
+            if (f < nf) {
+              const float inv = wsum[i] > 0.f ? 1.f / wsum[i] : 0.f;
+              const uint2 pk = make_uint2(pack_bf16x2(acc[i].x * inv, acc[i].y * inv),
+                                          pack_bf16x2(acc[i].z * inv, acc[i].w * inv));
+              *reinterpret_cast<uint2*>(a.out + row0 * D + static_cast<long long>(f) * 4) = pk;
+              if ((f * 4) % D == 0 && a.out_lse)
+                a.out_lse[row0 + (f * 4) / D] =
+                    wsum[i] > 0.f ? mrun[i] + __logf(wsum[i]) : -INFINITY;
+            }
+          }
         }
         if (ctid == 0) a.counters[c_first] = 0;
       }
+      named_barrier(1, kConsumerThreads);
     }
   }
 }
 
+int warps_per_head(int Hkv) { return Hkv >= kConsumerWarps ? 1 : kConsumerWarps / Hkv; }
+
+int pick_stages(int D, int Hkv, int pre_ints) {
+  const int wph = warps_per_head(Hkv);
+  const int budget = 227 * 1024 - 1024;  // minus alignment slack
+  int st = kMaxStages;
+  while (st > 2 && make_layout(D, Hkv, wph, st, pre_ints).total > budget) --st;
+  return st;
+}
+
 }  // namespace
 
-size_t balanced_slot_floats(int group, int head_dim) {
-  const size_t f = static_cast<size_t>(group) * head_dim + group;
+size_t balanced_slot_floats(int num_q_heads, int head_dim) {
+  const size_t f = static_cast<size_t>(num_q_heads) * (head_dim + 1);
   return (f + 63) / 64 * 64;
 }
 
-size_t balanced_workspace_bytes(int grid, int group, int head_dim) {
+size_t balanced_workspace_bytes(int grid, int num_q_heads, int head_dim) {
   const size_t counters = (static_cast<size_t>(grid) * 4 + 255) / 256 * 256;
-  return counters + static_cast<size_t>(grid) * 2 * balanced_slot_floats(group, head_dim) * 4;
+  return counters + static_cast<size_t>(grid) * 2 * balanced_slot_floats(num_q_heads, head_dim) * 4;
 }
 
 int decode_grid(int num_sms, int mode) {
@@ -559,15 +686,20 @@ int decode_grid(int num_sms, int mode) {
   return num_sms;
 }
 
-size_t decode_smem_bytes(int head_dim, int mode, int num_seqs) {
-  const size_t pre = mode == kModeBalanced ? static_cast<size_t>(num_seqs + 1) * 4 : 0;
-  const size_t fixed = head_dim == 128 ? Cfg<128>::kPreOff : Cfg<64>::kPreOff;
-  return fixed + pre + 1024;
+bool decode_supported(int head_dim, int num_kv_heads, int mode, int num_seqs) {
+  if (num_kv_heads > kConsumerWarps) return false;
+  const int pre = mode == kModeBalanced ? num_seqs + 1 : 0;
+  const int wph = warps_per_head(num_kv_heads);
+  return make_layout(head_dim, num_kv_heads, wph, 2, pre).total <= 227 * 1024 - 1024;
 }
 
-cudaError_t launch_decode(const DecodeArgs& a, const CUtensorMap* tm_k, const CUtensorMap* tm_v,
+cudaError_t launch_decode(DecodeArgs a, const CUtensorMap* tm_k, const CUtensorMap* tm_v,
                           int head_dim, int grid, cudaStream_t stream) {
-  const size_t smem = decode_smem_bytes(head_dim, a.mode, a.num_seqs);
+  const int pre = a.mode == kModeBalanced ? a.num_seqs + 1 : 0;
+  a.warps_per_head = warps_per_head(a.num_kv_heads);
+  a.stages = pick_stages(head_dim, a.num_kv_heads, pre);
+  const size_t smem =
+      make_layout(head_dim, a.num_kv_heads, a.warps_per_head, a.stages, pre).total + 1024;
   cudaError_t e;
   if (head_dim == 128) {
     e = cudaFuncSetAttribute(decode_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,

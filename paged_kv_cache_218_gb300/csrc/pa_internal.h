@@ -40,6 +40,8 @@ struct DecodeArgs {
   int part_blocks;   // fixed split / single pass: blocks per partition
   int max_parts;     // fixed split: P_max
   int slot_floats;   // balanced: floats per partial slot
+  int warps_per_head;  // set by the launcher
+  int stages;          // set by the launcher
 };
 
 struct MergeArgs {
@@ -76,15 +78,16 @@ struct PrefillArgs {
   float scale_log2;
 };
 
-// Balanced-mode workspace layout (shared by the size query and the launch).
-size_t balanced_slot_floats(int group, int head_dim);
-size_t balanced_workspace_bytes(int grid, int group, int head_dim);
+// Balanced-mode workspace layout (shared by the size query and the launch):
+// per-CTA merge tickets, then two partial slots per CTA of Hq*(D+1) floats.
+size_t balanced_slot_floats(int num_q_heads, int head_dim);
+size_t balanced_workspace_bytes(int grid, int num_q_heads, int head_dim);
 
 // Kernel launchers (return cudaError_t of the launch).
-cudaError_t launch_decode(const DecodeArgs& a, const CUtensorMap* tm_k, const CUtensorMap* tm_v,
+cudaError_t launch_decode(DecodeArgs a, const CUtensorMap* tm_k, const CUtensorMap* tm_v,
                           int head_dim, int grid, cudaStream_t stream);
 int decode_grid(int num_sms, int mode);
-size_t decode_smem_bytes(int head_dim, int mode, int num_seqs);
+bool decode_supported(int head_dim, int num_kv_heads, int mode, int num_seqs);
 cudaError_t launch_merge(const MergeArgs& a, cudaStream_t stream);
 cudaError_t launch_prefill(const PrefillArgs& a, const CUtensorMap* tm_q, const CUtensorMap* tm_k,
                            const CUtensorMap* tm_v, int grid_tiles, cudaStream_t stream);

@@ -171,6 +171,8 @@ EDGE = [
     (9, 1, 300, 12, 4, 128, 4),    # group 3 (padded MMA columns)
     (3, 1, 40, 7, 1, 64, 5),       # group 7, one kv head
     (33, 500, 3000, 32, 8, 128, 6),
+    (6, 1, 100, 6, 3, 128, 7),     # three kv heads: two warps per head, two warps idle
+    (4, 20, 90, 10, 5, 64, 8),     # five kv heads: one warp per head, three idle
 ]
 
 

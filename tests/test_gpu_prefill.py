@@ -1,0 +1,163 @@
+"""GPU parity of the tcgen05 causal prefill chunk and of the Sarathi hybrid
+step (chunk + decodes under one token budget) against the fp64 oracle."""
+import functools
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from paged_kv_cache_218_gb300 import workload as W
+from tests.gpu_common import DeviceWorkload, assert_close, oracle_scattered
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def pa(cuda_device):
+    from paged_kv_cache_218_gb300 import binding
+    binding.pa_device_error_flags(reset=True)
+    return binding
+
+
+def _prefill(pa, dw, with_lse=True, stream=None):
+    w = dw.w
+    C = w.num_chunks
+    T = int(w.cu_q_lens[C])
+    q = dw.q[:T]
+    out = torch.full((T, w.num_q_heads, w.head_dim), float("nan"), dtype=torch.bfloat16,
+                     device=q.device)
+    lse = torch.full((T, w.num_q_heads), float("nan"), dtype=torch.float32, device=q.device) \
+        if with_lse else None
+    max_q = int(np.max(np.diff(w.cu_q_lens)))
+    dev = q.device
+    pa.pa_prefill_chunk(out, q, dw.k_cache, dw.v_cache, dw.block_tables[:C],
+                        torch.from_numpy(w.cu_q_lens).to(dev),
+                        torch.from_numpy(w.q_start_pos).to(dev), dw.seq_lens[:C], max_q,
+                        w.scale, out_lse=lse, stream=stream)
+    return out, lse
+
+
+def _oracle_prefill(w):
+    kc, vc = oracle_scattered(w)
+    C = w.num_chunks
+    T = int(w.cu_q_lens[C])
+    return oracle.prefill(w.q[:T], kc, vc, w.block_tables[:C], w.cu_q_lens, w.q_start_pos,
+                          w.seq_lens[:C], w.scale)
+
+
+CHUNKS = [
+    # (chunks [(start, len)], Hq, Hkv, seed)
+    ([(0, 40)], 8, 2, 1),                                # one chunk from position 0, group 4
+    ([(0, 37), (40, 25), (7, 1), (100, 130)], 8, 2, 2),  # ragged starts and lengths
+    ([(0, 128), (128, 128)], 8, 8, 3),                   # group 1: 128 tokens per tile
+    ([(5, 77), (300, 19)], 16, 8, 4),                    # group 2
+    ([(33, 200), (0, 16), (250, 3)], 32, 4, 5),          # group 8: 16 tokens per tile
+    ([(1000, 300)], 16, 4, 6),                           # long prefix, several key tiles
+]
+
+
+@pytest.mark.parametrize("chunks,Hq,Hkv,seed", CHUNKS)
+def test_prefill_chunks_match_oracle(pa, cuda_device, chunks, Hq, Hkv, seed):
+    w = W.prefill_batch(chunks, Hq=Hq, Hkv=Hkv, D=128, seed=700 + seed, poison=True)
+    dw = DeviceWorkload(w, cuda_device)
+    dw.scatter(pa)
+    out, lse = _prefill(pa, dw)
+    torch.cuda.synchronize()
+    ref, ref_lse = _oracle_prefill(w)
+    assert torch.isfinite(out).all()
+    assert_close(out, ref, f"prefill {chunks} G={Hq // Hkv}")
+    assert_close(lse.cpu().numpy(), ref_lse, "prefill lse")
+    assert pa.pa_device_error_flags() == 0
+
+
+@functools.lru_cache(maxsize=None)
+def _hybrid():
+    w = W.sarathi_hybrid()
+    kc, vc = oracle_scattered(w)
+    ref_c, ref_c_lse = oracle.prefill(w.chunk_q, kc, vc, w.block_tables[:1], w.cu_q_lens,
+                                      w.q_start_pos, w.seq_lens[:1], w.scale)
+    ref_d, _ = oracle.decode(w.decode_q, kc, vc, w.decode_block_tables, w.decode_seq_lens,
+                             w.scale)
+    return w, ref_c, ref_c_lse, ref_d
+
+
+def test_sarathi_chunk_matches_oracle(pa, cuda_device):
+    w, ref_c, ref_c_lse, _ = _hybrid()
+    dw = DeviceWorkload(w, cuda_device)
+    dw.scatter(pa)
+    out, lse = _prefill(pa, dw)
+    torch.cuda.synchronize()
+    assert_close(out, ref_c, "sarathi chunk")
+    assert_close(lse.cpu().numpy(), ref_c_lse, "sarathi chunk lse")
+
+
+def test_sarathi_hybrid_step_on_two_streams(pa, cuda_device):
+    """Scatter the 640 new tokens, then run the chunk and the 128 decodes
+    concurrently on two streams; both results match the oracle."""
+    w, ref_c, _, ref_d = _hybrid()
+    dw = DeviceWorkload(w, cuda_device)
+    main = torch.cuda.current_stream()
+    s_chunk, s_dec = torch.cuda.Stream(), torch.cuda.Stream()
+    dw.scatter(pa)
+    ready = torch.cuda.Event()
+    ready.record(main)
+    s_chunk.wait_event(ready)
+    s_dec.wait_event(ready)
+    S, Hq, D = w.num_decode_seqs, w.num_q_heads, w.head_dim
+    out_d = torch.empty((S, Hq, D), dtype=torch.bfloat16, device=cuda_device)
+    ws = pa.alloc_workspace(pa.pa_decode_workspace_size(S, Hq, w.num_kv_heads, D,
+                                                        w.max_blocks_per_seq, 16, 0),
+                            cuda_device)
+    with torch.cuda.stream(s_chunk):
+        out_c, _ = _prefill(pa, dw, with_lse=False, stream=s_chunk)
+    with torch.cuda.stream(s_dec):
+        pa.pa_decode(out_d, dw.dq, dw.k_cache, dw.v_cache, dw.dtables, dw.dlens, w.scale,
+                     partition_tokens=0, workspace=ws, stream=s_dec)
+    main.wait_stream(s_chunk)
+    main.wait_stream(s_dec)
+    torch.cuda.synchronize()
+    assert_close(out_c, ref_c, "hybrid chunk")
+    assert_close(out_d, ref_d, "hybrid decode")
+    assert pa.pa_device_error_flags() == 0
+
+
+def test_prefill_query_equals_decode_of_its_prefix(pa, cuda_device):
+    """The chunk's query at position p and a decode with seq_len p + 1 over the
+    same cache agree (two different kernels)."""
+    w = W.prefill_batch([(50, 60)], Hq=8, Hkv=2, D=128, seed=41)
+    dw = DeviceWorkload(w, cuda_device)
+    dw.scatter(pa)
+    out, _ = _prefill(pa, dw, with_lse=False)
+    rows = [0, 17, 59]
+    q = dw.q[rows]
+    lens = torch.tensor([50 + r + 1 for r in rows], dtype=torch.int32, device=cuda_device)
+    tables = dw.block_tables[[0, 0, 0]]
+    out_d = torch.empty((3, 8, 128), dtype=torch.bfloat16, device=cuda_device)
+    pa.pa_decode(out_d, q, dw.k_cache, dw.v_cache, tables, lens, w.scale, partition_tokens=-1)
+    torch.cuda.synchronize()
+    diff = (out[rows].float() - out_d.float()).abs().max().item()
+    assert diff <= 2e-2
+
+
+def test_prefill_flags_inconsistent_chunks(pa, cuda_device):
+    w = W.prefill_batch([(0, 20), (10, 20)], Hq=8, Hkv=2, D=128, seed=9)
+    dw = DeviceWorkload(w, cuda_device)
+    dw.scatter(pa)
+    bad_start = w.q_start_pos.copy()
+    bad_start[1] = 25  # 25 + 20 > seq_len 30
+    w2 = W.Workload(**{**w.__dict__, "q_start_pos": bad_start})
+    dw.w = w2
+    out, _ = _prefill(pa, dw, with_lse=False)
+    torch.cuda.synchronize()
+    assert pa.pa_device_error_flags() & pa.PA_DEVERR_CHUNK
+    ref, _ = _oracle_prefill(w)
+    assert_close(out[:20], ref[:20], "good chunk beside a bad one")
+
+
+def test_prefill_rejects_unsupported_shapes(pa, cuda_device):
+    w = W.prefill_batch([(0, 20)], Hq=6, Hkv=2, D=128, seed=10)  # group 3 does not tile 128 rows
+    dw = DeviceWorkload(w, cuda_device)
+    with pytest.raises(pa.PAError) as e:
+        _prefill(pa, dw)
+    assert e.value.status == pa.PA_ERR_UNSUPPORTED
