@@ -60,18 +60,23 @@ def load_peaks():
         return FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS, "fallback"
 
 
-def profile_traffic(kernel_file: str, summary: str):
+def source_hash(files):
+    h = hashlib.sha256()
+    for f in files:
+        h.update(open(os.path.join(ROOT, "paged_kv_cache_218_gb300", "csrc", f), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def profile_traffic(kernel_files, summary: str):
     """Per-launch DRAM bytes recorded by an ncu capture in profiles/, valid only
-    while the kernel source still has the hash the summary was taken at."""
+    while the kernel sources still hash to the value the summary was taken at."""
     try:
-        src = open(os.path.join(ROOT, "paged_kv_cache_218_gb300", "csrc", kernel_file), "rb").read()
-        sha = hashlib.sha256(src).hexdigest()[:16]
         fields = {}
         for line in open(os.path.join(ROOT, "profiles", summary)):
             if ":" in line and line.strip().startswith("- "):
                 k, v = line.strip()[2:].split(":", 1)
                 fields[k.strip()] = v.strip().strip("`")
-        if fields.get("source_sha256_16") != sha:
+        if fields.get("source_sha256_16") != source_hash(kernel_files):
             return None
         return float(fields["traffic_bytes_per_launch"])
     except Exception:
@@ -452,7 +457,8 @@ def main():
     value = kvb * world * K / (res["elapsed_ms"] * 1e-3) / 1e9
     alg = decode_algorithmic_bytes(w)
     achieved = alg / (res["dec_ms"] * 1e-3) / 1e9
-    traffic = profile_traffic("pa_decode.cu", "decode_kernel_llama3_8b_decode_layer.md") \
+    traffic = profile_traffic(["pa_decode.cu", "pa_ptx.cuh", "pa_internal.h"],
+                              "decode_kernel_llama3_8b_decode_layer.md") \
         if args.config == "llama3_8b_decode_layer" else None
     e = res["e2e"]
     line = {
