@@ -58,7 +58,8 @@ typedef enum pa_status {
   PA_ERR_INVALID = -1,     /* bad pointer, size or metadata */
   PA_ERR_UNSUPPORTED = -2, /* valid but not implemented (head_dim, group, block_size) */
   PA_ERR_CUDA = -3,        /* a CUDA runtime call or launch failed */
-  PA_ERR_WORKSPACE = -4    /* workspace missing, too small or misaligned */
+  PA_ERR_WORKSPACE = -4,   /* workspace missing, too small or misaligned */
+  PA_ERR_SCRATCH_LIMIT = -5 /* pa_decode_noalloc: needs more than its static scratch */
 } pa_status;
 
 /* Bits of the device error word. */
@@ -185,6 +186,41 @@ int pa_prefill_chunk(void *out, const void *q, const void *k_cache, const void *
                      const int32_t *seq_lens, int num_chunks, int total_q_tokens, int max_q_len,
                      int num_q_heads, int num_kv_heads, int head_dim, int block_size,
                      int64_t num_blocks, float scale, float *out_lse, void *stream);
+
+/*
+ * Size of the static device scratch behind pa_decode_noalloc (8 MiB).
+ */
+#define PA_NOALLOC_SCRATCH_BYTES (8u << 20)
+
+/*
+ * pa_decode_noalloc -- the balanced decode of pa_decode (partition_tokens = 0)
+ * for callers that cannot allocate device memory.  The paper has no
+ * counterpart: this is a deployment variant of the same computation.
+ *
+ * Who needs it: a serving loop that must not call cudaMalloc on its hot path
+ * (an allocation can synchronize the device and stall every other stream),
+ * an engine whose device memory is reserved up front for the KV pool under a
+ * fixed budget, and plain-C callers with no framework allocator to carve a
+ * workspace from.  This entry point allocates nothing and calls no
+ * allocating routine; the caller still passes every input and output,
+ * exactly as for pa_decode (same arguments, layouts and results).
+ *
+ * Its scratch (the merge tickets and partial results of the balanced split)
+ * is one file-scope device array of PA_NOALLOC_SCRATCH_BYTES inside libpa.so;
+ * every GPU that loads the library holds it until the process exits.  The
+ * first call on a device looks up that array's device address (once per
+ * device, with that device current); make that first call before any stream
+ * capture.  Every call shares the one array and clears its tickets at the
+ * start, so calls that overlap on the GPU (two streams, or two threads) race
+ * and give wrong results: serialize them.  A shape whose scratch need
+ * exceeds the array (more than 32 q heads at head_dim 128 on a 152-SM GB300)
+ * is rejected with PA_ERR_SCRATCH_LIMIT before anything is launched.
+ */
+int pa_decode_noalloc(void *out, const void *q, const void *k_cache, const void *v_cache,
+                      const int32_t *block_tables, int max_blocks_per_seq,
+                      const int32_t *seq_lens, int num_seqs, int num_q_heads, int num_kv_heads,
+                      int head_dim, int block_size, int64_t num_blocks, float scale,
+                      float *out_lse, void *stream);
 
 /*
  * Host-side metadata check (host pointers; any of block_tables / slot_mapping

@@ -26,6 +26,7 @@ PA_ERR_INVALID = -1
 PA_ERR_UNSUPPORTED = -2
 PA_ERR_CUDA = -3
 PA_ERR_WORKSPACE = -4
+PA_ERR_SCRATCH_LIMIT = -5
 PA_DEVERR_BLOCK_ID = 1
 PA_DEVERR_SEQ_LEN = 2
 PA_DEVERR_SLOT = 4
@@ -46,6 +47,7 @@ _SIGS = {
     "pa_decode_workspace_size": ([_I, _I, _I, _I, _I, _I, _I], _S),
     "pa_decode": ([_P, _P, _P, _P, _P, _I, _P, _I, _I, _I, _I, _I, _L, _F, _I, _P, _P, _S, _P], _I),
     "pa_merge_partials": ([_P, _P, _P, _P, _P, _I, _I, _I, _I, _P], _I),
+    "pa_decode_noalloc": ([_P, _P, _P, _P, _P, _I, _P, _I, _I, _I, _I, _I, _L, _F, _P, _P], _I),
     "pa_prefill_chunk": ([_P, _P, _P, _P, _P, _I, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _L, _F,
                           _P, _P], _I),
     "pa_validate_metadata": ([_P, _I, _P, _I, _P, _I, _P, _L, _I], _I),
@@ -159,6 +161,26 @@ def pa_decode(out, q, k_cache, v_cache, block_tables, seq_lens, scale, partition
         _ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables),
         block_tables.shape[1], _ptr(seq_lens), S, Hq, Hkv, D, bs, nb, float(scale),
         int(partition_tokens), _ptr(out_lse), _ptr(workspace), ws_bytes, _stream(stream)))
+
+
+def pa_decode_noalloc(out, q, k_cache, v_cache, block_tables, seq_lens, scale, out_lse=None,
+                      stream=None) -> None:
+    """Balanced decode with the library's static scratch: no workspace, no
+    allocation (for callers that cannot allocate device memory)."""
+    _need(out, "out", torch.bfloat16, 3)
+    _need(q, "q", torch.bfloat16, 3)
+    _need(k_cache, "k_cache", torch.bfloat16, 4)
+    _need(v_cache, "v_cache", torch.bfloat16, 4)
+    _need(block_tables, "block_tables", torch.int32, 2)
+    _need(seq_lens, "seq_lens", torch.int32, 1)
+    if out_lse is not None:
+        _need(out_lse, "out_lse", torch.float32, 2)
+    S, Hq, D = q.shape
+    nb, bs, Hkv, _ = k_cache.shape
+    _check("pa_decode_noalloc", _lib.pa_decode_noalloc(
+        _ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables),
+        block_tables.shape[1], _ptr(seq_lens), S, Hq, Hkv, D, bs, nb, float(scale),
+        _ptr(out_lse), _stream(stream)))
 
 
 def pa_merge_partials(out, part_out, part_lse, num_parts, out_lse=None, stream=None) -> None:

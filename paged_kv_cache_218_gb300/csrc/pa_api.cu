@@ -232,6 +232,7 @@ const char* pa_status_string(int status) {
     case PA_ERR_UNSUPPORTED: return "PA_ERR_UNSUPPORTED";
     case PA_ERR_CUDA: return "PA_ERR_CUDA";
     case PA_ERR_WORKSPACE: return "PA_ERR_WORKSPACE";
+    case PA_ERR_SCRATCH_LIMIT: return "PA_ERR_SCRATCH_LIMIT";
     default: return "PA_ERR_UNKNOWN";
   }
 }
@@ -407,6 +408,51 @@ int pa_decode(void* out, const void* q, const void* k_cache, const void* v_cache
     if (launch_merge(m, st) != cudaSuccess) return PA_ERR_CUDA;
   }
   return PA_OK;
+}
+
+// Static scratch of pa_decode_noalloc: the balanced split's merge tickets and
+// partial slots, for callers that cannot allocate.  In host code the array's
+// name is only a host-side stand-in; kernels get its device address, looked
+// up once per device below.
+static __device__ __align__(256) unsigned char g_noalloc_scratch[PA_NOALLOC_SCRATCH_BYTES];
+static std::mutex g_noalloc_mu;
+static void* g_noalloc_ptr[pa::kMaxDevices];
+
+int pa_decode_noalloc(void* out, const void* q, const void* k_cache, const void* v_cache,
+                      const int32_t* block_tables, int max_blocks_per_seq,
+                      const int32_t* seq_lens, int num_seqs, int num_q_heads, int num_kv_heads,
+                      int head_dim, int block_size, int64_t num_blocks, float scale,
+                      float* out_lse, void* stream) {
+  if (int rc = check_shape(num_q_heads, num_kv_heads, head_dim, block_size)) return rc;
+  if (num_seqs < 0 || max_blocks_per_seq <= 0 || num_blocks <= 0) return PA_ERR_INVALID;
+  if (num_seqs == 0) return PA_OK;
+  DeviceInfo* d;
+  if (int rc = current_device_info(&d)) return rc;
+  const size_t need = balanced_workspace_bytes(decode_grid(d->num_sms, kModeBalanced),
+                                               num_q_heads, head_dim);
+  if (need > PA_NOALLOC_SCRATCH_BYTES) return PA_ERR_SCRATCH_LIMIT;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return PA_ERR_CUDA;
+  void* scratch = nullptr;
+  {
+    std::lock_guard<std::mutex> lock(g_noalloc_mu);
+    if (!g_noalloc_ptr[dev]) {
+      void* p = nullptr;
+      if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr)
+        return PA_ERR_CUDA;
+      g_noalloc_ptr[dev] = p;
+    }
+    scratch = g_noalloc_ptr[dev];
+  }
+  // the merge tickets must start at zero (the kernel leaves them zeroed, but a
+  // call cut short by an error may not)
+  const size_t tickets = (static_cast<size_t>(decode_grid(d->num_sms, kModeBalanced)) * 4 + 255) /
+                         256 * 256;
+  if (cudaMemsetAsync(scratch, 0, tickets, static_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return PA_ERR_CUDA;
+  return pa_decode(out, q, k_cache, v_cache, block_tables, max_blocks_per_seq, seq_lens, num_seqs,
+                   num_q_heads, num_kv_heads, head_dim, block_size, num_blocks, scale, 0, out_lse,
+                   scratch, PA_NOALLOC_SCRATCH_BYTES, stream);
 }
 
 int pa_merge_partials(void* out, float* out_lse, const float* part_out, const float* part_lse,
