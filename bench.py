@@ -256,14 +256,37 @@ def run_gpu(args, rank, world, local_rank):
     if pa.pa_device_error_flags() != 0:
         raise RuntimeError("device error flags set during warm-up")
 
+    # Decode-only steps replay one CUDA graph per replica (scatter, then decode
+    # as its programmatic dependent): the same kernels with the same inputs,
+    # without the per-launch host cost of the Python binding.
+    use_graphs = not hybrid and not args.no_graphs
+    g_step, g_dec = [], []
+    if use_graphs:
+        for r in range(R):
+            g1 = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g1):
+                step(r)
+            g2 = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g2):
+                pa.pa_decode(*decode_args(w, reps[r]), w.scale, partition_tokens=P, workspace=ws[r])
+            g_step.append(g1)
+            g_dec.append(g2)
+        for i in range(args.warmup):
+            g_step[i % R].replay()
+        torch.cuda.synchronize()
+
     dist = world > 1
     if dist:
         import torch.distributed as tdist
     K = args.steps
-    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-           for _ in range(K)]
-    cevs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-            for _ in range(K)] if hybrid else [None] * K
+    if use_graphs:
+        evs = []
+        cevs = [None] * K
+    else:
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(K)]
+        cevs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                for _ in range(K)] if hybrid else [None] * K
     sampler = ClockSampler(dev.index if dev.index is not None else 0)
     sampler.start()
     time.sleep(0.6)
@@ -272,8 +295,12 @@ def run_gpu(args, rank, world, local_rank):
         tdist.barrier()
     torch.cuda.synchronize()
     t_start.record(main)
-    for i in range(K):
-        step(i, evs[i], cevs[i])
+    if use_graphs:
+        for i in range(K):
+            g_step[i % R].replay()
+    else:
+        for i in range(K):
+            step(i, evs[i], cevs[i])
     t_end.record(main)
     torch.cuda.synchronize()
     if dist:
@@ -284,7 +311,21 @@ def run_gpu(args, rank, world, local_rank):
         t = torch.tensor([elapsed_ms], dtype=torch.float64, device=dev)
         tdist.all_reduce(t, op=tdist.ReduceOp.MAX)
         elapsed_ms = float(t.item())
-    dec_ms = sum(a.elapsed_time(b) for a, b in evs) / K
+    if use_graphs:
+        # the decode kernel alone: CUDA events on the launching stream around
+        # back-to-back decode-graph replays (one kernel each)
+        K2 = min(K, args.kernel_steps)
+        kev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(K2)]
+        torch.cuda.synchronize()
+        for i in range(K2):
+            kev[i][0].record(main)
+            g_dec[i % R].replay()
+            kev[i][1].record(main)
+        torch.cuda.synchronize()
+        dec_ms = sum(a.elapsed_time(b) for a, b in kev) / K2
+    else:
+        dec_ms = sum(a.elapsed_time(b) for a, b in evs) / K
     chunk_ms = sum(a.elapsed_time(b) for a, b in cevs) / K if hybrid else None
     flags = pa.pa_device_error_flags()
     if flags:
@@ -292,7 +333,7 @@ def run_gpu(args, rank, world, local_rank):
 
     e2e = run_e2e(args, w, reps, ws, dev, pa, dist)
     return dict(w=w, elapsed_ms=elapsed_ms, dec_ms=dec_ms, chunk_ms=chunk_ms, clocks=clocks,
-                e2e=e2e, launches=launches_per_step * K)
+                e2e=e2e, launches=launches_per_step * K, graphs=use_graphs)
 
 
 def run_e2e(args, w, reps, ws, dev, pa, dist):
@@ -426,6 +467,10 @@ def main():
     ap.add_argument("--replicas", type=int, default=8)
     ap.add_argument("--e2e-steps", type=int, default=2000)
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--kernel-steps", type=int, default=2000,
+                    help="decode-only launches timed for the roofline's kernel duration")
+    ap.add_argument("--no-graphs", action="store_true",
+                    help="launch every kernel from Python instead of replaying CUDA graphs")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
@@ -470,13 +515,18 @@ def main():
                    "accumulate": "fp32",
                    "l2": f"{args.replicas} independent KV pools in rotation "
                          f"({args.replicas * 2 * w.k_cache.nbytes / 1e9:.2f} GB) >> 129 MB L2",
-                   "parallelism": f"replicas x{world}"},
+                   "parallelism": f"replicas x{world}",
+                   "launch": "CUDA graph per replica (scatter + decode)" if res["graphs"]
+                             else "eager launches from Python"},
         "tokens_per_s": w.num_decode_seqs * world * K / (res["elapsed_ms"] * 1e-3),
         "pct_of_nominal_8tbps": 100.0 * value / world / NOMINAL_HBM_GBS,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
                      "frac": achieved / hbm, "traffic": traffic,
                      "kernel": "decode_kernel<128>", "peak_source": f"{peak_src} (hbm_gbs)",
-                     "bytes_per_launch": alg, "launch_ms": res["dec_ms"]},
+                     "bytes_per_launch": alg, "launch_ms": res["dec_ms"],
+                     "launch_timing": ("CUDA events on the launching stream around back-to-back "
+                                       "decode-only graph replays") if res["graphs"]
+                                      else "CUDA events around each decode launch in the timed region"},
         "e2e": {"value": kvb * world * e["steps"] / (e["ms"] * 1e-3) / 1e9, "unit": "GB/s",
                 "h2d_bytes_per_step": e["h2d"], "d2h_bytes_per_step": e["d2h"],
                 "steps": e["steps"], "ms_per_step": e["ms"] / e["steps"]},

@@ -14,6 +14,7 @@
 
 #include "../../include/pa.h"
 #include "pa_internal.h"
+#include "pa_ptx.cuh"
 
 namespace pa {
 namespace {
@@ -63,8 +64,8 @@ bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p
 
 // Paged pool [num_blocks * 16 tokens, Hkv, D] as a 3-D tensor; box = 64
 // columns x 1 head x `rows` tokens, 128-byte swizzle.
-int encode_pool_map(CUtensorMap* m, const void* pool, int64_t num_blocks, int Hkv, int D,
-                    int rows) {
+int encode_pool_map_uncached(CUtensorMap* m, const void* pool, int64_t num_blocks, int Hkv, int D,
+                             int rows) {
   cuuint64_t dims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(Hkv),
                         static_cast<cuuint64_t>(num_blocks) * kBlockSize};
   cuuint64_t strides[2] = {static_cast<cuuint64_t>(D) * 2, static_cast<cuuint64_t>(Hkv) * D * 2};
@@ -75,6 +76,42 @@ int encode_pool_map(CUtensorMap* m, const void* pool, int64_t num_blocks, int Hk
                         CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? PA_OK : PA_ERR_CUDA;
+}
+
+// A serving loop passes the same pools every step: keep the last few pool
+// descriptors (they are pure functions of pointer and shape) so a call does
+// not re-encode them.
+struct PoolMapEntry {
+  const void* pool;
+  int64_t num_blocks;
+  int Hkv, D, rows;
+  CUtensorMap map;
+};
+constexpr int kPoolMapCache = 32;
+std::mutex g_map_mu;
+PoolMapEntry g_map_cache[kPoolMapCache];
+int g_map_next = 0;
+
+int encode_pool_map(CUtensorMap* m, const void* pool, int64_t num_blocks, int Hkv, int D,
+                    int rows) {
+  std::lock_guard<std::mutex> lock(g_map_mu);
+  for (int i = 0; i < kPoolMapCache; ++i) {
+    const PoolMapEntry& e = g_map_cache[i];
+    if (e.pool == pool && e.num_blocks == num_blocks && e.Hkv == Hkv && e.D == D && e.rows == rows) {
+      *m = e.map;
+      return PA_OK;
+    }
+  }
+  if (int rc = encode_pool_map_uncached(m, pool, num_blocks, Hkv, D, rows)) return rc;
+  PoolMapEntry& e = g_map_cache[g_map_next];
+  g_map_next = (g_map_next + 1) % kPoolMapCache;
+  e.pool = pool;
+  e.num_blocks = num_blocks;
+  e.Hkv = Hkv;
+  e.D = D;
+  e.rows = rows;
+  e.map = *m;
+  return PA_OK;
 }
 
 // q [T, Hq, D] as a 3-D tensor; box = 64 columns x `heads` heads x `rows` tokens.
@@ -110,6 +147,9 @@ __global__ void reshape_and_cache_kernel(const uint4* __restrict__ key,
                                          const int64_t* __restrict__ slots, int num_tokens,
                                          int vec_per_token, int64_t num_slots,
                                          unsigned int* err) {
+  // the decode / prefill launched after this may begin its prologue now; it
+  // waits for this kernel's writes before reading any global memory
+  griddep_launch_dependents();
   const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   if (i >= static_cast<int64_t>(num_tokens) * vec_per_token) return;
   const int t = static_cast<int>(i / vec_per_token);
@@ -340,7 +380,8 @@ int pa_decode(void* out, const void* q, const void* k_cache, const void* v_cache
   const int mode = decode_mode(partition_tokens);
   if (mode == kModeFixedSplit && partition_tokens % block_size) return PA_ERR_INVALID;
   if (mode == kModeBalanced && num_seqs > kMaxSeqsBalanced) return PA_ERR_UNSUPPORTED;
-  if (!decode_supported(head_dim, num_kv_heads, mode, num_seqs)) return PA_ERR_UNSUPPORTED;
+  if (!decode_supported(head_dim, num_kv_heads, num_q_heads, mode, num_seqs))
+    return PA_ERR_UNSUPPORTED;
   DeviceInfo* d;
   if (int rc = current_device_info(&d)) return rc;
 

@@ -31,6 +31,8 @@
 // still meeting its named barriers.
 #include <math.h>
 
+#include <mutex>
+
 #include "../../include/pa.h"
 #include "pa_internal.h"
 #include "pa_ptx.cuh"
@@ -64,20 +66,23 @@ struct Layout {
   int head_bytes;   // K (or V) of one block, one kv head
   int stage_bytes;  // K + V of one block, all kv heads
   int stages;
-  int obuf_off, ml_off, bar_off, misc_off, pre_off, total;
+  int q_bytes;      // one staged query row set: Hq x D bf16
+  int q_off, obuf_off, ml_off, bar_off, misc_off, pre_off, total;
 };
 
-__host__ __device__ inline Layout make_layout(int D, int Hkv, int wph, int stages,
+__host__ __device__ inline Layout make_layout(int D, int Hkv, int Hq, int wph, int stages,
                                               int pre_ints) {
   Layout L;
   L.head_bytes = (D / 64) * kBoxBytes;
   L.stage_bytes = 2 * Hkv * L.head_bytes;
   L.stages = stages;
-  L.obuf_off = stages * L.stage_bytes;
+  L.q_bytes = (Hq * D * 2 + 127) / 128 * 128;
+  L.q_off = stages * L.stage_bytes;
+  L.obuf_off = L.q_off + 2 * L.q_bytes;
   const int obuf = wph > 1 ? kConsumerWarps * kMaxGroup * (D + 4) * 4 : 0;
   L.ml_off = L.obuf_off + obuf;
   L.bar_off = L.ml_off + kConsumerWarps * kMaxGroup * 2 * 4;
-  L.misc_off = L.bar_off + kMaxStages * 2 * 8;
+  L.misc_off = L.bar_off + (kMaxStages * 2 + 4) * 8;
   L.pre_off = L.misc_off + 64;
   L.total = L.pre_off + pre_ints * 4;
   return L;
@@ -143,30 +148,6 @@ __device__ bool next_piece(const DecodeArgs& a, const int* pre, Cursor& c, Piece
     return true;
   }
   return false;
-}
-
-// Chunks of up to 32 consecutive blocks of the CTA's piece sequence.
-struct ChunkIter {
-  Cursor cur;
-  Piece pc;
-  int jb;
-  bool valid;
-};
-
-__device__ __forceinline__ bool next_chunk(const DecodeArgs& a, const int* pre, ChunkIter& it,
-                                           int& s, int& jb, int& n) {
-  while (true) {
-    if (it.valid && it.jb < it.pc.j1) {
-      s = it.pc.s;
-      jb = it.jb;
-      n = min(32, it.pc.j1 - it.jb);
-      it.jb += n;
-      return true;
-    }
-    if (!next_piece(a, pre, it.cur, it.pc, false)) return false;
-    it.valid = true;
-    it.jb = it.pc.j0;
-  }
 }
 
 __device__ __forceinline__ int load_ids(const DecodeArgs& a, int s, int jb, int n, int lane) {
@@ -256,6 +237,71 @@ __device__ __forceinline__ void attend_block(uint32_t kbase, uint32_t vbase,
   }
 }
 
+// Log-sum-exp merge of a sequence's partial pieces, held in the slots of CTAs
+// c_first (its "after" slot) and c_first+1 .. c_first+npieces-1 ("before"
+// slots); writes the final bf16 output (and lse).  A running log-sum-exp per
+// float4 group over the pieces; a thread's loads of one piece are independent,
+// so each piece costs about one L2 round trip per batch of groups.
+template <int D>
+__device__ __forceinline__ void merge_pieces(const DecodeArgs& a, int s, long long c_first,
+                                             int npieces, int ctid) {
+  const int Hq = a.num_q_heads;
+    constexpr int kNI = 4;  // float4 groups per thread per batch
+    const int nf = Hq * D / 4;  // float4 groups of the sequence's output
+    const long long row0 = static_cast<long long>(s) * Hq;
+    for (int fb0 = 0; fb0 < nf; fb0 += kNI * kConsumerThreads) {
+      float4 acc[kNI];
+      float mrun[kNI], wsum[kNI];
+#pragma unroll
+      for (int i = 0; i < kNI; ++i) {
+        acc[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+        mrun[i] = -INFINITY;
+        wsum[i] = 0.f;
+      }
+#pragma unroll 1
+      for (int k = 0; k < npieces; ++k) {
+        const float* sl = a.part_o + ((c_first + k) * 2 + (k == 0 ? 1 : 0)) * a.slot_floats;
+        float lk[kNI];
+        float4 ok[kNI];
+#pragma unroll
+        for (int i = 0; i < kNI; ++i) {
+          const int f = fb0 + ctid + i * kConsumerThreads;
+          if (f < nf) {
+            lk[i] = __ldcg(sl + Hq * D + (f * 4) / D);
+            ok[i] = __ldcg(reinterpret_cast<const float4*>(sl) + f);
+          }
+        }
+#pragma unroll
+        for (int i = 0; i < kNI; ++i) {
+          const int f = fb0 + ctid + i * kConsumerThreads;
+          if (f < nf && lk[i] != -INFINITY) {
+            const float mn = fmaxf(mrun[i], lk[i]);
+            const float sc = __expf(mrun[i] - mn), w = __expf(lk[i] - mn);
+            acc[i].x = acc[i].x * sc + w * ok[i].x;
+            acc[i].y = acc[i].y * sc + w * ok[i].y;
+            acc[i].z = acc[i].z * sc + w * ok[i].z;
+            acc[i].w = acc[i].w * sc + w * ok[i].w;
+            wsum[i] = wsum[i] * sc + w;
+            mrun[i] = mn;
+          }
+        }
+      }
+#pragma unroll
+      for (int i = 0; i < kNI; ++i) {
+        const int f = fb0 + ctid + i * kConsumerThreads;
+        if (f < nf) {
+          const float inv = wsum[i] > 0.f ? 1.f / wsum[i] : 0.f;
+          const uint2 pk = make_uint2(pack_bf16x2(acc[i].x * inv, acc[i].y * inv),
+                                      pack_bf16x2(acc[i].z * inv, acc[i].w * inv));
+          *reinterpret_cast<uint2*>(a.out + row0 * D + static_cast<long long>(f) * 4) = pk;
+          if ((f * 4) % D == 0 && a.out_lse)
+            a.out_lse[row0 + (f * 4) / D] =
+                wsum[i] > 0.f ? mrun[i] + __logf(wsum[i]) : -INFINITY;
+        }
+      }
+    }
+}
+
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
     decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
@@ -266,16 +312,19 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* smem = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
   const uint32_t sbase = smem_u32(smem);
 
-  const int Hkv = a.num_kv_heads, G = a.group;
+  const int Hkv = a.num_kv_heads, G = a.group, Hq = a.num_q_heads;
   const int wph = a.warps_per_head;
-  const Layout L = make_layout(D, Hkv, wph, a.stages, 0);
+  const Layout L = make_layout(D, Hkv, Hq, wph, a.stages, 0);
   float* obuf = reinterpret_cast<float*>(smem + L.obuf_off);
   float* mlbuf = reinterpret_cast<float*>(smem + L.ml_off);
   int* misc = reinterpret_cast<int*>(smem + L.misc_off);
   int* pre = reinterpret_cast<int*>(smem + L.pre_off);
   const uint32_t bar_full = sbase + L.bar_off;
   const uint32_t bar_empty = bar_full + kMaxStages * 8;
+  const uint32_t bar_qfull = bar_empty + kMaxStages * 8;  // two query slots
+  const uint32_t bar_qempty = bar_qfull + 16;
   const int NS = L.stages;
+  const int active_warps = Hkv * wph < kConsumerWarps ? Hkv * wph : kConsumerWarps;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
@@ -284,9 +333,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(bar_full + st * 8, 1);
       mbar_init(bar_empty + st * 8, Hkv);  // one arrival per kv head's warp
     }
+    for (int k = 0; k < 2; ++k) {
+      mbar_init(bar_qfull + k * 8, 1);
+      mbar_init(bar_qempty + k * 8, active_warps);
+    }
     misc[0] = 0;  // abort flag
     fence_mbar_init();
   }
+  // Nothing above touches global memory: launched as a programmatic dependent
+  // of the previous kernel on the stream, the CTA may get here early and waits
+  // here until that kernel has finished and its writes are visible.
+  griddep_wait();
 
   Cursor cur{};
   if (a.mode == kModeBalanced) {
@@ -334,17 +391,56 @@ __global__ void __launch_bounds__(kThreads, 1)
       tma_prefetch_desc(&tm_v);
     }
     const uint64_t pol = l2_policy_evict_first();
-    ChunkIter it{cur, Piece{}, 0, false};
+    const uint32_t qrow_bytes = static_cast<uint32_t>(Hq) * D * 2;
+    bool ok = true;
+    // query rows of the piece's sequence into query slot qi & 1 (lane 0)
+    auto stage_q = [&](const Piece& p, int qi) {
+      if (lane != 0 || !ok) return;
+      const int k = qi & 1;
+      if (qi >= 2 && !mbar_wait(bar_qempty + k * 8, ((qi >> 1) - 1) & 1)) {
+        atomicOr(a.err, PA_DEVERR_TIMEOUT);
+        ok = false;
+        return;
+      }
+      mbar_arrive_expect_tx(bar_qfull + k * 8, qrow_bytes);
+      bulk_load(sbase + L.q_off + k * L.q_bytes, a.q + static_cast<long long>(p.s) * Hq * D,
+                qrow_bytes, bar_qfull + k * 8);
+    };
+    Piece p{};
+    int qi = 0, jbp = 0;
+    bool have_p = next_piece(a, pre, cur, p, false);
+    if (have_p) {
+      stage_q(p, qi++);
+      jbp = p.j0;
+    }
+    // next chunk of up to 32 blocks, staging the queries of every piece reached
+    auto next_chunk2 = [&](int& s, int& jb, int& n) -> bool {
+      while (have_p) {
+        if (jbp < p.j1) {
+          s = p.s;
+          jb = jbp;
+          n = min(32, p.j1 - jbp);
+          jbp += n;
+          return true;
+        }
+        have_p = next_piece(a, pre, cur, p, false);
+        if (!have_p) return false;
+        stage_q(p, qi++);
+        jbp = p.j0;
+      }
+      return false;
+    };
     int s, jb, n;
-    bool have = next_chunk(a, pre, it, s, jb, n);
+    bool have = next_chunk2(s, jb, n);
     int ids = have ? load_ids(a, s, jb, n, lane) : 0;
     uint32_t g = 0;
-    bool ok = true;
+    ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
     while (have && ok) {
       int s2, jb2, n2;
-      const bool have2 = next_chunk(a, pre, it, s2, jb2, n2);
+      const bool have2 = next_chunk2(s2, jb2, n2);
       const int ids2 = have2 ? load_ids(a, s2, jb2, n2, lane) : 0;
-      for (int i = 0; i < n; ++i, ++g) {
+      ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+      for (int i = 0; i < n && ok; ++i, ++g) {
         const int blk = __shfl_sync(0xffffffffu, ids, i);
         const uint32_t st = g % NS;
         const uint32_t fb = bar_full + st * 8;
@@ -375,6 +471,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       ids = ids2;
       have = have2;
     }
+    // queries of pieces without blocks (empty sequences) still get staged
+    while (ok && have_p) {
+      have_p = next_piece(a, pre, cur, p, false);
+      if (have_p) stage_q(p, qi++);
+    }
+    if (!ok) *reinterpret_cast<volatile int*>(misc) = 1;
     return;
   }
 
@@ -384,36 +486,55 @@ __global__ void __launch_bounds__(kThreads, 1)
     // sequences without tokens produce out = 0, lse = -inf
     for (int s = blockIdx.x; s < a.num_seqs; s += gridDim.x) {
       if (load_len(a, s, ctid == 0) != 0) continue;
-      for (int e = ctid; e < a.num_q_heads * D; e += kConsumerThreads)
-        a.out[static_cast<long long>(s) * a.num_q_heads * D + e] = __float2bfloat16(0.f);
+      for (int e = ctid; e < Hq * D; e += kConsumerThreads)
+        a.out[static_cast<long long>(s) * Hq * D + e] = __float2bfloat16(0.f);
       if (a.out_lse)
-        for (int h = ctid; h < a.num_q_heads; h += kConsumerThreads)
-          a.out_lse[static_cast<long long>(s) * a.num_q_heads + h] = -INFINITY;
+        for (int h = ctid; h < Hq; h += kConsumerThreads)
+          a.out_lse[static_cast<long long>(s) * Hq + h] = -INFINITY;
     }
   }
 
-  const bool active = warp < Hkv * wph;
-  const int hw = warp % Hkv;  // this warp's kv head
-  const int sub = warp / Hkv; // which of the head's warps
+  const bool active = warp < active_warps;
+  const int hw = warp % Hkv;   // this warp's kv head
+  const int sub = warp / Hkv;  // which of the head's warps
   const int q4 = lane & 3;
   const int d0 = lane >> 2;
+  const int hq = lane >> 2;
   volatile int* abort_flag = misc;
+  // balanced partial pieces (at most the CTA's first and last) are published
+  // as they finish; their tickets and merges wait until the CTA is done
+  long long def_cf[2] = {0, 0};
+  int def_np[2] = {0, 0}, def_s[2] = {0, 0}, ndef = 0;
   Piece pc;
   uint32_t g = 0;
+  int qi = 0;
   while (next_piece(a, pre, cur, pc, ctid == 0)) {
-    // query fragments of the group: B operand (k = dim, n = head)
+    const long long head0 = static_cast<long long>(pc.s) * Hq + hw * G;
     uint32_t qf[KS][2];
-    const int hq = lane >> 2;
-    const long long head0 = static_cast<long long>(pc.s) * a.num_q_heads + hw * G;
     if (active) {
-      const __nv_bfloat16* qrow = a.q + (head0 + hq) * D;
+      // query fragments of the group (B operand: k = dim, n = head) from the
+      // piece's staged query rows
+      const int k = qi & 1;
+      if (!*abort_flag && !mbar_wait(bar_qfull + k * 8, (qi >> 1) & 1)) {
+        atomicOr(a.err, PA_DEVERR_TIMEOUT);
+        *abort_flag = 1;
+      }
+      const uint32_t qrow = sbase + L.q_off + k * L.q_bytes + (hw * G + hq) * D * 2;
 #pragma unroll
       for (int ks = 0; ks < KS; ++ks) {
-        const int c = ks * 16 + q4 * 2;
-        qf[ks][0] = hq < G ? *reinterpret_cast<const uint32_t*>(qrow + c) : 0u;
-        qf[ks][1] = hq < G ? *reinterpret_cast<const uint32_t*>(qrow + c + 8) : 0u;
+        const uint32_t c = (ks * 16 + q4 * 2) * 2;
+        uint32_t x0 = 0u, x1 = 0u;
+        if (hq < G) {
+          asm volatile("ld.shared.b32 %0, [%1];" : "=r"(x0) : "r"(qrow + c));
+          asm volatile("ld.shared.b32 %0, [%1];" : "=r"(x1) : "r"(qrow + c + 16));
+        }
+        qf[ks][0] = x0;
+        qf[ks][1] = x1;
       }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar_qempty + k * 8);
     }
+    ++qi;
     float o[KS][4];
 #pragma unroll
     for (int mt = 0; mt < KS; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
@@ -446,7 +567,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       l0 += __shfl_xor_sync(0xffffffffu, l0, off);
       l1 += __shfl_xor_sync(0xffffffffu, l1, off);
     }
-    float fa, fb, lsea, lseb;  // scale applied to this warp's O, and the head's lse
+    float fa, fb, lsea, lseb;
     if (wph > 1) {
       // several warps share the head: merge their (m, l, O) through smem
       if (active && lane < 4) {
@@ -563,9 +684,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
     } else {
-      // balanced partial: publish to this CTA's slot [Hq][D] + lse[Hq], then the
-      // last of the sequence's pieces merges them all
-      const int Hq = a.num_q_heads;
+      // balanced partial: publish to this CTA's slot [Hq][D] + lse[Hq]
       float* slot = a.part_o + (static_cast<long long>(blockIdx.x) * 2 + pc.which) * a.slot_floats;
       if (writer) {
         const int hga = hw * G + ha, hgb = hw * G + hb;
@@ -586,72 +705,29 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (hb < G) slot[Hq * D + hgb] = lseb;
         }
       }
-      __threadfence();
-      named_barrier(1, kConsumerThreads);
-      const long long c_first = cta_of(pc.seg_start, cur.W, cur.C);
-      const long long c_last = cta_of(pc.seg_start + pc.nb - 1, cur.W, cur.C);
-      const int npieces = static_cast<int>(c_last - c_first + 1);
+      if (ndef < 2) {
+        def_cf[ndef] = cta_of(pc.seg_start, cur.W, cur.C);
+        def_np[ndef] = static_cast<int>(cta_of(pc.seg_start + pc.nb - 1, cur.W, cur.C) -
+                                        def_cf[ndef] + 1);
+        def_s[ndef] = pc.s;
+        ++ndef;
+      }
+    }
+  }
+
+  // ---- tickets of this CTA's partial pieces; the last piece of a sequence to
+  // arrive merges all of them by log-sum-exp
+  if (a.mode == kModeBalanced && ndef > 0) {
+    __threadfence();
+    named_barrier(1, kConsumerThreads);
+    for (int k = 0; k < ndef; ++k) {
+      const long long c_first = def_cf[k];
+      const int npieces = def_np[k];
       if (ctid == 0) misc[1] = atomicAdd(a.counters + c_first, 1);
       named_barrier(1, kConsumerThreads);
       if (misc[1] == npieces - 1) {
         __threadfence();
-        // a running log-sum-exp per float4 group over the pieces; a thread's
-        // loads of one piece are independent, so each piece costs about one
-        // L2 round trip per batch of groups
-        constexpr int kNI = 4;  // float4 groups per thread per batch
-        const int nf = Hq * D / 4;  // float4 groups of the sequence's output
-        const long long row0 = static_cast<long long>(pc.s) * Hq;
-        for (int fb0 = 0; fb0 < nf; fb0 += kNI * kConsumerThreads) {
-          float4 acc[kNI];
-          float mrun[kNI], wsum[kNI];
-#pragma unroll
-          for (int i = 0; i < kNI; ++i) {
-            acc[i] = make_float4(0.f, 0.f, 0.f, 0.f);
-            mrun[i] = -INFINITY;
-            wsum[i] = 0.f;
-          }
-#pragma unroll 1
-          for (int k = 0; k < npieces; ++k) {
-            const float* sl = a.part_o + ((c_first + k) * 2 + (k == 0 ? 1 : 0)) * a.slot_floats;
-            float lk[kNI];
-            float4 ok[kNI];
-#pragma unroll
-            for (int i = 0; i < kNI; ++i) {
-              const int f = fb0 + ctid + i * kConsumerThreads;
-              if (f < nf) {
-                lk[i] = __ldcg(sl + Hq * D + (f * 4) / D);
-                ok[i] = __ldcg(reinterpret_cast<const float4*>(sl) + f);
-              }
-            }
-#pragma unroll
-            for (int i = 0; i < kNI; ++i) {
-              const int f = fb0 + ctid + i * kConsumerThreads;
-              if (f < nf && lk[i] != -INFINITY) {
-                const float mn = fmaxf(mrun[i], lk[i]);
-                const float sc = __expf(mrun[i] - mn), w = __expf(lk[i] - mn);
-                acc[i].x = acc[i].x * sc + w * ok[i].x;
-                acc[i].y = acc[i].y * sc + w * ok[i].y;
-                acc[i].z = acc[i].z * sc + w * ok[i].z;
-                acc[i].w = acc[i].w * sc + w * ok[i].w;
-                wsum[i] = wsum[i] * sc + w;
-                mrun[i] = mn;
-              }
-            }
-          }
-#pragma unroll
-          for (int i = 0; i < kNI; ++i) {
-            const int f = fb0 + ctid + i * kConsumerThreads;
-            if (f < nf) {
-              const float inv = wsum[i] > 0.f ? 1.f / wsum[i] : 0.f;
-              const uint2 pk = make_uint2(pack_bf16x2(acc[i].x * inv, acc[i].y * inv),
-                                          pack_bf16x2(acc[i].z * inv, acc[i].w * inv));
-              *reinterpret_cast<uint2*>(a.out + row0 * D + static_cast<long long>(f) * 4) = pk;
-              if ((f * 4) % D == 0 && a.out_lse)
-                a.out_lse[row0 + (f * 4) / D] =
-                    wsum[i] > 0.f ? mrun[i] + __logf(wsum[i]) : -INFINITY;
-            }
-          }
-        }
+        merge_pieces<D>(a, def_s[k], c_first, npieces, ctid);
         if (ctid == 0) a.counters[c_first] = 0;
       }
       named_barrier(1, kConsumerThreads);
@@ -661,11 +737,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 int warps_per_head(int Hkv) { return Hkv >= kConsumerWarps ? 1 : kConsumerWarps / Hkv; }
 
-int pick_stages(int D, int Hkv, int pre_ints) {
+int pick_stages(int D, int Hkv, int Hq, int pre_ints) {
   const int wph = warps_per_head(Hkv);
   const int budget = 227 * 1024 - 1024;  // minus alignment slack
   int st = kMaxStages;
-  while (st > 2 && make_layout(D, Hkv, wph, st, pre_ints).total > budget) --st;
+  while (st > 2 && make_layout(D, Hkv, Hq, wph, st, pre_ints).total > budget) --st;
   return st;
 }
 
@@ -686,32 +762,55 @@ int decode_grid(int num_sms, int mode) {
   return num_sms;
 }
 
-bool decode_supported(int head_dim, int num_kv_heads, int mode, int num_seqs) {
+bool decode_supported(int head_dim, int num_kv_heads, int num_q_heads, int mode, int num_seqs) {
   if (num_kv_heads > kConsumerWarps) return false;
   const int pre = mode == kModeBalanced ? num_seqs + 1 : 0;
   const int wph = warps_per_head(num_kv_heads);
-  return make_layout(head_dim, num_kv_heads, wph, 2, pre).total <= 227 * 1024 - 1024;
+  return make_layout(head_dim, num_kv_heads, num_q_heads, wph, 2, pre).total <=
+         227 * 1024 - 1024;
 }
 
 cudaError_t launch_decode(DecodeArgs a, const CUtensorMap* tm_k, const CUtensorMap* tm_v,
                           int head_dim, int grid, cudaStream_t stream) {
   const int pre = a.mode == kModeBalanced ? a.num_seqs + 1 : 0;
   a.warps_per_head = warps_per_head(a.num_kv_heads);
-  a.stages = pick_stages(head_dim, a.num_kv_heads, pre);
-  const size_t smem =
-      make_layout(head_dim, a.num_kv_heads, a.warps_per_head, a.stages, pre).total + 1024;
-  cudaError_t e;
-  if (head_dim == 128) {
-    e = cudaFuncSetAttribute(decode_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(smem));
-    if (e != cudaSuccess) return e;
-    decode_kernel<128><<<grid, kThreads, smem, stream>>>(*tm_k, *tm_v, a);
-  } else {
-    e = cudaFuncSetAttribute(decode_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(smem));
-    if (e != cudaSuccess) return e;
-    decode_kernel<64><<<grid, kThreads, smem, stream>>>(*tm_k, *tm_v, a);
+  a.stages = pick_stages(head_dim, a.num_kv_heads, a.num_q_heads, pre);
+  const size_t smem = make_layout(head_dim, a.num_kv_heads, a.num_q_heads, a.warps_per_head,
+                                  a.stages, pre).total + 1024;
+  void (*kern)(const CUtensorMap, const CUtensorMap, const DecodeArgs) =
+      head_dim == 128 ? decode_kernel<128> : decode_kernel<64>;
+  // raise the kernel's dynamic shared-memory limit once per device
+  static std::mutex mu;
+  static int set_for[2][64] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  {
+    std::lock_guard<std::mutex> lock(mu);
+    int& done = set_for[head_dim == 128 ? 1 : 0][dev];
+    if (done < static_cast<int>(smem)) {
+      e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               227 * 1024);
+      if (e != cudaSuccess) return e;
+      done = 227 * 1024;
+    }
   }
+  // programmatic dependent launch: the CTAs may start while the previous
+  // kernel on the stream finishes; they touch no global memory before
+  // griddepcontrol.wait
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  e = cudaLaunchKernelEx(&cfg, kern, *tm_k, *tm_v, a);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 

@@ -4,29 +4,35 @@
 // Engines Papers", section 3 Sarathi / Sarathi-Serve); a chunk's query at
 // absolute position p attends over keys 0..p of its own paged KV, the K/V of
 // later chunks not being there yet.  This is the one dense contraction of the
-// path, so it runs on the 5th-generation tensor cores:
+// path, so it runs on the 5th-generation tensor cores, FlashAttention-style
+// (tiles through on-chip memory with an online softmax: FlashAttention and
+// Milakov & Gimelshein, "References" page):
 //
-//  * One CTA (4 warps) per (128-row query tile, chunk, kv head).  GQA packs
-//    the group's q heads into the tile's rows: row r = token (r / G), head
-//    (r % G), so each K/V tile serves all G heads (128 / G tokens per tile).
-//  * Q lands in shared memory once (TMA, 128-byte swizzle).  K/V tiles of 128
-//    keys are assembled from eight 16-token paged blocks by TMA, double
-//    buffered behind an mbarrier each.
-//  * S = Q K^T: eight tcgen05.mma (M=128, N=128, K=16, bf16 in, fp32
-//    accumulate) into tensor memory columns [0, 128); one elected thread
-//    issues them and commits to an mbarrier.
-//  * Each thread owns one tensor-memory lane = one query row: tcgen05.ld of
-//    its 128 scores, causal mask, online-softmax update (running max and
-//    sum, FlashAttention-style tiling with the Milakov & Gimelshein
-//    recurrence, "References" page), P rounded to bf16 into shared memory
-//    (swizzled K-major operand), and the accumulator O rescaled in tensor
-//    memory when its row maximum moved.
-//  * O += P V: eight tcgen05.mma into columns [128, 256), V read as an
-//    MN-major operand straight from the paged tile.
+//  * One CTA per (128-row query tile, chunk, kv head).  GQA packs the group's
+//    q heads into the rows: row r = token (r / G), head (r % G), so each K/V
+//    tile serves all G heads (128 / G tokens per tile).
+//  * Warp roles.  Warp 9 loads: Q once, then K/V tiles of 128 keys assembled
+//    from eight 16-token paged blocks by TMA (128-byte swizzle), double
+//    buffered.  Warp 8 issues the tensor-core work from one thread:
+//    S = Q K^T into one of two tensor-memory score buffers (tcgen05.mma,
+//    M = N = 128, K = 16, bf16 in, fp32 accumulate) and O += P V into a third
+//    region.  Warps 0-7 run the softmax: two warps per tensor-memory lane
+//    quadrant, each owning 64 of a row's 128 score columns.
+//  * Pipelining.  Scores of tile j+1 are computed while the softmax works on
+//    tile j (two score buffers), and PV of tile j-1 runs meanwhile too.
+//  * Softmax per row: tcgen05.ld of its scores, causal mask, row maximum
+//    shared by the two half-row owners, p = 2^(x - m) rounded to bf16 into
+//    shared memory as the K-major A operand of PV.  The running maximum only
+//    moves (and O in tensor memory is only rescaled) when the row maximum
+//    grows by more than 2^8, which keeps every p below 256 and the fp32
+//    accumulators far from overflow; the final division uses the same
+//    reference maximum, so the result is exact up to rounding.
 //  * Epilogue: tcgen05.ld of O, divide by the row sum, bf16 store; lse.
-// Every mbarrier wait is bounded; a timeout sets PA_DEVERR_TIMEOUT and the
-// CTA leaves its loop together (the decision is taken at a block barrier).
+// Every mbarrier wait is bounded; after a timeout the roles skip their
+// remaining waits, still meet their barriers, and PA_DEVERR_TIMEOUT is set.
 #include <math.h>
+
+#include <mutex>
 
 #include "../../include/pa.h"
 #include "pa_internal.h"
@@ -35,17 +41,24 @@
 namespace pa {
 namespace {
 
-constexpr int kThreads = 128;
+constexpr int kSoftmaxWarps = 8;
+constexpr int kMmaWarp = 8;
+constexpr int kLoadWarp = 9;
+constexpr int kThreads = 10 * 32;
 constexpr int kTileKeys = 128;
-constexpr int kHalf = 128 * 128;  // one 64-column half of a 128-row operand: 128 rows x 128 B
+constexpr int kHalf = 128 * 128;  // a 64-column half of a 128-row operand: 128 rows x 128 B
 constexpr int kQOff = 0;
 constexpr int kPOff = kQOff + 2 * kHalf;
 constexpr int kStageOff = kPOff + 2 * kHalf;
 constexpr int kStageBytes = 4 * kHalf;  // K (two halves) + V (two halves)
 constexpr int kVOff = 2 * kHalf;        // V within a stage
-constexpr int kBarOff = kStageOff + 2 * kStageBytes;
-constexpr int kSmemBytes = kBarOff + 128;
-constexpr uint32_t kTmemCols = 256;  // S in [0, 128), O in [128, 256)
+constexpr int kRedOff = kStageOff + 2 * kStageBytes;  // row max / sum exchange
+constexpr int kRedOff2 = kRedOff + 2 * 2 * 128 * 4;  // row-sum exchange
+constexpr int kBarOff = kRedOff2 + 2 * 128 * 4;
+constexpr int kSmemBytes = kBarOff + 256;
+constexpr uint32_t kTmemCols = 512;  // S0 [0,128), S1 [128,256), O [256,384)
+constexpr uint32_t kTmemO = 256;
+constexpr float kRescaleThreshold = 8.0f;  // log2 units
 constexpr float kLn2 = 0.6931471805599453f;
 
 // tcgen05 shared-memory matrix descriptor, 128-byte swizzle.
@@ -62,12 +75,23 @@ __device__ __forceinline__ uint64_t smem_desc(uint32_t addr, uint32_t lbo, uint3
 // Instruction descriptor, kind::f16: bf16 A and B, fp32 D, M = N = 128;
 // A K-major; B K-major (b_mn = 0) or MN-major (b_mn = 1).
 __host__ __device__ constexpr uint32_t instr_desc(uint32_t b_mn) {
-  return (1u << 4)            // D format: f32
-         | (1u << 7)          // A format: bf16
-         | (1u << 10)         // B format: bf16
-         | (b_mn << 16)       // B major-ness
+  return (1u << 4)              // D format: f32
+         | (1u << 7)            // A format: bf16
+         | (1u << 10)           // B format: bf16
+         | (b_mn << 16)         // B major-ness
          | ((128u >> 3) << 17)  // N / 8
          | ((128u >> 4) << 24); // M / 16
+}
+
+// Bounded wait that gives up at once after an earlier timeout anywhere in
+// the CTA (so every role still reaches its barriers).
+__device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, volatile int* abort,
+                                              unsigned int* err) {
+  if (*abort) return false;
+  if (mbar_wait(bar, parity)) return true;
+  *abort = 1;
+  atomicOr(err, PA_DEVERR_TIMEOUT);
+  return false;
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
@@ -78,10 +102,16 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* smem = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
   const uint32_t sbase = smem_u32(smem);
   const uint32_t bar_q = sbase + kBarOff;
-  const uint32_t bar_kv = bar_q + 8;  // two stages
-  const uint32_t bar_s = bar_q + 24;
-  const uint32_t bar_o = bar_q + 32;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kBarOff + 64);
+  const uint32_t bar_kv_full = bar_q + 8;    // [2]
+  const uint32_t bar_kv_empty = bar_q + 24;  // [2]
+  const uint32_t bar_s_full = bar_q + 40;    // [2]
+  const uint32_t bar_s_free = bar_q + 56;    // [2]
+  const uint32_t bar_p_full = bar_q + 72;
+  const uint32_t bar_o_done = bar_q + 80;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kBarOff + 96);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kBarOff + 100);
+  float* red_max = reinterpret_cast<float*>(smem + kRedOff);   // [2 parity][2 half][128]
+  float* red_sum = reinterpret_cast<float*>(smem + kRedOff2);  // [2 half][128]
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int Hkv = a.num_kv_heads, G = a.group;
@@ -90,6 +120,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int t2 = blockIdx.x / Hkv;
   const int c = t2 % a.num_chunks;
   const int m = t2 / a.num_chunks;
+
+  // launched as a programmatic dependent of the previous kernel (the scatter
+  // of this step's K/V): nothing before this line touches global memory
+  griddep_wait();
 
   // ---- chunk metadata (uniform over the CTA)
   const int q0 = a.cu_q_lens[c], q1 = a.cu_q_lens[c + 1];
@@ -108,10 +142,15 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (tid == 0) {
     mbar_init(bar_q, 1);
-    mbar_init(bar_kv, 1);
-    mbar_init(bar_kv + 8, 1);
-    mbar_init(bar_s, 1);
-    mbar_init(bar_o, 1);
+    for (int k = 0; k < 2; ++k) {
+      mbar_init(bar_kv_full + 8 * k, 1);
+      mbar_init(bar_kv_empty + 8 * k, 1);
+      mbar_init(bar_s_full + 8 * k, 1);
+      mbar_init(bar_s_free + 8 * k, kSoftmaxWarps);
+    }
+    mbar_init(bar_p_full, kSoftmaxWarps);
+    mbar_init(bar_o_done, 1);
+    *abort_flag = 0;
     fence_mbar_init();
   }
   if (warp == 0) {
@@ -122,39 +161,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  const uint32_t tmem_s = tmem;
-  const uint32_t tmem_o = tmem + 128;
-  const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
 
-  // K/V tiles are re-read by every query tile of the chunk: keep them in L2
-  const uint64_t pol = l2_policy_evict_last();
-  // K/V tile j (8 paged blocks) into stage st; blocks past the visible keys
-  // are read from outside the pool, which fills zeros
-  auto load_tile = [&](int j, int st) {
-    const uint32_t fb = bar_kv + st * 8;
-    if (lane == 0) mbar_arrive_expect_tx(fb, kStageBytes);
-    __syncwarp();
-    if (lane < 8) {
-      const int jb = j * 8 + lane;
-      int id = -1;
-      if (jb < nb_vis) {
-        id = a.block_tables[static_cast<long long>(c) * a.max_blocks + jb];
-        if (id < 0 || id >= a.num_blocks) {
-          atomicOr(a.err, PA_DEVERR_BLOCK_ID);
-          id = -1;
-        }
-      }
-      const uint32_t kd = sbase + kStageOff + st * kStageBytes + lane * kBlockSize * 128;
-      const int z = id * kBlockSize;
-#pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        tma_load_3d(kd + h * kHalf, &tm_k, h * 64, kvh, z, fb, pol);
-        tma_load_3d(kd + kVOff + h * kHalf, &tm_v, h * 64, kvh, z, fb, pol);
-      }
-    }
-  };
-
-  if (warp == 0) {
+  if (warp == kLoadWarp) {
+    // ------------------------------------------------------------ loader
+    // K/V tiles are re-read by every query tile of the chunk: keep them in L2
+    const uint64_t pol = l2_policy_evict_last();
     if (lane == 0) {
       tma_prefetch_desc(&tm_q);
       tma_prefetch_desc(&tm_k);
@@ -163,171 +174,199 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int h = 0; h < 2; ++h)
         tma_load_3d(sbase + kQOff + h * kHalf, &tm_q, h * 64, kvh * G, q0 + t0, bar_q, pol);
     }
-    load_tile(0, 0);
-  }
-
-  // this thread's query row
-  const int r = tid;
-  const int pos = p0 + t0 + r / G;
-  const int lim = min(pos, kmax - 1);  // last visible key of the row
-  float m_run = -INFINITY, l_run = 0.f;
-  bool timed_out = false;
-  const uint32_t idesc_s = instr_desc(0), idesc_o = instr_desc(1);
-
-  if (tid == 0 && !mbar_wait(bar_q, 0)) timed_out = true;
-
-  int j = 0;
-  for (; j < nkt; ++j) {
-    const int st = j & 1;
-    const uint32_t stage = sbase + kStageOff + st * kStageBytes;
-    // ---- S = Q K_j^T
-    if (tid == 0 && !timed_out) {
-      if (!mbar_wait(bar_kv + st * 8, (j >> 1) & 1)) {
-        timed_out = true;
-      } else {
-        tc_fence_after();
-#pragma unroll
-        for (int ks = 0; ks < 8; ++ks) {
-          const uint32_t koff = (ks >> 2) * kHalf + (ks & 3) * 32;
-          tc_mma_f16(tmem_s, smem_desc(sbase + kQOff + koff, 16, 1024),
-                     smem_desc(stage + koff, 16, 1024), idesc_s, ks > 0);
+    for (int j = 0; j < nkt; ++j) {
+      const int st = j & 1;
+      bool ok = true;
+      if (j >= 2 && lane == 0)
+        ok = wait_or_abort(bar_kv_empty + 8 * st, ((j >> 1) - 1) & 1, abort_flag, a.err);
+      if (__shfl_sync(0xffffffffu, ok ? 1 : 0, 0) == 0) break;
+      // tile j = paged blocks 8j .. 8j+7; blocks past the visible keys are read
+      // from outside the pool, which fills zeros
+      const uint32_t fb = bar_kv_full + 8 * st;
+      if (lane == 0) mbar_arrive_expect_tx(fb, kStageBytes);
+      __syncwarp();
+      if (lane < 8) {
+        const int jb = j * 8 + lane;
+        int id = -1;
+        if (jb < nb_vis) {
+          id = a.block_tables[static_cast<long long>(c) * a.max_blocks + jb];
+          if (id < 0 || id >= a.num_blocks) {
+            atomicOr(a.err, PA_DEVERR_BLOCK_ID);
+            id = -1;
+          }
         }
-        tc_commit(bar_s);
+        const uint32_t kd = sbase + kStageOff + st * kStageBytes + lane * kBlockSize * 128;
+        const int z = id * kBlockSize;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          tma_load_3d(kd + h * kHalf, &tm_k, h * 64, kvh, z, fb, pol);
+          tma_load_3d(kd + kVOff + h * kHalf, &tm_v, h * 64, kvh, z, fb, pol);
+        }
       }
     }
-    // ---- prefetch tile j+1 into the other stage once PV_{j-1} released it
-    if (warp == 0 && j + 1 < nkt) {
-      bool free_ok = true;
-      if (j >= 1 && lane == 0) free_ok = mbar_wait(bar_o, (j - 1) & 1);
-      free_ok = __shfl_sync(0xffffffffu, free_ok ? 1 : 0, 0) != 0;
-      if (free_ok) load_tile(j + 1, st ^ 1);
-      else timed_out = true;
-    }
-    if (!timed_out && !mbar_wait(bar_s, j & 1)) timed_out = true;
-    if (!timed_out && !mbar_wait(bar_kv + st * 8, (j >> 1) & 1)) timed_out = true;
-    tc_fence_after();
-
-    // ---- pass 1: row maximum of the visible scores
-    const int kb = j * kTileKeys;
-    uint32_t v[32];
-    float mx = -INFINITY;
+  } else if (warp == kMmaWarp) {
+    // ------------------------------------------------------------ tensor-core issue
+    if (lane == 0) {
+      const uint32_t idesc_s = instr_desc(0), idesc_o = instr_desc(1);
+      bool ok = wait_or_abort(bar_q, 0, abort_flag, a.err);
+      for (int j = 0; ok && j <= nkt; ++j) {
+        if (j < nkt) {
+          const int b = j & 1;
+          const uint32_t stage = sbase + kStageOff + b * kStageBytes;
+          if (!wait_or_abort(bar_kv_full + 8 * b, (j >> 1) & 1, abort_flag, a.err)) break;
+          if (j >= 2 && !wait_or_abort(bar_s_free + 8 * b, ((j >> 1) - 1) & 1, abort_flag, a.err))
+            break;
+          tc_fence_after();
 #pragma unroll
-    for (int cc = 0; cc < 4; ++cc) {
-      tmem_ld32(tmem_s + lane_off + cc * 32, v);
+          for (int ks = 0; ks < 8; ++ks) {
+            const uint32_t koff = (ks >> 2) * kHalf + (ks & 3) * 32;
+            tc_mma_f16(tmem + b * 128, smem_desc(sbase + kQOff + koff, 16, 1024),
+                       smem_desc(stage + koff, 16, 1024), idesc_s, ks > 0);
+          }
+          tc_commit(bar_s_full + 8 * b);
+        }
+        if (j >= 1) {
+          const int jp = j - 1;
+          const uint32_t stage = sbase + kStageOff + (jp & 1) * kStageBytes;
+          if (!wait_or_abort(bar_p_full, jp & 1, abort_flag, a.err)) break;
+          tc_fence_after();
 #pragma unroll
-      for (int i = 0; i < 32; ++i) {
-        const int k = kb + cc * 32 + i;
-        const float x = k <= lim ? __uint_as_float(v[i]) * a.scale_log2 : -INFINITY;
-        mx = fmaxf(mx, x);
+          for (int ks = 0; ks < 8; ++ks) {
+            const uint32_t poff = (ks >> 2) * kHalf + (ks & 3) * 32;
+            tc_mma_f16(tmem + kTmemO, smem_desc(sbase + kPOff + poff, 16, 1024),
+                       smem_desc(stage + kVOff + ks * 16 * 128, kHalf, 1024), idesc_o,
+                       (jp > 0 || ks > 0) ? 1u : 0u);
+          }
+          tc_commit(bar_o_done);
+          tc_commit(bar_kv_empty + 8 * (jp & 1));
+        }
       }
     }
-    const float m_new = fmaxf(m_run, mx);
-    const float alpha = fast_exp2(m_run - m_new);
-
-    // ---- PV_{j-1} must be done before O and the P buffer are touched
-    if (j >= 1 && !timed_out && !mbar_wait(bar_o, (j - 1) & 1)) timed_out = true;
-    tc_fence_after();
-    if (j >= 1 && __any_sync(0xffffffffu, alpha != 1.f)) {
-#pragma unroll
-      for (int cc = 0; cc < 4; ++cc) {
-        tmem_ld32(tmem_o + lane_off + cc * 32, v);
-#pragma unroll
-        for (int i = 0; i < 32; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) * alpha);
-        tmem_st32(tmem_o + lane_off + cc * 32, v);
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------ softmax warps
+    const int qd = warp & 3, hc = warp >> 2;
+    const int r = qd * 32 + lane;  // query row = tensor-memory lane
+    const uint32_t lane_off = static_cast<uint32_t>(qd * 32) << 16;
+    const int pos = p0 + t0 + r / G;
+    const int lim = min(pos, kmax - 1);  // last visible key of the row
+    float m_run = -INFINITY, l_run = 0.f;
+    uint32_t v[64];
+    for (int j = 0; j < nkt; ++j) {
+      const int b = j & 1;
+      wait_or_abort(bar_s_full + 8 * b, (j >> 1) & 1, abort_flag, a.err);
+      tc_fence_after();
+      const uint32_t scol = tmem + lane_off + b * 128 + hc * 64;
+      {
+        uint32_t (&v0)[32] = *reinterpret_cast<uint32_t(*)[32]>(&v[0]);
+        uint32_t (&v1)[32] = *reinterpret_cast<uint32_t(*)[32]>(&v[32]);
+        tmem_ld32(scol, v0);
+        tmem_ld32(scol + 32, v1);
       }
-    }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar_s_free + 8 * b);
 
-    // ---- pass 2: p = 2^(x - m_new), row sum, P (bf16) into shared memory
-    float rs = 0.f;
+      const int kb = j * kTileKeys + hc * 64;
+      float mloc = -INFINITY;
 #pragma unroll
-    for (int cc = 0; cc < 4; ++cc) {
-      tmem_ld32(tmem_s + lane_off + cc * 32, v);
-      uint32_t pk[16];
+      for (int i = 0; i < 64; ++i)
+        if (kb + i <= lim) mloc = fmaxf(mloc, __uint_as_float(v[i]) * a.scale_log2);
+      red_max[(b * 2 + hc) * 128 + r] = mloc;
+      named_barrier(1 + qd, 64);
+      const float mx = fmaxf(mloc, red_max[(b * 2 + (hc ^ 1)) * 128 + r]);
+      const float m_new = fmaxf(m_run, mx);
+      const bool move = m_new > m_run + kRescaleThreshold;  // true on the first tile
+      const float m_use = move ? m_new : m_run;
+      const float alpha = move ? fast_exp2(m_run - m_use) : 1.f;
+      float rs = 0.f;
+      uint32_t pk[32];
 #pragma unroll
-      for (int i = 0; i < 32; i += 2) {
-        const int k = kb + cc * 32 + i;
-        const float x0 = k <= lim ? __uint_as_float(v[i]) * a.scale_log2 : -INFINITY;
-        const float x1 = k + 1 <= lim ? __uint_as_float(v[i + 1]) * a.scale_log2 : -INFINITY;
-        const float e0 = fast_exp2(x0 - m_new), e1 = fast_exp2(x1 - m_new);
+      for (int i = 0; i < 64; i += 2) {
+        const float x0 = kb + i <= lim ? __uint_as_float(v[i]) * a.scale_log2 : -INFINITY;
+        const float x1 = kb + i + 1 <= lim ? __uint_as_float(v[i + 1]) * a.scale_log2 : -INFINITY;
+        const float e0 = fast_exp2(x0 - m_use), e1 = fast_exp2(x1 - m_use);
         rs += e0 + e1;
         pk[i / 2] = pack_bf16x2(e0, e1);
       }
-      // keys cc*32 .. cc*32+31 = half cc/2, 16-byte chunks (cc%2)*4 .. +3 of row r
-      const uint32_t rowbase = sbase + kPOff + (cc >> 1) * kHalf + r * 128;
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        const int chunk = (cc & 1) * 4 + q;
-        const uint32_t addr = rowbase + ((chunk ^ (r & 7)) << 4);
-        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(pk[4 * q]),
-                     "r"(pk[4 * q + 1]), "r"(pk[4 * q + 2]), "r"(pk[4 * q + 3])
-                     : "memory");
-      }
-    }
-    l_run = l_run * alpha + rs;
-    m_run = m_new;
+      l_run = l_run * alpha + rs;
+      m_run = m_use;
 
-    // ---- the sequence's last block may end inside this tile: its slots past
-    // seq_len hold no token and must not reach the PV product
-    if ((n & (kBlockSize - 1)) != 0) {
-      const int jl = (n - 1) / kBlockSize;
-      if (jl < nb_vis && jl / 8 == j) {
-        const int first = n - jl * kBlockSize;  // rows first..15 of block jl % 8
-        const int rows = kBlockSize - first;
-        for (int e = tid; e < rows * 2 * 8; e += kThreads) {
-          const int row = first + e / 16, h = (e / 8) & 1, chunk = e & 7;
-          const uint32_t addr =
-              stage + kVOff + h * kHalf + ((jl & 7) * kBlockSize + row) * 128 + (chunk << 4);
-          asm volatile("st.shared.v4.b32 [%0], {%1, %1, %1, %1};" ::"r"(addr), "r"(0u) : "memory");
+      // PV of the previous tile must be done before O and the P buffer change
+      if (j >= 1) wait_or_abort(bar_o_done, (j - 1) & 1, abort_flag, a.err);
+      tc_fence_after();
+      if (j >= 1 && __any_sync(0xffffffffu, alpha != 1.f)) {
+        const uint32_t ocol = tmem + lane_off + kTmemO + hc * 64;
+#pragma unroll
+        for (int cc = 0; cc < 2; ++cc) {
+          uint32_t (&w)[32] = *reinterpret_cast<uint32_t(*)[32]>(&v[32 * cc]);
+          tmem_ld32(ocol + 32 * cc, w);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) w[i] = __float_as_uint(__uint_as_float(w[i]) * alpha);
+          tmem_st32(ocol + 32 * cc, w);
         }
       }
-    }
-    fence_proxy_async_smem();
-    tc_fence_before();
-    if (__syncthreads_or(timed_out ? 1 : 0)) break;
-
-    // ---- O += P V_j
-    if (tid == 0) {
-      tc_fence_after();
+      // P row r, keys hc*64 .. hc*64+63 = the K-major operand's half hc
+      const uint32_t prow = sbase + kPOff + hc * kHalf + r * 128;
 #pragma unroll
-      for (int ks = 0; ks < 8; ++ks) {
-        const uint32_t poff = (ks >> 2) * kHalf + (ks & 3) * 32;
-        tc_mma_f16(tmem_o, smem_desc(sbase + kPOff + poff, 16, 1024),
-                   smem_desc(stage + kVOff + ks * 16 * 128, kHalf, 1024), idesc_o,
-                   (j > 0 || ks > 0) ? 1u : 0u);
+      for (int ch = 0; ch < 8; ++ch) {
+        const uint32_t addr = prow + ((ch ^ (r & 7)) << 4);
+        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(pk[4 * ch]),
+                     "r"(pk[4 * ch + 1]), "r"(pk[4 * ch + 2]), "r"(pk[4 * ch + 3])
+                     : "memory");
       }
-      tc_commit(bar_o);
+      // the sequence's last block may end inside this tile: its slots past
+      // seq_len hold no token and must not reach the PV product
+      if ((n & (kBlockSize - 1)) != 0) {
+        const int jl = (n - 1) / kBlockSize;
+        if (jl < nb_vis && jl / 8 == j) {
+          wait_or_abort(bar_kv_full + 8 * b, (j >> 1) & 1, abort_flag, a.err);
+          const uint32_t stage = sbase + kStageOff + b * kStageBytes;
+          const int first = n - jl * kBlockSize;  // rows first..15 of block jl % 8
+          const int rows = kBlockSize - first;
+          for (int e = tid; e < rows * 2 * 8; e += kSoftmaxWarps * 32) {
+            const int row = first + e / 16, h = (e / 8) & 1, chunk = e & 7;
+            const uint32_t addr =
+                stage + kVOff + h * kHalf + ((jl & 7) * kBlockSize + row) * 128 + (chunk << 4);
+            asm volatile("st.shared.v4.b32 [%0], {%1, %1, %1, %1};" ::"r"(addr), "r"(0u)
+                         : "memory");
+          }
+        }
+      }
+      fence_proxy_async_smem();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar_p_full);
     }
-  }
 
-  bool bad = !(j == nkt && !timed_out);
-  if (!bad && !mbar_wait(bar_o, (nkt - 1) & 1)) bad = true;
-  bad = __syncthreads_or(bad ? 1 : 0) != 0;  // uniform: tcgen05.ld below is warp-collective
-  tc_fence_after();
-  if (bad) {
-    if (tid == 0) atomicOr(a.err, PA_DEVERR_TIMEOUT);
-  } else {
     // ---- epilogue: O / l -> bf16, and lse
+    wait_or_abort(bar_o_done, (nkt - 1) & 1, abort_flag, a.err);
+    tc_fence_after();
+    red_sum[hc * 128 + r] = l_run;
+    named_barrier(1 + qd, 64);
+    const float l_tot = l_run + red_sum[(hc ^ 1) * 128 + r];
     const int tok = r / G, g = r % G;
-    const bool store = tok < tv;
-    const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
+    const bool store = tok < tv && !*abort_flag;
+    const float inv = l_tot > 0.f ? 1.f / l_tot : 0.f;
     const long long row = static_cast<long long>(q0 + t0 + tok) * a.num_q_heads + kvh * G + g;
-    uint32_t v[32];
+    const uint32_t ocol = tmem + lane_off + kTmemO + hc * 64;
 #pragma unroll
-    for (int cc = 0; cc < 4; ++cc) {
-      tmem_ld32(tmem_o + lane_off + cc * 32, v);
+    for (int cc = 0; cc < 2; ++cc) {
+      uint32_t (&w)[32] = *reinterpret_cast<uint32_t(*)[32]>(&v[32 * cc]);
+      tmem_ld32(ocol + 32 * cc, w);
       if (store) {
         uint32_t pk[16];
 #pragma unroll
         for (int i = 0; i < 32; i += 2)
-          pk[i / 2] = pack_bf16x2(__uint_as_float(v[i]) * inv, __uint_as_float(v[i + 1]) * inv);
-        uint4* dst = reinterpret_cast<uint4*>(a.out + row * 128 + cc * 32);
+          pk[i / 2] = pack_bf16x2(__uint_as_float(w[i]) * inv, __uint_as_float(w[i + 1]) * inv);
+        uint4* dst = reinterpret_cast<uint4*>(a.out + row * 128 + hc * 64 + cc * 32);
 #pragma unroll
         for (int q = 0; q < 4; ++q)
           dst[q] = make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
       }
     }
-    if (store && a.out_lse)
-      a.out_lse[row] = l_run > 0.f ? (m_run + __log2f(l_run)) * kLn2 : -INFINITY;
+    if (store && hc == 0 && a.out_lse)
+      a.out_lse[row] = l_tot > 0.f ? (m_run + __log2f(l_tot)) * kLn2 : -INFINITY;
   }
   tc_fence_before();
   __syncthreads();
@@ -341,10 +380,37 @@ size_t prefill_smem_bytes() { return kSmemBytes + 1024; }
 cudaError_t launch_prefill(const PrefillArgs& a, const CUtensorMap* tm_q, const CUtensorMap* tm_k,
                            const CUtensorMap* tm_v, int grid_tiles, cudaStream_t stream) {
   const size_t smem = prefill_smem_bytes();
-  cudaError_t e = cudaFuncSetAttribute(prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       static_cast<int>(smem));
+  // raise the kernel's dynamic shared-memory limit once per device
+  static std::mutex mu;
+  static bool set_for[64] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
-  prefill_kernel<<<grid_tiles, kThreads, smem, stream>>>(*tm_q, *tm_k, *tm_v, a);
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  {
+    std::lock_guard<std::mutex> lock(mu);
+    if (!set_for[dev]) {
+      e = cudaFuncSetAttribute(prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               static_cast<int>(smem));
+      if (e != cudaSuccess) return e;
+      set_for[dev] = true;
+    }
+  }
+  // programmatic dependent launch: the CTAs may start while the previous
+  // kernel on the stream finishes; they touch no global memory before
+  // griddepcontrol.wait
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid_tiles);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  e = cudaLaunchKernelEx(&cfg, prefill_kernel, *tm_q, *tm_k, *tm_v, a);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 
