@@ -11,18 +11,21 @@
 //  * One CTA per (128-row query tile, chunk, kv head).  GQA packs the group's
 //    q heads into the rows: row r = token (r / G), head (r % G), so each K/V
 //    tile serves all G heads (128 / G tokens per tile).
-//  * Warp roles.  Warp 9 loads: Q once, then K/V tiles of 128 keys assembled
-//    from eight 16-token paged blocks by TMA (128-byte swizzle), double
-//    buffered.  Warp 8 issues the tensor-core work from one thread:
+//  * Warp roles.  Warp 9 loads: Q once, then K and V tiles of 128 keys, each
+//    assembled from eight 16-token paged blocks by TMA (128-byte swizzle), in
+//    rings of two K and three V tiles (a K tile is free once its scores are
+//    done, a V tile only once its PV product is).  Warp 8 issues the tensor-core work from one thread:
 //    S = Q K^T into one of two tensor-memory score buffers (tcgen05.mma,
 //    M = N = 128, K = 16, bf16 in, fp32 accumulate) and O += P V into a third
 //    region.  Warps 0-7 run the softmax: two warps per tensor-memory lane
 //    quadrant, each owning 64 of a row's 128 score columns.
-//  * Pipelining.  Scores of tile j+1 are computed while the softmax works on
-//    tile j (two score buffers), and PV of tile j-1 runs meanwhile too.
+//  * Pipelining.  Loader and MMA issuer poll their barriers and issue
+//    whatever is ready, so scores of tile j+1 are computed while the softmax
+//    works on tile j (two score buffers) and PV of tile j-1 runs meanwhile.
 //  * Softmax per row: tcgen05.ld of its scores, causal mask, row maximum
-//    shared by the two half-row owners, p = 2^(x - m) rounded to bf16 into
-//    shared memory as the K-major A operand of PV.  The running maximum only
+//    shared by the two half-row owners, p = 2^(x - m) rounded to bf16 and
+//    stored back into tensor memory (tcgen05.st), double buffered, where the
+//    PV product reads it as its A operand.  The running maximum only
 //    moves (and O in tensor memory is only rescaled) when the row maximum
 //    grows by more than 2^8, which keeps every p below 256 and the fp32
 //    accumulators far from overflow; the final division uses the same
@@ -48,16 +51,20 @@ constexpr int kThreads = 10 * 32;
 constexpr int kTileKeys = 128;
 constexpr int kHalf = 128 * 128;  // a 64-column half of a 128-row operand: 128 rows x 128 B
 constexpr int kQOff = 0;
-constexpr int kPOff = kQOff + 2 * kHalf;
-constexpr int kStageOff = kPOff + 2 * kHalf;
-constexpr int kStageBytes = 4 * kHalf;  // K (two halves) + V (two halves)
-constexpr int kVOff = 2 * kHalf;        // V within a stage
-constexpr int kRedOff = kStageOff + 2 * kStageBytes;  // row max / sum exchange
+constexpr int kNK = 2;                  // K tiles in flight (freed as soon as their scores are done)
+constexpr int kNV = 3;                  // V tiles in flight (held until their PV product is done)
+constexpr int kTileBytes = 2 * kHalf;   // one K or V tile: 128 keys x 128 columns
+constexpr int kKOff = kQOff + 2 * kHalf;
+constexpr int kVOff = kKOff + kNK * kTileBytes;
+constexpr int kIdsOff = kVOff + kNV * kTileBytes;      // block ids of the tiles in flight
+constexpr int kRedOff = kIdsOff + 4 * 8 * 4;          // row max / sum exchange
 constexpr int kRedOff2 = kRedOff + 2 * 2 * 128 * 4;  // row-sum exchange
 constexpr int kBarOff = kRedOff2 + 2 * 128 * 4;
 constexpr int kSmemBytes = kBarOff + 256;
-constexpr uint32_t kTmemCols = 512;  // S0 [0,128), S1 [128,256), O [256,384)
+static_assert(kNK <= 3 && kNV <= 3, "barrier slots");
+constexpr uint32_t kTmemCols = 512;  // S0 [0,128), S1 [128,256), O [256,384), P0, P1
 constexpr uint32_t kTmemO = 256;
+constexpr uint32_t kTmemP = 384;     // P (bf16 pairs): 64 columns per buffer
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
 constexpr float kLn2 = 0.6931471805599453f;
 
@@ -102,14 +109,17 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* smem = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
   const uint32_t sbase = smem_u32(smem);
   const uint32_t bar_q = sbase + kBarOff;
-  const uint32_t bar_kv_full = bar_q + 8;    // [2]
-  const uint32_t bar_kv_empty = bar_q + 24;  // [2]
-  const uint32_t bar_s_full = bar_q + 40;    // [2]
-  const uint32_t bar_s_free = bar_q + 56;    // [2]
-  const uint32_t bar_p_full = bar_q + 72;
-  const uint32_t bar_o_done = bar_q + 80;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kBarOff + 96);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kBarOff + 100);
+  const uint32_t bar_k_full = bar_q + 8;     // [3] (kNK used)
+  const uint32_t bar_k_empty = bar_q + 32;   // [3]
+  const uint32_t bar_v_full = bar_q + 56;    // [3] (kNV used)
+  const uint32_t bar_v_empty = bar_q + 80;   // [3]
+  const uint32_t bar_s_full = bar_q + 104;   // [2]
+  const uint32_t bar_s_free = bar_q + 120;   // [2]
+  const uint32_t bar_p_full = bar_q + 136;   // [2]: softmax of even / odd tiles done
+  const uint32_t bar_o_done = bar_q + 152;   // [2]: PV of even / odd tiles done
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kBarOff + 168);
+  int* ids_smem = reinterpret_cast<int*>(smem + kIdsOff);      // [4 tiles][8 blocks]
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kBarOff + 172);
   float* red_max = reinterpret_cast<float*>(smem + kRedOff);   // [2 parity][2 half][128]
   float* red_sum = reinterpret_cast<float*>(smem + kRedOff2);  // [2 half][128]
 
@@ -142,14 +152,20 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (tid == 0) {
     mbar_init(bar_q, 1);
+    for (int k = 0; k < kNK; ++k) {
+      mbar_init(bar_k_full + 8 * k, 1);
+      mbar_init(bar_k_empty + 8 * k, 1);
+    }
+    for (int k = 0; k < kNV; ++k) {
+      mbar_init(bar_v_full + 8 * k, 1);
+      mbar_init(bar_v_empty + 8 * k, 1);
+    }
     for (int k = 0; k < 2; ++k) {
-      mbar_init(bar_kv_full + 8 * k, 1);
-      mbar_init(bar_kv_empty + 8 * k, 1);
       mbar_init(bar_s_full + 8 * k, 1);
       mbar_init(bar_s_free + 8 * k, kSoftmaxWarps);
+      mbar_init(bar_p_full + 8 * k, kSoftmaxWarps);
+      mbar_init(bar_o_done + 8 * k, 1);
     }
-    mbar_init(bar_p_full, kSoftmaxWarps);
-    mbar_init(bar_o_done, 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -174,34 +190,70 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int h = 0; h < 2; ++h)
         tma_load_3d(sbase + kQOff + h * kHalf, &tm_q, h * 64, kvh * G, q0 + t0, bar_q, pol);
     }
-    for (int j = 0; j < nkt; ++j) {
-      const int st = j & 1;
-      bool ok = true;
-      if (j >= 2 && lane == 0)
-        ok = wait_or_abort(bar_kv_empty + 8 * st, ((j >> 1) - 1) & 1, abort_flag, a.err);
-      if (__shfl_sync(0xffffffffu, ok ? 1 : 0, 0) == 0) break;
-      // tile j = paged blocks 8j .. 8j+7; blocks past the visible keys are read
-      // from outside the pool, which fills zeros
-      const uint32_t fb = bar_kv_full + 8 * st;
-      if (lane == 0) mbar_arrive_expect_tx(fb, kStageBytes);
+    // tile j = paged blocks 8j .. 8j+7 (their ids are read once, with the K
+    // tile, and kept for the V tile); blocks past the visible keys are read
+    // from outside the pool, which fills zeros
+    auto issue = [&](int j, bool is_k, uint32_t dst, uint32_t bar) {
+      if (lane == 0) mbar_arrive_expect_tx(bar, kTileBytes);
       __syncwarp();
       if (lane < 8) {
-        const int jb = j * 8 + lane;
-        int id = -1;
-        if (jb < nb_vis) {
-          id = a.block_tables[static_cast<long long>(c) * a.max_blocks + jb];
-          if (id < 0 || id >= a.num_blocks) {
-            atomicOr(a.err, PA_DEVERR_BLOCK_ID);
-            id = -1;
+        int id;
+        if (is_k) {
+          const int jb = j * 8 + lane;
+          id = -1;
+          if (jb < nb_vis) {
+            id = a.block_tables[static_cast<long long>(c) * a.max_blocks + jb];
+            if (id < 0 || id >= a.num_blocks) {
+              atomicOr(a.err, PA_DEVERR_BLOCK_ID);
+              id = -1;
+            }
           }
+          ids_smem[(j & 3) * 8 + lane] = id;
+        } else {
+          id = ids_smem[(j & 3) * 8 + lane];
         }
-        const uint32_t kd = sbase + kStageOff + st * kStageBytes + lane * kBlockSize * 128;
+        const uint32_t d = dst + lane * kBlockSize * 128;
         const int z = id * kBlockSize;
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          tma_load_3d(kd + h * kHalf, &tm_k, h * 64, kvh, z, fb, pol);
-          tma_load_3d(kd + kVOff + h * kHalf, &tm_v, h * 64, kvh, z, fb, pol);
+        for (int h = 0; h < 2; ++h)
+          tma_load_3d(d + h * kHalf, is_k ? &tm_k : &tm_v, h * 64, kvh, z, bar, pol);
+      }
+      __syncwarp();
+    };
+    int jk = 0, jv = 0;
+    uint64_t t_last = global_ns();  // time of the last issue
+    while ((jk < nkt || jv < nkt) && !*abort_flag) {
+      bool progressed = false;
+      if (jk < nkt && jk < jv + 4) {  // the id ring holds four tiles
+        const int slot = jk % kNK;
+        bool free_slot = jk < kNK;
+        if (!free_slot && lane == 0)
+          free_slot = mbar_test_wait(bar_k_empty + 8 * slot, ((jk / kNK) - 1) & 1);
+        if (__shfl_sync(0xffffffffu, free_slot ? 1 : 0, 0)) {
+          issue(jk, true, sbase + kKOff + slot * kTileBytes, bar_k_full + 8 * slot);
+          ++jk;
+          progressed = true;
         }
+      }
+      if (jv < jk) {
+        const int slot = jv % kNV;
+        bool free_slot = jv < kNV;
+        if (!free_slot && lane == 0)
+          free_slot = mbar_test_wait(bar_v_empty + 8 * slot, ((jv / kNV) - 1) & 1);
+        if (__shfl_sync(0xffffffffu, free_slot ? 1 : 0, 0)) {
+          issue(jv, false, sbase + kVOff + slot * kTileBytes, bar_v_full + 8 * slot);
+          ++jv;
+          progressed = true;
+        }
+      }
+      if (progressed) {
+        t_last = global_ns();
+      } else if (global_ns() - t_last > kWaitLimitNs) {
+        if (lane == 0) {
+          *abort_flag = 1;
+          atomicOr(a.err, PA_DEVERR_TIMEOUT);
+        }
+        break;
       }
     }
   } else if (warp == kMmaWarp) {
@@ -209,36 +261,51 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       const uint32_t idesc_s = instr_desc(0), idesc_o = instr_desc(1);
       bool ok = wait_or_abort(bar_q, 0, abort_flag, a.err);
-      for (int j = 0; ok && j <= nkt; ++j) {
-        if (j < nkt) {
-          const int b = j & 1;
-          const uint32_t stage = sbase + kStageOff + b * kStageBytes;
-          if (!wait_or_abort(bar_kv_full + 8 * b, (j >> 1) & 1, abort_flag, a.err)) break;
-          if (j >= 2 && !wait_or_abort(bar_s_free + 8 * b, ((j >> 1) - 1) & 1, abort_flag, a.err))
-            break;
+      int js = 0, jp = 0;  // next score tile / next PV product to issue
+      uint64_t t_last = global_ns();  // time of the last issue
+      while (ok && jp < nkt) {
+        bool progressed = false;
+        // S(js) = Q K_js^T into score buffer js & 1, once K_js landed and the
+        // softmax has read that buffer's previous tile
+        if (js < nkt && js <= jp + 1 &&
+            mbar_test_wait(bar_k_full + 8 * (js % kNK), (js / kNK) & 1) &&
+            (js < 2 || mbar_test_wait(bar_s_free + 8 * (js & 1), ((js >> 1) - 1) & 1))) {
           tc_fence_after();
+          const uint32_t kt = sbase + kKOff + (js % kNK) * kTileBytes;
 #pragma unroll
           for (int ks = 0; ks < 8; ++ks) {
             const uint32_t koff = (ks >> 2) * kHalf + (ks & 3) * 32;
-            tc_mma_f16(tmem + b * 128, smem_desc(sbase + kQOff + koff, 16, 1024),
-                       smem_desc(stage + koff, 16, 1024), idesc_s, ks > 0);
+            tc_mma_f16(tmem + (js & 1) * 128, smem_desc(sbase + kQOff + koff, 16, 1024),
+                       smem_desc(kt + koff, 16, 1024), idesc_s, ks > 0);
           }
-          tc_commit(bar_s_full + 8 * b);
+          tc_commit(bar_s_full + 8 * (js & 1));
+          tc_commit(bar_k_empty + 8 * (js % kNK));
+          ++js;
+          progressed = true;
         }
-        if (j >= 1) {
-          const int jp = j - 1;
-          const uint32_t stage = sbase + kStageOff + (jp & 1) * kStageBytes;
-          if (!wait_or_abort(bar_p_full, jp & 1, abort_flag, a.err)) break;
+        // O += P_jp V_jp once the softmax wrote P_jp and V_jp landed
+        if (jp < js && mbar_test_wait(bar_p_full + 8 * (jp & 1), (jp >> 1) & 1) &&
+            mbar_test_wait(bar_v_full + 8 * (jp % kNV), (jp / kNV) & 1)) {
           tc_fence_after();
+          const uint32_t vt = sbase + kVOff + (jp % kNV) * kTileBytes;
 #pragma unroll
-          for (int ks = 0; ks < 8; ++ks) {
-            const uint32_t poff = (ks >> 2) * kHalf + (ks & 3) * 32;
-            tc_mma_f16(tmem + kTmemO, smem_desc(sbase + kPOff + poff, 16, 1024),
-                       smem_desc(stage + kVOff + ks * 16 * 128, kHalf, 1024), idesc_o,
-                       (jp > 0 || ks > 0) ? 1u : 0u);
+          for (int ks = 0; ks < 8; ++ks)
+            tc_mma_f16_tmem_a(tmem + kTmemO, tmem + kTmemP + (jp & 1) * 64 + ks * 8,
+                              smem_desc(vt + ks * 16 * 128, kHalf, 1024), idesc_o,
+                              (jp > 0 || ks > 0) ? 1u : 0u);
+          tc_commit(bar_o_done + 8 * (jp & 1));
+          tc_commit(bar_v_empty + 8 * (jp % kNV));
+          ++jp;
+          progressed = true;
+        }
+        if (progressed) {
+          t_last = global_ns();
+        } else if (*abort_flag || global_ns() - t_last > kWaitLimitNs) {
+          if (!*abort_flag) {
+            *abort_flag = 1;
+            atomicOr(a.err, PA_DEVERR_TIMEOUT);
           }
-          tc_commit(bar_o_done);
-          tc_commit(bar_kv_empty + 8 * (jp & 1));
+          ok = false;
         }
       }
     }
@@ -256,22 +323,23 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int b = j & 1;
       wait_or_abort(bar_s_full + 8 * b, (j >> 1) & 1, abort_flag, a.err);
       tc_fence_after();
-      const uint32_t scol = tmem + lane_off + b * 128 + hc * 64;
-      {
-        uint32_t (&v0)[32] = *reinterpret_cast<uint32_t(*)[32]>(&v[0]);
-        uint32_t (&v1)[32] = *reinterpret_cast<uint32_t(*)[32]>(&v[32]);
-        tmem_ld32(scol, v0);
-        tmem_ld32(scol + 32, v1);
-      }
+      tmem_ld64(tmem + lane_off + b * 128 + hc * 64, v);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar_s_free + 8 * b);
 
       const int kb = j * kTileKeys + hc * 64;
-      float mloc = -INFINITY;
+      const int nvis = lim - kb + 1;  // visible columns of this half (may be <= 0 or > 64)
+      // eight independent partial maxima keep the dependency chains short
+      float mp[8];
+#pragma unroll
+      for (int k = 0; k < 8; ++k) mp[k] = -INFINITY;
 #pragma unroll
       for (int i = 0; i < 64; ++i)
-        if (kb + i <= lim) mloc = fmaxf(mloc, __uint_as_float(v[i]) * a.scale_log2);
+        if (i < nvis) mp[i & 7] = fmaxf(mp[i & 7], __uint_as_float(v[i]));
+      float mloc = fmaxf(fmaxf(fmaxf(mp[0], mp[1]), fmaxf(mp[2], mp[3])),
+                         fmaxf(fmaxf(mp[4], mp[5]), fmaxf(mp[6], mp[7])));
+      mloc = mloc * a.scale_log2;  // scale > 0 keeps the order
       red_max[(b * 2 + hc) * 128 + r] = mloc;
       named_barrier(1 + qd, 64);
       const float mx = fmaxf(mloc, red_max[(b * 2 + (hc ^ 1)) * 128 + r]);
@@ -279,23 +347,26 @@ __global__ void __launch_bounds__(kThreads, 1)
       const bool move = m_new > m_run + kRescaleThreshold;  // true on the first tile
       const float m_use = move ? m_new : m_run;
       const float alpha = move ? fast_exp2(m_run - m_use) : 1.f;
-      float rs = 0.f;
+      float rsp[4] = {0.f, 0.f, 0.f, 0.f};
       uint32_t pk[32];
+      const float sl = a.scale_log2;
 #pragma unroll
       for (int i = 0; i < 64; i += 2) {
-        const float x0 = kb + i <= lim ? __uint_as_float(v[i]) * a.scale_log2 : -INFINITY;
-        const float x1 = kb + i + 1 <= lim ? __uint_as_float(v[i + 1]) * a.scale_log2 : -INFINITY;
-        const float e0 = fast_exp2(x0 - m_use), e1 = fast_exp2(x1 - m_use);
-        rs += e0 + e1;
+        // p = 2^(scale*s - m): one FMA per score before the exp
+        const float e0 = i < nvis ? fast_exp2(fmaf(__uint_as_float(v[i]), sl, -m_use)) : 0.f;
+        const float e1 = i + 1 < nvis ? fast_exp2(fmaf(__uint_as_float(v[i + 1]), sl, -m_use)) : 0.f;
+        rsp[(i >> 1) & 3] += e0 + e1;
         pk[i / 2] = pack_bf16x2(e0, e1);
       }
+      const float rs = (rsp[0] + rsp[1]) + (rsp[2] + rsp[3]);
       l_run = l_run * alpha + rs;
       m_run = m_use;
 
-      // PV of the previous tile must be done before O and the P buffer change
-      if (j >= 1) wait_or_abort(bar_o_done, (j - 1) & 1, abort_flag, a.err);
-      tc_fence_after();
+      // O is rescaled only when a row maximum moved; then PV of the previous
+      // tile must have landed first
       if (j >= 1 && __any_sync(0xffffffffu, alpha != 1.f)) {
+        wait_or_abort(bar_o_done + 8 * ((j - 1) & 1), ((j - 1) >> 1) & 1, abort_flag, a.err);
+        tc_fence_after();
         const uint32_t ocol = tmem + lane_off + kTmemO + hc * 64;
 #pragma unroll
         for (int cc = 0; cc < 2; ++cc) {
@@ -306,28 +377,26 @@ __global__ void __launch_bounds__(kThreads, 1)
           tmem_st32(ocol + 32 * cc, w);
         }
       }
-      // P row r, keys hc*64 .. hc*64+63 = the K-major operand's half hc
-      const uint32_t prow = sbase + kPOff + hc * kHalf + r * 128;
-#pragma unroll
-      for (int ch = 0; ch < 8; ++ch) {
-        const uint32_t addr = prow + ((ch ^ (r & 7)) << 4);
-        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(pk[4 * ch]),
-                     "r"(pk[4 * ch + 1]), "r"(pk[4 * ch + 2]), "r"(pk[4 * ch + 3])
-                     : "memory");
+      // P buffer j & 1 is free once PV of tile j-2 has read it
+      if (j >= 2) {
+        wait_or_abort(bar_o_done + 8 * (j & 1), ((j >> 1) - 1) & 1, abort_flag, a.err);
+        tc_fence_after();
       }
+      // keys hc*64 .. hc*64+63 of row r = columns hc*32 .. +31 of P buffer j & 1
+      tmem_st32(tmem + lane_off + kTmemP + (j & 1) * 64 + hc * 32, pk);
       // the sequence's last block may end inside this tile: its slots past
       // seq_len hold no token and must not reach the PV product
       if ((n & (kBlockSize - 1)) != 0) {
         const int jl = (n - 1) / kBlockSize;
         if (jl < nb_vis && jl / 8 == j) {
-          wait_or_abort(bar_kv_full + 8 * b, (j >> 1) & 1, abort_flag, a.err);
-          const uint32_t stage = sbase + kStageOff + b * kStageBytes;
+          wait_or_abort(bar_v_full + 8 * (j % kNV), (j / kNV) & 1, abort_flag, a.err);
+          const uint32_t vt = sbase + kVOff + (j % kNV) * kTileBytes;
           const int first = n - jl * kBlockSize;  // rows first..15 of block jl % 8
           const int rows = kBlockSize - first;
           for (int e = tid; e < rows * 2 * 8; e += kSoftmaxWarps * 32) {
             const int row = first + e / 16, h = (e / 8) & 1, chunk = e & 7;
             const uint32_t addr =
-                stage + kVOff + h * kHalf + ((jl & 7) * kBlockSize + row) * 128 + (chunk << 4);
+                vt + h * kHalf + ((jl & 7) * kBlockSize + row) * 128 + (chunk << 4);
             asm volatile("st.shared.v4.b32 [%0], {%1, %1, %1, %1};" ::"r"(addr), "r"(0u)
                          : "memory");
           }
@@ -336,11 +405,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       fence_proxy_async_smem();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(bar_p_full);
+      if (lane == 0) mbar_arrive(bar_p_full + 8 * (j & 1));
     }
 
     // ---- epilogue: O / l -> bf16, and lse
-    wait_or_abort(bar_o_done, (nkt - 1) & 1, abort_flag, a.err);
+    wait_or_abort(bar_o_done + 8 * ((nkt - 1) & 1), ((nkt - 1) >> 1) & 1, abort_flag, a.err);
     tc_fence_after();
     red_sum[hc * 128 + r] = l_run;
     named_barrier(1 + qd, 64);
