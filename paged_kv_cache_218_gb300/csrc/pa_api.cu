@@ -64,12 +64,24 @@ bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p
 
 // Paged pool [num_blocks * 16 tokens, Hkv, D] as a 3-D tensor; box = 64
 // columns x 1 head x `rows` tokens, 128-byte swizzle.
+// rows > 0: box = 64 columns x 1 head x `rows` tokens (one head of a block).
+// rows == 0: the same pool seen as (D, tokens, heads), box = 64 columns x 16
+// tokens x Hkv heads -- one whole block, every head, in a single load that
+// lands as [head][token][64 columns].
 int encode_pool_map_uncached(CUtensorMap* m, const void* pool, int64_t num_blocks, int Hkv, int D,
                              int rows) {
   cuuint64_t dims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(Hkv),
                         static_cast<cuuint64_t>(num_blocks) * kBlockSize};
   cuuint64_t strides[2] = {static_cast<cuuint64_t>(D) * 2, static_cast<cuuint64_t>(Hkv) * D * 2};
   cuuint32_t box[3] = {64, 1, static_cast<cuuint32_t>(rows)};
+  if (rows == 0) {
+    dims[1] = static_cast<cuuint64_t>(num_blocks) * kBlockSize;
+    dims[2] = static_cast<cuuint64_t>(Hkv);
+    strides[0] = static_cast<cuuint64_t>(Hkv) * D * 2;
+    strides[1] = static_cast<cuuint64_t>(D) * 2;
+    box[1] = kBlockSize;
+    box[2] = static_cast<cuuint32_t>(Hkv);
+  }
   cuuint32_t estr[3] = {1, 1, 1};
   CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(pool), dims,
                         strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
@@ -426,8 +438,8 @@ int pa_decode(void* out, const void* q, const void* k_cache, const void* v_cache
   }
 
   CUtensorMap tm_k, tm_v;
-  if (encode_pool_map(&tm_k, k_cache, num_blocks, num_kv_heads, head_dim, kBlockSize) ||
-      encode_pool_map(&tm_v, v_cache, num_blocks, num_kv_heads, head_dim, kBlockSize))
+  if (encode_pool_map(&tm_k, k_cache, num_blocks, num_kv_heads, head_dim, 0) ||
+      encode_pool_map(&tm_v, v_cache, num_blocks, num_kv_heads, head_dim, 0))
     return PA_ERR_CUDA;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (launch_decode(a, &tm_k, &tm_v, head_dim, grid, st) != cudaSuccess) return PA_ERR_CUDA;

@@ -10,9 +10,11 @@
 //    contiguous in the pool -- is streamed as a whole (DRAM-page friendly).
 //  * The producer walks the CTA's pieces, prefetches block-table rows 32
 //    entries at a time, and lands each block in a ring of shared-memory
-//    stages with TMA tensor loads: per kv head, K and V as 64-column boxes of
-//    16 token rows, 128-byte swizzled so warp-level matrix loads are
-//    bank-conflict free.  One mbarrier per stage counts the bytes in.
+//    stages with TMA tensor loads: for K and for V, one box per 64-column
+//    half covering 16 tokens x every kv head (the pool is described to TMA as
+//    (columns, tokens, heads), so a box lands as [head][token][64 columns]),
+//    128-byte swizzled so warp-level matrix loads are bank-conflict free.
+//    One mbarrier per stage counts the bytes in.
 //  * Consumer warps map to kv heads (with Hkv < 8, several warps share a head
 //    and split its blocks).  GQA: the group's q heads are the N=8 columns of
 //    a warp MMA, so each K/V byte loaded serves every q head of its group:
@@ -163,13 +165,15 @@ __device__ __forceinline__ int load_ids(const DecodeArgs& a, int s, int jb, int 
 }
 
 // Address of the 16-byte chunk `chunk` (8 bf16) of token row `tok` in one
-// head's block, staged as 128-byte-swizzled boxes of 16 rows x 64 columns.
-__device__ __forceinline__ uint32_t swz(uint32_t base, int tok, int chunk) {
-  return base + (chunk >> 3) * kBoxBytes + tok * 128 + (((chunk & 7) ^ (tok & 7)) << 4);
+// head's block.  A stage holds, for K and then for V, one 128-byte-swizzled
+// box per 64-column half covering [head][16 tokens][64 columns]; `half` is
+// the distance between the two halves (Hkv x 16 rows x 128 B).
+__device__ __forceinline__ uint32_t swz(uint32_t base, int tok, int chunk, uint32_t half) {
+  return base + (chunk >> 3) * half + tok * 128 + (((chunk & 7) ^ (tok & 7)) << 4);
 }
 
 template <int D>
-__device__ __forceinline__ void attend_block(uint32_t kbase, uint32_t vbase,
+__device__ __forceinline__ void attend_block(uint32_t kbase, uint32_t vbase, uint32_t half,
                                              const uint32_t (&qf)[D / 16][2],
                                              float (&o)[D / 16][4], float& m0, float& m1,
                                              float& l0, float& l1, int valid, float scale_log2,
@@ -182,8 +186,8 @@ __device__ __forceinline__ void attend_block(uint32_t kbase, uint32_t vbase,
 #pragma unroll
   for (int ks = 0; ks < KS; ks += 2) {
     uint32_t a0[4], a1[4];
-    ldsm_x4(swz(kbase, ktok, ks * 2 + (i >> 1)), a0);
-    ldsm_x4(swz(kbase, ktok, (ks + 1) * 2 + (i >> 1)), a1);
+    ldsm_x4(swz(kbase, ktok, ks * 2 + (i >> 1), half), a0);
+    ldsm_x4(swz(kbase, ktok, (ks + 1) * 2 + (i >> 1), half), a1);
     mma_bf16_16816(sa, a0, qf[ks][0], qf[ks][1]);
     mma_bf16_16816(sb, a1, qf[ks + 1][0], qf[ks + 1][1]);
   }
@@ -228,7 +232,7 @@ __device__ __forceinline__ void attend_block(uint32_t kbase, uint32_t vbase,
 #pragma unroll
   for (int mt = 0; mt < KS; ++mt) {
     uint32_t a[4];
-    ldsm_x4_trans(swz(vbase, vtok, mt * 2 + (i & 1)), a);
+    ldsm_x4_trans(swz(vbase, vtok, mt * 2 + (i & 1), half), a);
     a[0] &= keep01;
     a[1] &= keep01;
     a[2] &= keep23;
@@ -454,14 +458,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
         if (!ok) break;
-        if (lane < Hkv) {
-          const uint32_t kdst = sbase + st * L.stage_bytes + lane * L.head_bytes;
+        if (lane == 0) {
+          // one box per 64-column half: 16 tokens x every kv head of the block
+          const uint32_t kdst = sbase + st * L.stage_bytes;
           const uint32_t vdst = kdst + Hkv * L.head_bytes;
-          const int z = blk * kBlockSize;
+          const int y = blk * kBlockSize;
 #pragma unroll
           for (int h = 0; h < D / 64; ++h) {
-            tma_load_3d(kdst + h * kBoxBytes, &tm_k, h * 64, lane, z, fb, pol);
-            tma_load_3d(vdst + h * kBoxBytes, &tm_v, h * 64, lane, z, fb, pol);
+            tma_load_3d(kdst + h * Hkv * kBoxBytes, &tm_k, h * 64, y, 0, fb, pol);
+            tma_load_3d(vdst + h * Hkv * kBoxBytes, &tm_v, h * 64, y, 0, fb, pol);
           }
         }
       }
@@ -551,9 +556,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           continue;
         }
         const int valid = min(kBlockSize, pc.len - j * kBlockSize);
-        const uint32_t kb = sbase + st * L.stage_bytes + hw * L.head_bytes;
-        attend_block<D>(kb, kb + Hkv * L.head_bytes, qf, o, m0, m1, l0, l1, valid,
-                        a.scale_log2, lane);
+        const uint32_t kb = sbase + st * L.stage_bytes + hw * kBoxBytes;
+        attend_block<D>(kb, kb + Hkv * L.head_bytes, Hkv * kBoxBytes, qf, o, m0, m1, l0, l1,
+                        valid, a.scale_log2, lane);
         __syncwarp();
         if (lane == 0) mbar_arrive(bar_empty + st * 8);
       }
