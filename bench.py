@@ -135,6 +135,20 @@ class ClockSampler:
                 "samples": len(sms), "reasons": sorted(reasons)}
 
 
+def reduce_over_ranks(elapsed_ms, units, device=None):
+    """Slowest rank's elapsed time and the units (bytes, tokens) of all ranks;
+    the identity when torch.distributed is not initialised or has one rank."""
+    import torch
+    import torch.distributed as tdist
+    if not (tdist.is_available() and tdist.is_initialized()) or tdist.get_world_size() == 1:
+        return float(elapsed_ms), float(units)
+    t = torch.tensor([float(elapsed_ms)], dtype=torch.float64, device=device)
+    u = torch.tensor([float(units)], dtype=torch.float64, device=device)
+    tdist.all_reduce(t, op=tdist.ReduceOp.MAX)
+    tdist.all_reduce(u, op=tdist.ReduceOp.SUM)
+    return float(t.item()), float(u.item())
+
+
 # ----------------------------------------------------------------------------- workload
 
 def make_workload(name):
@@ -306,11 +320,7 @@ def run_gpu(args, rank, world, local_rank):
     if dist:
         tdist.barrier()
     clocks = sampler.stop()
-    elapsed_ms = t_start.elapsed_time(t_end)
-    if dist:
-        t = torch.tensor([elapsed_ms], dtype=torch.float64, device=dev)
-        tdist.all_reduce(t, op=tdist.ReduceOp.MAX)
-        elapsed_ms = float(t.item())
+    elapsed_ms, kv_all = reduce_over_ranks(t_start.elapsed_time(t_end), kv_bytes_decode(w) * K, dev)
     if use_graphs:
         # the decode kernel alone: CUDA events on the launching stream around
         # back-to-back decode-graph replays (one kernel each)
@@ -332,8 +342,8 @@ def run_gpu(args, rank, world, local_rank):
         raise RuntimeError(f"device error flags {flags} after the timed region")
 
     e2e = run_e2e(args, w, reps, ws, dev, pa, dist)
-    return dict(w=w, elapsed_ms=elapsed_ms, dec_ms=dec_ms, chunk_ms=chunk_ms, clocks=clocks,
-                e2e=e2e, launches=launches_per_step * K, graphs=use_graphs)
+    return dict(w=w, elapsed_ms=elapsed_ms, kv_all=kv_all, dec_ms=dec_ms, chunk_ms=chunk_ms,
+                clocks=clocks, e2e=e2e, launches=launches_per_step * K, graphs=use_graphs)
 
 
 def run_e2e(args, w, reps, ws, dev, pa, dist):
@@ -374,12 +384,8 @@ def run_e2e(args, w, reps, ws, dev, pa, dist):
         step(i)
     b.record(main)
     torch.cuda.synchronize()
-    ms = a.elapsed_time(b)
-    if dist:
-        t = torch.tensor([ms], dtype=torch.float64, device=dev)
-        tdist.all_reduce(t, op=tdist.ReduceOp.MAX)
-        ms = float(t.item())
-    return dict(ms=ms, steps=K, h2d=h2d, d2h=d2h)
+    ms, kv_all = reduce_over_ranks(a.elapsed_time(b), kv_bytes_decode(w) * K, dev)
+    return dict(ms=ms, steps=K, h2d=h2d, d2h=d2h, kv_all=kv_all)
 
 
 def run_oracle(w, min_seconds):
@@ -499,7 +505,7 @@ def main():
     K = args.steps
     kvb = kv_bytes_decode(w)
     step_ms = res["elapsed_ms"] / K
-    value = kvb * world * K / (res["elapsed_ms"] * 1e-3) / 1e9
+    value = res["kv_all"] / (res["elapsed_ms"] * 1e-3) / 1e9
     alg = decode_algorithmic_bytes(w)
     achieved = alg / (res["dec_ms"] * 1e-3) / 1e9
     traffic = profile_traffic(["pa_decode.cu", "pa_ptx.cuh", "pa_internal.h"],
@@ -527,7 +533,7 @@ def main():
                      "launch_timing": ("CUDA events on the launching stream around back-to-back "
                                        "decode-only graph replays") if res["graphs"]
                                       else "CUDA events around each decode launch in the timed region"},
-        "e2e": {"value": kvb * world * e["steps"] / (e["ms"] * 1e-3) / 1e9, "unit": "GB/s",
+        "e2e": {"value": e["kv_all"] / (e["ms"] * 1e-3) / 1e9, "unit": "GB/s",
                 "h2d_bytes_per_step": e["h2d"], "d2h_bytes_per_step": e["d2h"],
                 "steps": e["steps"], "ms_per_step": e["ms"] / e["steps"]},
         "gpu_launches": res["launches"],
