@@ -330,13 +330,20 @@ __global__ void __launch_bounds__(kThreads, 1)
 
       const int kb = j * kTileKeys + hc * 64;
       const int nvis = lim - kb + 1;  // visible columns of this half (may be <= 0 or > 64)
-      // eight independent partial maxima keep the dependency chains short
+      // eight independent partial maxima keep the dependency chains short; a
+      // warp whose rows all see the whole half skips the per-element masks
+      const bool full = __all_sync(0xffffffffu, nvis >= 64);
       float mp[8];
 #pragma unroll
       for (int k = 0; k < 8; ++k) mp[k] = -INFINITY;
+      if (full) {
 #pragma unroll
-      for (int i = 0; i < 64; ++i)
-        if (i < nvis) mp[i & 7] = fmaxf(mp[i & 7], __uint_as_float(v[i]));
+        for (int i = 0; i < 64; ++i) mp[i & 7] = fmaxf(mp[i & 7], __uint_as_float(v[i]));
+      } else {
+#pragma unroll
+        for (int i = 0; i < 64; ++i)
+          if (i < nvis) mp[i & 7] = fmaxf(mp[i & 7], __uint_as_float(v[i]));
+      }
       float mloc = fmaxf(fmaxf(fmaxf(mp[0], mp[1]), fmaxf(mp[2], mp[3])),
                          fmaxf(fmaxf(mp[4], mp[5]), fmaxf(mp[6], mp[7])));
       mloc = mloc * a.scale_log2;  // scale > 0 keeps the order
@@ -350,13 +357,24 @@ __global__ void __launch_bounds__(kThreads, 1)
       float rsp[4] = {0.f, 0.f, 0.f, 0.f};
       uint32_t pk[32];
       const float sl = a.scale_log2;
+      if (full) {
 #pragma unroll
-      for (int i = 0; i < 64; i += 2) {
-        // p = 2^(scale*s - m): one FMA per score before the exp
-        const float e0 = i < nvis ? fast_exp2(fmaf(__uint_as_float(v[i]), sl, -m_use)) : 0.f;
-        const float e1 = i + 1 < nvis ? fast_exp2(fmaf(__uint_as_float(v[i + 1]), sl, -m_use)) : 0.f;
-        rsp[(i >> 1) & 3] += e0 + e1;
-        pk[i / 2] = pack_bf16x2(e0, e1);
+        for (int i = 0; i < 64; i += 2) {
+          // p = 2^(scale*s - m): one FMA per score before the exp
+          const float e0 = fast_exp2(fmaf(__uint_as_float(v[i]), sl, -m_use));
+          const float e1 = fast_exp2(fmaf(__uint_as_float(v[i + 1]), sl, -m_use));
+          rsp[(i >> 1) & 3] += e0 + e1;
+          pk[i / 2] = pack_bf16x2(e0, e1);
+        }
+      } else {
+#pragma unroll
+        for (int i = 0; i < 64; i += 2) {
+          const float e0 = i < nvis ? fast_exp2(fmaf(__uint_as_float(v[i]), sl, -m_use)) : 0.f;
+          const float e1 =
+              i + 1 < nvis ? fast_exp2(fmaf(__uint_as_float(v[i + 1]), sl, -m_use)) : 0.f;
+          rsp[(i >> 1) & 3] += e0 + e1;
+          pk[i / 2] = pack_bf16x2(e0, e1);
+        }
       }
       const float rs = (rsp[0] + rsp[1]) + (rsp[2] + rsp[3]);
       l_run = l_run * alpha + rs;
