@@ -573,6 +573,8 @@ int pa_prefill_chunk(void* out, const void* q, const void* k_cache, const void* 
   a.group = group;
   const int tokens_per_tile = 128 / group;
   a.tiles_per_chunk = (max_q_len + tokens_per_tile - 1) / tokens_per_tile;
+  const int cl = prefill_cluster();
+  a.tiles_per_chunk = (a.tiles_per_chunk + cl - 1) / cl * cl;
   a.scale_log2 = scale * 1.4426950408889634f;
   CUtensorMap tm_q, tm_k, tm_v;
   if (encode_q_map(&tm_q, q, total_q_tokens, num_q_heads, head_dim, group, tokens_per_tile) ||

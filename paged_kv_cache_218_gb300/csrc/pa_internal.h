@@ -92,5 +92,6 @@ cudaError_t launch_merge(const MergeArgs& a, cudaStream_t stream);
 cudaError_t launch_prefill(const PrefillArgs& a, const CUtensorMap* tm_q, const CUtensorMap* tm_k,
                            const CUtensorMap* tm_v, int grid_tiles, cudaStream_t stream);
 size_t prefill_smem_bytes();
+int prefill_cluster();  // query tiles per cluster (the grid is a multiple of it)
 
 }  // namespace pa

@@ -10,7 +10,11 @@
 //
 //  * One CTA per (128-row query tile, chunk, kv head).  GQA packs the group's
 //    q heads into the rows: row r = token (r / G), head (r % G), so each K/V
-//    tile serves all G heads (128 / G tokens per tile).
+//    tile serves all G heads (128 / G tokens per tile).  Four consecutive
+//    query tiles of the same kv head form a cluster and share every K/V tile:
+//    each CTA loads a quarter of a tile's paged blocks with TMA multicast into
+//    all four, so each SM issues a quarter of the loads (the per-SM TMA
+//    request rate, not bandwidth, bounds this pipeline).
 //  * Warp roles.  Warp 9 loads: Q once, then K and V tiles of 128 keys, each
 //    assembled from eight 16-token paged blocks by TMA (128-byte swizzle), in
 //    rings of two K and three V tiles (a K tile is free once its scores are
@@ -44,6 +48,7 @@
 namespace pa {
 namespace {
 
+constexpr int kCluster = 4;   // query tiles of one kv head sharing every K/V tile load
 constexpr int kSoftmaxWarps = 8;
 constexpr int kMmaWarp = 8;
 constexpr int kLoadWarp = 9;
@@ -126,10 +131,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int Hkv = a.num_kv_heads, G = a.group;
   const int tpt = kTileKeys / G;  // query tokens per tile
-  const int kvh = blockIdx.x % Hkv;
-  const int t2 = blockIdx.x / Hkv;
-  const int c = t2 % a.num_chunks;
-  const int m = t2 / a.num_chunks;
+  const int rank = static_cast<int>(blockIdx.x % kCluster);  // rank in the cluster
+  const int rest = static_cast<int>(blockIdx.x / kCluster);
+  const int kvh = rest % Hkv;
+  const int t3 = rest / Hkv;
+  const int c = t3 % a.num_chunks;
+  const int mg = t3 / a.num_chunks;  // cluster index along the chunk
+  const int m = mg * kCluster + rank;
+  constexpr uint16_t kMask = (1u << kCluster) - 1;
 
   // launched as a programmatic dependent of the previous kernel (the scatter
   // of this step's K/V): nothing before this line touches global memory
@@ -144,9 +153,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     return;
   }
   const int t0 = m * tpt;
-  if (t0 >= qlen) return;
-  const int tv = min(tpt, qlen - t0);  // valid query tokens in this tile
-  const int kmax = p0 + t0 + tv;       // keys [0, kmax) are visible to some row
+  const int tc0 = mg * kCluster * tpt;  // first query token of the cluster
+  if (tc0 >= qlen) return;              // the whole cluster is past the chunk
+  const int tv = qlen - t0 < tpt ? qlen - t0 : tpt;  // valid tokens here (<= 0: none)
+  // keys [0, kmax) are visible to some row of the cluster; every member walks
+  // the same tiles (its own rows mask what they may not see)
+  const int kmax = p0 + min(qlen, tc0 + kCluster * tpt);
   const int nkt = (kmax + kTileKeys - 1) / kTileKeys;
   const int nb_vis = (kmax + kBlockSize - 1) / kBlockSize;
 
@@ -154,11 +166,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(bar_q, 1);
     for (int k = 0; k < kNK; ++k) {
       mbar_init(bar_k_full + 8 * k, 1);
-      mbar_init(bar_k_empty + 8 * k, 1);
+      mbar_init(bar_k_empty + 8 * k, kCluster);  // released by every member of the cluster
     }
     for (int k = 0; k < kNV; ++k) {
       mbar_init(bar_v_full + 8 * k, 1);
-      mbar_init(bar_v_empty + 8 * k, 1);
+      mbar_init(bar_v_empty + 8 * k, kCluster);
     }
     for (int k = 0; k < 2; ++k) {
       mbar_init(bar_s_full + 8 * k, 1);
@@ -174,7 +186,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     tmem_relinquish();
   }
   tc_fence_before();
-  __syncthreads();
+  cluster_sync();  // every member's barriers exist before any multicast reaches them
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
@@ -194,12 +206,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     // tile, and kept for the V tile); blocks past the visible keys are read
     // from outside the pool, which fills zeros
     auto issue = [&](int j, bool is_k, uint32_t dst, uint32_t bar) {
-      if (lane == 0) mbar_arrive_expect_tx(bar, kTileBytes);
+      if (lane == 0) mbar_arrive_expect_tx(bar, kTileBytes);  // the whole tile lands here
       __syncwarp();
-      if (lane < 8) {
+      if (lane < 8 / kCluster) {
+        const int bl = lane * kCluster + rank;  // this CTA's share of the tile's blocks
         int id;
         if (is_k) {
-          const int jb = j * 8 + lane;
+          const int jb = j * 8 + bl;
           id = -1;
           if (jb < nb_vis) {
             id = a.block_tables[static_cast<long long>(c) * a.max_blocks + jb];
@@ -208,15 +221,16 @@ __global__ void __launch_bounds__(kThreads, 1)
               id = -1;
             }
           }
-          ids_smem[(j & 3) * 8 + lane] = id;
+          ids_smem[(j & 3) * 8 + bl] = id;
         } else {
-          id = ids_smem[(j & 3) * 8 + lane];
+          id = ids_smem[(j & 3) * 8 + bl];
         }
-        const uint32_t d = dst + lane * kBlockSize * 128;
+        const uint32_t d = dst + bl * kBlockSize * 128;
         const int z = id * kBlockSize;
 #pragma unroll
         for (int h = 0; h < 2; ++h)
-          tma_load_3d(d + h * kHalf, is_k ? &tm_k : &tm_v, h * 64, kvh, z, bar, pol);
+          tma_load_3d_multicast(d + h * kHalf, is_k ? &tm_k : &tm_v, h * 64, kvh, z, bar, kMask,
+                                pol);
       }
       __syncwarp();
     };
@@ -256,6 +270,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         break;
       }
     }
+    // every member's release of the last fill of each slot has reached this
+    // CTA before it may leave the cluster
+    if (lane == 0) {
+      for (int sl = 0; sl < kNK && sl < nkt; ++sl)
+        wait_or_abort(bar_k_empty + 8 * sl, ((nkt - 1 - sl) / kNK) & 1, abort_flag, a.err);
+      for (int sl = 0; sl < kNV && sl < nkt; ++sl)
+        wait_or_abort(bar_v_empty + 8 * sl, ((nkt - 1 - sl) / kNV) & 1, abort_flag, a.err);
+    }
+    __syncwarp();
   } else if (warp == kMmaWarp) {
     // ------------------------------------------------------------ tensor-core issue
     if (lane == 0) {
@@ -267,8 +290,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         bool progressed = false;
         // S(js) = Q K_js^T into score buffer js & 1, once K_js landed and the
         // softmax has read that buffer's previous tile
-        if (js < nkt && js <= jp + 1 &&
-            mbar_test_wait(bar_k_full + 8 * (js % kNK), (js / kNK) & 1) &&
+        if (js < nkt && mbar_test_wait(bar_k_full + 8 * (js % kNK), (js / kNK) & 1) &&
             (js < 2 || mbar_test_wait(bar_s_free + 8 * (js & 1), ((js >> 1) - 1) & 1))) {
           tc_fence_after();
           const uint32_t kt = sbase + kKOff + (js % kNK) * kTileBytes;
@@ -279,7 +301,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                        smem_desc(kt + koff, 16, 1024), idesc_s, ks > 0);
           }
           tc_commit(bar_s_full + 8 * (js & 1));
-          tc_commit(bar_k_empty + 8 * (js % kNK));
+          tc_commit_multicast(bar_k_empty + 8 * (js % kNK), kMask);
           ++js;
           progressed = true;
         }
@@ -294,7 +316,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                               smem_desc(vt + ks * 16 * 128, kHalf, 1024), idesc_o,
                               (jp > 0 || ks > 0) ? 1u : 0u);
           tc_commit(bar_o_done + 8 * (jp & 1));
-          tc_commit(bar_v_empty + 8 * (jp % kNV));
+          tc_commit_multicast(bar_v_empty + 8 * (jp % kNV), kMask);
           ++jp;
           progressed = true;
         }
@@ -456,13 +478,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       a.out_lse[row] = l_tot > 0.f ? (m_run + __log2f(l_tot)) * kLn2 : -INFINITY;
   }
   tc_fence_before();
-  __syncthreads();
+  cluster_sync();  // no member leaves while a partner may still write to it
   if (warp == 0) tmem_dealloc(tmem, kTmemCols);
 }
 
 }  // namespace
 
 size_t prefill_smem_bytes() { return kSmemBytes + 1024; }
+
+int prefill_cluster() { return kCluster; }
 
 cudaError_t launch_prefill(const PrefillArgs& a, const CUtensorMap* tm_q, const CUtensorMap* tm_k,
                            const CUtensorMap* tm_v, int grid_tiles, cudaStream_t stream) {
@@ -491,11 +515,15 @@ cudaError_t launch_prefill(const PrefillArgs& a, const CUtensorMap* tm_q, const 
   cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributeClusterDimension;
+  attr[1].val.clusterDim.x = kCluster;
+  attr[1].val.clusterDim.y = 1;
+  attr[1].val.clusterDim.z = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 2;
   e = cudaLaunchKernelEx(&cfg, prefill_kernel, *tm_q, *tm_k, *tm_v, a);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
