@@ -246,9 +246,10 @@ def run_gpu(args, rank, world, local_rank):
 
     def step(i, ev=None, cev=None):
         r = reps[i % R]
+        cur = torch.cuda.current_stream()
         pa.pa_reshape_and_cache(r.key, r.value, r.k_cache, r.v_cache, r.slot_mapping)
         if hybrid:
-            s_chunk.wait_stream(main)
+            s_chunk.wait_stream(cur)
             if cev is not None:
                 cev[0].record(s_chunk)
             pa.pa_prefill_chunk(r.out_chunk, r.q[:T], r.k_cache, r.v_cache,
@@ -257,12 +258,18 @@ def run_gpu(args, rank, world, local_rank):
             if cev is not None:
                 cev[1].record(s_chunk)
         if ev is not None:
-            ev[0].record(main)
+            ev[0].record(cur)
         pa.pa_decode(*decode_args(w, r), w.scale, partition_tokens=P, workspace=ws[i % R])
         if ev is not None:
-            ev[1].record(main)
+            ev[1].record(cur)
         if hybrid:
-            main.wait_stream(s_chunk)
+            cur.wait_stream(s_chunk)
+
+    def chunk_only(i):
+        r = reps[i % R]
+        pa.pa_prefill_chunk(r.out_chunk, r.q[:T], r.k_cache, r.v_cache,
+                            r.block_tables[:w.num_chunks], r.cu, r.qs,
+                            r.seq_lens[:w.num_chunks], max_q, w.scale)
 
     for i in range(args.warmup):
         step(i)
@@ -270,23 +277,33 @@ def run_gpu(args, rank, world, local_rank):
     if pa.pa_device_error_flags() != 0:
         raise RuntimeError("device error flags set during warm-up")
 
-    # Decode-only steps replay one CUDA graph per replica (scatter, then decode
-    # as its programmatic dependent): the same kernels with the same inputs,
-    # without the per-launch host cost of the Python binding.
-    use_graphs = not hybrid and not args.no_graphs
-    g_step, g_dec = [], []
+    # Graph replay: one CUDA graph per round of R steps (every replica's
+    # scatter, then its decode; the hybrid step forks the prefill chunk onto a
+    # second stream), each kernel a programmatic dependent of the one before,
+    # so consecutive kernels overlap launch and prologue with the previous
+    # one's drain.  Single-step graphs cover a remainder of K mod R steps.
+    use_graphs = not args.no_graphs
     if use_graphs:
-        for r in range(R):
+        g_round, g_dec_round, g_chunk_round = (torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph(),
+                                               torch.cuda.CUDAGraph() if hybrid else None)
+        with torch.cuda.graph(g_round):
+            for r in range(R):
+                step(r)
+        with torch.cuda.graph(g_dec_round):
+            for r in range(R):
+                pa.pa_decode(*decode_args(w, reps[r]), w.scale, partition_tokens=P, workspace=ws[r])
+        if hybrid:
+            with torch.cuda.graph(g_chunk_round):
+                for r in range(R):
+                    chunk_only(r)
+        g_step = []
+        for r in range(args.steps % R):
             g1 = torch.cuda.CUDAGraph()
             with torch.cuda.graph(g1):
                 step(r)
-            g2 = torch.cuda.CUDAGraph()
-            with torch.cuda.graph(g2):
-                pa.pa_decode(*decode_args(w, reps[r]), w.scale, partition_tokens=P, workspace=ws[r])
             g_step.append(g1)
-            g_dec.append(g2)
-        for i in range(args.warmup):
-            g_step[i % R].replay()
+        for i in range(max(1, args.warmup // R)):
+            g_round.replay()
         torch.cuda.synchronize()
 
     dist = world > 1
@@ -310,8 +327,10 @@ def run_gpu(args, rank, world, local_rank):
     torch.cuda.synchronize()
     t_start.record(main)
     if use_graphs:
-        for i in range(K):
-            g_step[i % R].replay()
+        for _ in range(K // R):
+            g_round.replay()
+        for g1 in g_step:
+            g1.replay()
     else:
         for i in range(K):
             step(i, evs[i], cevs[i])
@@ -321,22 +340,26 @@ def run_gpu(args, rank, world, local_rank):
         tdist.barrier()
     clocks = sampler.stop()
     elapsed_ms, kv_all = reduce_over_ranks(t_start.elapsed_time(t_end), kv_bytes_decode(w) * K, dev)
+
+    def back_to_back(g, n_launch):
+        # CUDA events on the launching stream around n rounds of R launches
+        n = max(1, n_launch // R)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        a.record(main)
+        for _ in range(n):
+            g.replay()
+        b.record(main)
+        torch.cuda.synchronize()
+        return a.elapsed_time(b) / (n * R)
+
     if use_graphs:
-        # the decode kernel alone: CUDA events on the launching stream around
-        # back-to-back decode-graph replays (one kernel each)
         K2 = min(K, args.kernel_steps)
-        kev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-               for _ in range(K2)]
-        torch.cuda.synchronize()
-        for i in range(K2):
-            kev[i][0].record(main)
-            g_dec[i % R].replay()
-            kev[i][1].record(main)
-        torch.cuda.synchronize()
-        dec_ms = sum(a.elapsed_time(b) for a, b in kev) / K2
+        dec_ms = back_to_back(g_dec_round, K2)
+        chunk_ms = back_to_back(g_chunk_round, K2) if hybrid else None
     else:
         dec_ms = sum(a.elapsed_time(b) for a, b in evs) / K
-    chunk_ms = sum(a.elapsed_time(b) for a, b in cevs) / K if hybrid else None
+        chunk_ms = sum(a.elapsed_time(b) for a, b in cevs) / K if hybrid else None
     flags = pa.pa_device_error_flags()
     if flags:
         raise RuntimeError(f"device error flags {flags} after the timed region")
@@ -522,7 +545,9 @@ def main():
                    "l2": f"{args.replicas} independent KV pools in rotation "
                          f"({args.replicas * 2 * w.k_cache.nbytes / 1e9:.2f} GB) >> 129 MB L2",
                    "parallelism": f"replicas x{world}",
-                   "launch": "CUDA graph per replica (scatter + decode)" if res["graphs"]
+                   "launch": (f"CUDA graph per round of {args.replicas} steps (scatter, "
+                              + ("prefill chunk on a second stream, " if w.num_chunks else "")
+                              + "decode; programmatic dependent launches)") if res["graphs"]
                              else "eager launches from Python"},
         "tokens_per_s": w.num_decode_seqs * world * K / (res["elapsed_ms"] * 1e-3),
         "pct_of_nominal_8tbps": 100.0 * value / world / NOMINAL_HBM_GBS,
@@ -531,7 +556,9 @@ def main():
                      "kernel": "decode_kernel<128>", "peak_source": f"{peak_src} (hbm_gbs)",
                      "bytes_per_launch": alg, "launch_ms": res["dec_ms"],
                      "launch_timing": ("CUDA events on the launching stream around back-to-back "
-                                       "decode-only graph replays") if res["graphs"]
+                                       f"decode-only launches (graphs of {args.replicas}, one per "
+                                       "KV pool, each launch a programmatic dependent of the one "
+                                       "before); time / launches") if res["graphs"]
                                       else "CUDA events around each decode launch in the timed region"},
         "e2e": {"value": e["kv_all"] / (e["ms"] * 1e-3) / 1e9, "unit": "GB/s",
                 "h2d_bytes_per_step": e["h2d"], "d2h_bytes_per_step": e["d2h"],
@@ -544,7 +571,11 @@ def main():
         line["prefill_chunk"] = {"tflops": fl / (res["chunk_ms"] * 1e-3) / 1e12,
                                  "frac_of_bf16_peak": fl / (res["chunk_ms"] * 1e-3) / 1e12 / bf16,
                                  "peak": bf16, "gflop": fl / 1e9, "launch_ms": res["chunk_ms"],
-                                 "peak_source": f"{peak_src} (bf16_tflops)"}
+                                 "peak_source": f"{peak_src} (bf16_tflops)",
+                                 "timing": ("back-to-back chunk-only launches (graphs of "
+                                            f"{args.replicas}); time / launches") if res["graphs"]
+                                           else "CUDA events around each chunk launch while "
+                                                "the decode runs beside it"}
     if rank == 0:
         line["cpu_baseline"] = cpu_baseline_obj(w, args.cpu_seconds)
         print(json.dumps(line), flush=True)

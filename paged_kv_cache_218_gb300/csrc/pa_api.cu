@@ -162,6 +162,10 @@ __global__ void reshape_and_cache_kernel(const uint4* __restrict__ key,
   // the decode / prefill launched after this may begin its prologue now; it
   // waits for this kernel's writes before reading any global memory
   griddep_launch_dependents();
+  // launched as a programmatic dependent itself: the previous kernel on the
+  // stream (say the last step's decode, still reading the pool) must finish
+  // before any slot is written
+  griddep_wait();
   const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   if (i >= static_cast<int64_t>(num_tokens) * vec_per_token) return;
   const int t = static_cast<int>(i / vec_per_token);
@@ -313,11 +317,24 @@ int pa_reshape_and_cache(const void* key, const void* value, int64_t key_token_s
   const int64_t total = static_cast<int64_t>(num_tokens) * vec;
   const int threads = 256;
   const int64_t blocks = (total + threads - 1) / threads;
-  reshape_and_cache_kernel<<<static_cast<unsigned>(blocks), threads, 0,
-                             static_cast<cudaStream_t>(stream)>>>(
-      static_cast<const uint4*>(key), static_cast<const uint4*>(value), key_token_stride / 8,
-      value_token_stride / 8, static_cast<uint4*>(k_cache), static_cast<uint4*>(v_cache),
-      slot_mapping, num_tokens, vec, num_blocks * block_size, d->err);
+  // programmatic dependent launch: the CTAs may be scheduled while the
+  // previous kernel drains, and wait for it inside (griddepcontrol.wait)
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(blocks));
+  cfg.blockDim = dim3(threads);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = static_cast<cudaStream_t>(stream);
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (cudaLaunchKernelEx(&cfg, reshape_and_cache_kernel, static_cast<const uint4*>(key),
+                         static_cast<const uint4*>(value), key_token_stride / 8,
+                         value_token_stride / 8, static_cast<uint4*>(k_cache),
+                         static_cast<uint4*>(v_cache), slot_mapping, num_tokens, vec,
+                         num_blocks * block_size, d->err) != cudaSuccess)
+    return PA_ERR_CUDA;
   return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
 

@@ -243,67 +243,87 @@ __device__ __forceinline__ void attend_block(uint32_t kbase, uint32_t vbase, uin
 
 // Log-sum-exp merge of a sequence's partial pieces, held in the slots of CTAs
 // c_first (its "after" slot) and c_first+1 .. c_first+npieces-1 ("before"
-// slots); writes the final bf16 output (and lse).  A running log-sum-exp per
-// float4 group over the pieces; a thread's loads of one piece are independent,
-// so each piece costs about one L2 round trip per batch of groups.
+// slots); writes the final bf16 output (and lse).  Each thread owns kNI float4
+// groups of the output and keeps, per group, the running maximum M, the sum
+// S = sum_k exp(lse_k - M) and the weighted sum of the pieces' outputs.  The
+// pieces are read kKB at a time with all their loads issued together, so a
+// merge of up to kKB pieces costs about one L2 round trip.  Not inlined: it
+// runs at most twice per CTA and gets its registers apart from the main loop.
 template <int D>
-__device__ __forceinline__ void merge_pieces(const DecodeArgs& a, int s, long long c_first,
+__device__ __noinline__ void merge_pieces(const DecodeArgs& a, int s, long long c_first,
                                              int npieces, int ctid) {
   const int Hq = a.num_q_heads;
-    constexpr int kNI = 4;  // float4 groups per thread per batch
-    const int nf = Hq * D / 4;  // float4 groups of the sequence's output
-    const long long row0 = static_cast<long long>(s) * Hq;
-    for (int fb0 = 0; fb0 < nf; fb0 += kNI * kConsumerThreads) {
-      float4 acc[kNI];
-      float mrun[kNI], wsum[kNI];
+  constexpr int kNI = 4;  // float4 groups per thread per batch
+  constexpr int kKB = 4;  // pieces per round
+  const int nf = Hq * D / 4;
+  const long long row0 = static_cast<long long>(s) * Hq;
+  for (int fb0 = 0; fb0 < nf; fb0 += kNI * kConsumerThreads) {
+    float4 acc[kNI];
+    float M[kNI], S[kNI];
 #pragma unroll
-      for (int i = 0; i < kNI; ++i) {
-        acc[i] = make_float4(0.f, 0.f, 0.f, 0.f);
-        mrun[i] = -INFINITY;
-        wsum[i] = 0.f;
-      }
+    for (int i = 0; i < kNI; ++i) {
+      acc[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+      M[i] = -INFINITY;
+      S[i] = 0.f;
+    }
 #pragma unroll 1
-      for (int k = 0; k < npieces; ++k) {
-        const float* sl = a.part_o + ((c_first + k) * 2 + (k == 0 ? 1 : 0)) * a.slot_floats;
-        float lk[kNI];
-        float4 ok[kNI];
+    for (int k0 = 0; k0 < npieces; k0 += kKB) {
+      float4 ok[kKB][kNI];
+      float lk[kKB][kNI];
+#pragma unroll
+      for (int u = 0; u < kKB; ++u) {
+        const int k = k0 + u;
+        const float* sl =
+            a.part_o + ((c_first + (k < npieces ? k : 0)) * 2 + (k == 0 ? 1 : 0)) * a.slot_floats;
 #pragma unroll
         for (int i = 0; i < kNI; ++i) {
           const int f = fb0 + ctid + i * kConsumerThreads;
-          if (f < nf) {
-            lk[i] = __ldcg(sl + Hq * D + (f * 4) / D);
-            ok[i] = __ldcg(reinterpret_cast<const float4*>(sl) + f);
-          }
-        }
-#pragma unroll
-        for (int i = 0; i < kNI; ++i) {
-          const int f = fb0 + ctid + i * kConsumerThreads;
-          if (f < nf && lk[i] != -INFINITY) {
-            const float mn = fmaxf(mrun[i], lk[i]);
-            const float sc = __expf(mrun[i] - mn), w = __expf(lk[i] - mn);
-            acc[i].x = acc[i].x * sc + w * ok[i].x;
-            acc[i].y = acc[i].y * sc + w * ok[i].y;
-            acc[i].z = acc[i].z * sc + w * ok[i].z;
-            acc[i].w = acc[i].w * sc + w * ok[i].w;
-            wsum[i] = wsum[i] * sc + w;
-            mrun[i] = mn;
+          if (k < npieces && f < nf) {
+            lk[u][i] = __ldcg(sl + Hq * D + (f * 4) / D);
+            ok[u][i] = __ldcg(reinterpret_cast<const float4*>(sl) + f);
+          } else {
+            lk[u][i] = -INFINITY;
+            ok[u][i] = make_float4(0.f, 0.f, 0.f, 0.f);
           }
         }
       }
 #pragma unroll
       for (int i = 0; i < kNI; ++i) {
-        const int f = fb0 + ctid + i * kConsumerThreads;
-        if (f < nf) {
-          const float inv = wsum[i] > 0.f ? 1.f / wsum[i] : 0.f;
-          const uint2 pk = make_uint2(pack_bf16x2(acc[i].x * inv, acc[i].y * inv),
-                                      pack_bf16x2(acc[i].z * inv, acc[i].w * inv));
-          *reinterpret_cast<uint2*>(a.out + row0 * D + static_cast<long long>(f) * 4) = pk;
-          if ((f * 4) % D == 0 && a.out_lse)
-            a.out_lse[row0 + (f * 4) / D] =
-                wsum[i] > 0.f ? mrun[i] + __logf(wsum[i]) : -INFINITY;
+        float mx = M[i];
+#pragma unroll
+        for (int u = 0; u < kKB; ++u) mx = fmaxf(mx, lk[u][i]);
+        if (mx == -INFINITY) continue;
+        const float sc = __expf(M[i] - mx);  // 0 while M is still -inf
+        acc[i].x *= sc;
+        acc[i].y *= sc;
+        acc[i].z *= sc;
+        acc[i].w *= sc;
+        S[i] *= sc;
+#pragma unroll
+        for (int u = 0; u < kKB; ++u) {
+          const float w = __expf(lk[u][i] - mx);  // 0 for absent pieces
+          acc[i].x += w * ok[u][i].x;
+          acc[i].y += w * ok[u][i].y;
+          acc[i].z += w * ok[u][i].z;
+          acc[i].w += w * ok[u][i].w;
+          S[i] += w;
         }
+        M[i] = mx;
       }
     }
+#pragma unroll
+    for (int i = 0; i < kNI; ++i) {
+      const int f = fb0 + ctid + i * kConsumerThreads;
+      if (f < nf) {
+        const float inv = S[i] > 0.f ? 1.f / S[i] : 0.f;
+        const uint2 pk = make_uint2(pack_bf16x2(acc[i].x * inv, acc[i].y * inv),
+                                    pack_bf16x2(acc[i].z * inv, acc[i].w * inv));
+        *reinterpret_cast<uint2*>(a.out + row0 * D + static_cast<long long>(f) * 4) = pk;
+        if ((f * 4) % D == 0 && a.out_lse)
+          a.out_lse[row0 + (f * 4) / D] = S[i] > 0.f ? M[i] + __logf(S[i]) : -INFINITY;
+      }
+    }
+  }
 }
 
 template <int D>
@@ -344,10 +364,27 @@ __global__ void __launch_bounds__(kThreads, 1)
     misc[0] = 0;  // abort flag
     fence_mbar_init();
   }
-  // Nothing above touches global memory: launched as a programmatic dependent
-  // of the previous kernel on the stream, the CTA may get here early and waits
-  // here until that kernel has finished and its writes are visible.
+  // Launched as a programmatic dependent of the previous kernel on the stream,
+  // the CTA may get here while that kernel still runs.  Until griddep_wait()
+  // returns it reads no global memory; it only asks L2 for the lines of this
+  // launch's lengths, block tables and queries (at most 4 MB of each), spread
+  // over every thread of the grid, so that the reads after the wait hit L2.
+  {
+    const long long nthr = static_cast<long long>(gridDim.x) * kThreads;
+    const long long me = static_cast<long long>(blockIdx.x) * kThreads + tid;
+    auto warm = [&](const void* base, long long bytes) {
+      bytes = bytes < (4ll << 20) ? bytes : (4ll << 20);
+      for (long long off = me * 128; off < bytes; off += nthr * 128)
+        prefetch_l2(static_cast<const char*>(base) + off);
+    };
+    warm(a.seq_lens, static_cast<long long>(a.num_seqs) * 4);
+    warm(a.block_tables, static_cast<long long>(a.num_seqs) * a.max_blocks * 4);
+    warm(a.q, static_cast<long long>(a.num_seqs) * Hq * D * 2);
+  }
   griddep_wait();
+  // The next kernel on the stream may start launching now: its CTAs take SMs
+  // as these exit, and it waits for this grid before it reads memory.
+  griddep_launch_dependents();
 
   Cursor cur{};
   if (a.mode == kModeBalanced) {
@@ -509,7 +546,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   // balanced partial pieces (at most the CTA's first and last) are published
   // as they finish; their tickets and merges wait until the CTA is done
   long long def_cf[2] = {0, 0};
-  int def_np[2] = {0, 0}, def_s[2] = {0, 0}, ndef = 0;
+  int def_np[2] = {0, 0}, def_s[2] = {0, 0}, def_tk[2] = {0, 0}, ndef = 0;
   Piece pc;
   uint32_t g = 0;
   int qi = 0;
@@ -710,32 +747,34 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (hb < G) slot[Hq * D + hgb] = lseb;
         }
       }
+      // take the sequence's ticket now (release of the slot stores above);
+      // the result is read after the CTA's last piece, so a first piece does
+      // not hold up the stream, and a merge is left to the end
+      const long long cf = cta_of(pc.seg_start, cur.W, cur.C);
+      named_barrier(1, kConsumerThreads);
+      int tk = 0;
+      if (ctid == 0) tk = atom_add_acq_rel_gpu(a.counters + cf, 1);
       if (ndef < 2) {
-        def_cf[ndef] = cta_of(pc.seg_start, cur.W, cur.C);
-        def_np[ndef] = static_cast<int>(cta_of(pc.seg_start + pc.nb - 1, cur.W, cur.C) -
-                                        def_cf[ndef] + 1);
+        def_cf[ndef] = cf;
+        def_np[ndef] = static_cast<int>(cta_of(pc.seg_start + pc.nb - 1, cur.W, cur.C) - cf + 1);
         def_s[ndef] = pc.s;
+        def_tk[ndef] = tk;
         ++ndef;
       }
     }
   }
 
-  // ---- tickets of this CTA's partial pieces; the last piece of a sequence to
-  // arrive merges all of them by log-sum-exp
+  // ---- the last piece of a sequence to draw its ticket merges all of them
   if (a.mode == kModeBalanced && ndef > 0) {
-    __threadfence();
+    if (ctid == 0)
+      for (int k = 0; k < ndef; ++k) misc[1 + k] = def_tk[k];
     named_barrier(1, kConsumerThreads);
     for (int k = 0; k < ndef; ++k) {
-      const long long c_first = def_cf[k];
-      const int npieces = def_np[k];
-      if (ctid == 0) misc[1] = atomicAdd(a.counters + c_first, 1);
-      named_barrier(1, kConsumerThreads);
-      if (misc[1] == npieces - 1) {
-        __threadfence();
-        merge_pieces<D>(a, def_s[k], c_first, npieces, ctid);
-        if (ctid == 0) a.counters[c_first] = 0;
+      if (misc[1 + k] == def_np[k] - 1) {
+        merge_pieces<D>(a, def_s[k], def_cf[k], def_np[k], ctid);
+        if (ctid == 0) a.counters[def_cf[k]] = 0;
+        named_barrier(1, kConsumerThreads);
       }
-      named_barrier(1, kConsumerThreads);
     }
   }
 }

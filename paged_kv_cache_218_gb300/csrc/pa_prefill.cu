@@ -143,6 +143,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   // launched as a programmatic dependent of the previous kernel (the scatter
   // of this step's K/V): nothing before this line touches global memory
   griddep_wait();
+  // the next kernel on the stream may start launching; it waits for this grid
+  griddep_launch_dependents();
 
   // ---- chunk metadata (uniform over the CTA)
   const int q0 = a.cu_q_lens[c], q1 = a.cu_q_lens[c + 1];

@@ -113,6 +113,27 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_
       : "memory");
 }
 
+// Hint: bring the 128-byte line holding `p` into L2.  It returns no data, and
+// L2 is the point of coherence, so it is harmless even for memory that the
+// previous kernel on the stream may still write.
+__device__ __forceinline__ void prefetch_l2(const void* p) {
+  asm volatile("prefetch.global.L2 [%0];" ::"l"(reinterpret_cast<uint64_t>(p)));
+}
+
+// Ticket counter shared by CTAs: atomic add with acquire-release semantics at
+// GPU scope.  A CTA publishes with plain stores, meets a CTA barrier, then one
+// thread takes the ticket: the release covers the CTA's stores ordered before
+// it by the barrier; the acquire lets the thread that draws the last ticket
+// (and, after another barrier, its CTA) read every publisher's stores.
+__device__ __forceinline__ int atom_add_acq_rel_gpu(int* p, int v) {
+  int old;
+  asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], %2;"
+               : "=r"(old)
+               : "l"(p), "r"(v)
+               : "memory");
+  return old;
+}
+
 // Programmatic dependent launch: wait until the previous kernel on the stream
 // has finished and its memory is visible / let the next kernel start launching.
 __device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
