@@ -437,6 +437,60 @@ def cpu_baseline_obj(w, min_seconds):
                       f"slot scatter excluded", "tokens_per_s": w.num_decode_seqs / sec}
 
 
+def block_manager_timing(steps=64, seqs=256, group=4, system_tokens=256):
+    """Host block manager at serving scale, the C++ manager (through its C ABI)
+    and the plain-Python oracle manager on the same script: admit a
+    continuous-batching mix (``seqs`` requests; groups of ``group`` share a
+    ``system_tokens``-token system prompt through the prefix cache; suffix
+    lengths lognormal, median 512, clipped to [1, 8192]), fork one member per
+    group, then decode steps of one appended token per sequence, each ended
+    with its copy pairs and the batch's block tables."""
+    import numpy as np
+
+    from oracle.block_manager import BlockManagerOracle
+    from paged_kv_cache_218_gb300.block_manager import BlockManager
+    rng = np.random.default_rng(4004)
+    systems = [rng.integers(0, 32000, system_tokens).tolist() for _ in range(seqs // group)]
+    prompts = [systems[i // group] + rng.integers(
+        0, 32000, int(np.clip(np.rint(np.exp(np.log(512.0) + rng.standard_normal())), 1, 8192))
+    ).tolist() for i in range(seqs)]
+    toks = rng.integers(0, 32000, (steps, seqs + seqs // group)).tolist()
+    nb = sum(-(-(len(p) + steps) // 16) for p in prompts) + 2 * seqs
+    max_blocks = max(-(-(len(p) + steps) // 16) for p in prompts)
+
+    def run(m, oracle_side):
+        t0 = time.perf_counter()
+        for i, p in enumerate(prompts):
+            m.add_sequence(i, p)
+        for g in range(seqs // group):
+            m.fork(g * group, seqs + g)
+        m.end_step()
+        t1 = time.perf_counter()
+        ids = list(range(seqs + seqs // group))
+        for st in range(steps):
+            if oracle_side:
+                for i in ids:
+                    m.append_token(i, toks[st][i])
+            else:
+                m.append_tokens(ids, toks[st])
+            m.end_step()
+            m.build_tables(ids, max_blocks)
+        t2 = time.perf_counter()
+        return (t1 - t0) / seqs * 1e6, (t2 - t1) / steps * 1e6
+
+    m = BlockManager(nb, 16, True)
+    admit_us, step_us = run(m, False)
+    cached = m.num_cached_blocks()
+    m.close()
+    o_admit_us, o_step_us = run(BlockManagerOracle(nb, 16, True), True)
+    return {"unit": "us", "admit_us_per_seq": admit_us, "decode_step_us": step_us,
+            "batch": seqs + seqs // group, "cached_blocks": cached,
+            "oracle_admit_us_per_seq": o_admit_us, "oracle_decode_step_us": o_step_us,
+            "workload": f"{seqs} requests, groups of {group} sharing a {system_tokens}-token "
+                        "system prompt, lognormal(median 512) suffixes, one fork per group; "
+                        f"{steps} decode steps of one token per sequence + copy pairs + tables"}
+
+
 def reference_arm(args):
     """K timed steps of the oracle, each a bounded sample of the workload: a
     rotating subset of the sequences sized so that warm-up + K steps take
@@ -578,6 +632,7 @@ def main():
                                                 "the decode runs beside it"}
     if rank == 0:
         line["cpu_baseline"] = cpu_baseline_obj(w, args.cpu_seconds)
+        line["host_block_manager"] = block_manager_timing()
         print(json.dumps(line), flush=True)
     if world > 1:
         import torch.distributed as tdist

@@ -17,8 +17,9 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(ROOT, "_build")
 LIB = os.path.join(PKG, "libpa.so")
-SOURCES = ["pa_api.cu", "pa_decode.cu", "pa_prefill.cu"]
-HEADERS = ["pa_internal.h", "pa_ptx.cuh", os.path.join("..", "..", "include", "pa.h")]
+SOURCES = ["pa_api.cu", "pa_decode.cu", "pa_prefill.cu", "pa_block_manager.cpp"]
+HEADERS = ["pa_internal.h", "pa_ptx.cuh", os.path.join("..", "..", "include", "pa.h"),
+           os.path.join("..", "..", "include", "pa_block_manager.h")]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC,-O2", "--expt-relaxed-constexpr"]
 
@@ -45,7 +46,7 @@ def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
     jobs = []
     for src in SOURCES:
         s = os.path.join(CSRC, src)
-        o = os.path.join(BUILD, src.replace(".cu", ".o"))
+        o = os.path.join(BUILD, os.path.splitext(src)[0] + ".o")
         objs.append(o)
         if force or _stale(o, [s] + headers):
             cmd = [nvcc, *ARCH, *FLAGS, *extra_flags, "-c", s, "-o", o]
