@@ -57,6 +57,9 @@ def _load():
                 "oracle_attend_range": [P, P, P, P, I, I, I, L, L, I, I, I, I, L, D, P, P],
                 "oracle_merge": [P, P, P, I, I, I, I, P, P],
                 "oracle_prefill": [P, P, P, P, I, P, P, P, I, I, I, I, I, L, D, P, P],
+                "oracle_reshape_and_cache_fp8": [P, P, L, L, P, P, P, P, P, I, I, I, I, L],
+                "oracle_decode_fp8": [P, P, P, P, P, P, I, P, I, I, I, I, I, L, D, P, P],
+                "oracle_e4m3_encode": [ctypes.c_float],
                 "oracle_num_threads": [],
                 "oracle_set_num_threads": [I],
             }
@@ -64,6 +67,8 @@ def _load():
                 fn = getattr(lib, name)
                 fn.argtypes = args
                 fn.restype = ctypes.c_int if name != "oracle_set_num_threads" else None
+            lib.oracle_e4m3_value.argtypes = [ctypes.c_uint8]
+            lib.oracle_e4m3_value.restype = ctypes.c_double
             _lib = lib
     return _lib
 
@@ -210,4 +215,66 @@ def prefill(q, k_cache, v_cache, block_tables, cu_q_lens, q_start_pos, seq_lens,
                                 _ptr(cu), _ptr(qs), _ptr(sl), C, Hq, Hkv, D, bs, nb,
                                 float(scale), _ptr(out), _ptr(lse))
     _check(rc, "prefill")
+    return out, lse
+
+
+# ----------------------------------------------------------------- FP8 (E4M3) KV cache
+
+def e4m3_value(code: int) -> float:
+    """The value of one E4M3 byte (NaN for 0x7F / 0xFF)."""
+    return float(_load().oracle_e4m3_value(int(code) & 0xFF))
+
+
+def e4m3_encode(v: float) -> int:
+    """The E4M3 code nearest to the fp32 value v (ties to even, saturating)."""
+    return int(_load().oracle_e4m3_encode(float(np.float32(v))))
+
+
+def reshape_and_cache_fp8(key, value, k_cache, v_cache, slot_mapping, k_scales, v_scales,
+                          block_size=16):
+    """Quantizing scatter of bf16 key/value [T, Hkv, D] into copies of uint8
+    E4M3 pools: code = E4M3(x / scale[h]), the division in IEEE fp32."""
+    key = _c(key, np.uint16)
+    value = _c(value, np.uint16)
+    kc = np.array(k_cache, dtype=np.uint8, copy=True, order="C")
+    vc = np.array(v_cache, dtype=np.uint8, copy=True, order="C")
+    slots = _c(slot_mapping, np.int64)
+    ks = _c(np.asarray(k_scales, dtype=np.float32), np.float32)
+    vs = _c(np.asarray(v_scales, dtype=np.float32), np.float32)
+    T, Hkv, D = key.shape
+    rc = _load().oracle_reshape_and_cache_fp8(
+        _ptr(key), _ptr(value), Hkv * D, Hkv * D, _ptr(kc), _ptr(vc), _ptr(slots), _ptr(ks),
+        _ptr(vs), T, Hkv, D, block_size, kc.shape[0])
+    _check(rc, "reshape_and_cache_fp8")
+    return kc, vc
+
+
+def copy_blocks_fp8(k_cache, v_cache, pairs):
+    """Whole-block copies src -> dst of uint8 pools (copies returned)."""
+    kc = np.array(k_cache, dtype=np.uint8, copy=True, order="C")
+    vc = np.array(v_cache, dtype=np.uint8, copy=True, order="C")
+    for src, dst in np.asarray(pairs, dtype=np.int64).reshape(-1, 2):
+        kc[dst] = kc[src]
+        vc[dst] = vc[src]
+    return kc, vc
+
+
+def decode_fp8(q, k_cache, v_cache, k_scales, v_scales, block_tables, seq_lens, scale):
+    """Decode over E4M3 pools, dequantized exactly in fp64:
+    q [S, Hq, D] -> (out [S, Hq, D], lse [S, Hq])."""
+    q = _c(q, np.uint16)
+    k_cache = _c(k_cache, np.uint8)
+    v_cache = _c(v_cache, np.uint8)
+    ks = _c(np.asarray(k_scales, dtype=np.float32), np.float32)
+    vs = _c(np.asarray(v_scales, dtype=np.float32), np.float32)
+    bt = _c(block_tables, np.int32)
+    sl = _c(seq_lens, np.int32)
+    S, Hq, D = q.shape
+    nb, bs, Hkv, _ = k_cache.shape
+    out = np.zeros((S, Hq, D), dtype=np.float64)
+    lse = np.zeros((S, Hq), dtype=np.float64)
+    rc = _load().oracle_decode_fp8(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(ks), _ptr(vs),
+                                   _ptr(bt), bt.shape[1], _ptr(sl), S, Hq, Hkv, D, bs, nb,
+                                   float(scale), _ptr(out), _ptr(lse))
+    _check(rc, "decode_fp8")
     return out, lse

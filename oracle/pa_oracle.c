@@ -342,6 +342,140 @@ int oracle_prefill(const uint16_t *q, const uint16_t *k_cache, const uint16_t *v
   return bad ? -1 : 0;
 }
 
+/* ---------------------------------------------------------------------- */
+/* FP8 (E4M3) KV cache: both engines ship FP8 KV caches with per-tensor or  */
+/* per-head scales ("The LLM inference engine playbook", Theme 3, shrinking */
+/* the cache).  E4M3 as the format defines it: a sign bit, 4 exponent bits  */
+/* (bias 7) and 3 mantissa bits; exponent field 0 holds subnormals m*2^-9;  */
+/* no infinity; 0x7F and 0xFF are NaN; the largest finite magnitude is      */
+/* (1 + 6/8) * 2^8 = 448.                                                   */
+/* ---------------------------------------------------------------------- */
+double oracle_e4m3_value(uint8_t code) {
+  int e = (code >> 3) & 15, m = code & 7;
+  double v;
+  if (e == 15 && m == 7) return NAN;
+  if (e == 0)
+    v = ldexp((double)m, -9);
+  else
+    v = ldexp(8.0 + m, e - 10); /* (1 + m/8) * 2^(e - 7) */
+  return (code & 0x80) ? -v : v;
+}
+
+/* The E4M3 code nearest to v, ties to the even code (even mantissa);
+ * magnitudes of 448 and above (infinity included) give +-448; NaN gives 0x7F.
+ * Below 2^-6 the grid has step 2^-9 (codes 0..8 are code * 2^-9); in
+ * [2^k, 2^(k+1)) it has step 2^(k-3), and a rounding up to 2^(k+1) carries
+ * into the exponent field. */
+int oracle_e4m3_encode(float v) {
+  if (isnan(v)) return 0x7F;
+  int sign = signbit(v) ? 0x80 : 0;
+  double a = fabs((double)v);
+  if (a >= 448.0) return sign | 0x7E;
+  int code;
+  if (a < ldexp(1.0, -6)) {
+    code = (int)nearbyint(a * 512.0); /* exact scaling; round half to even */
+  } else {
+    int k;
+    frexp(a, &k);
+    k -= 1; /* a in [2^k, 2^(k+1)) */
+    double q = nearbyint(ldexp(a, 3 - k)); /* in [8, 16] */
+    code = ((k + 7) << 3) + (int)q - 8;
+  }
+  if (code > 0x7E) code = 0x7E;
+  return sign | code;
+}
+
+/* Quantizing scatter: code = E4M3(x / scale[h]), the division in IEEE fp32. */
+int oracle_reshape_and_cache_fp8(const uint16_t *key, const uint16_t *value,
+                                 int64_t key_token_stride, int64_t value_token_stride,
+                                 uint8_t *k_cache, uint8_t *v_cache, const int64_t *slot_mapping,
+                                 const float *k_scales, const float *v_scales, int num_tokens,
+                                 int num_kv_heads, int head_dim, int block_size,
+                                 int64_t num_blocks) {
+  int bad = 0;
+  /* tokens in parallel: valid slots are distinct, so no two write one byte */
+#pragma omp parallel for schedule(static) reduction(| : bad)
+  for (int t = 0; t < num_tokens; ++t) {
+    int64_t slot = slot_mapping[t];
+    if (slot < 0) continue;
+    if (slot >= num_blocks * (int64_t)block_size) {
+      bad = 1;
+      continue;
+    }
+    for (int h = 0; h < num_kv_heads; ++h) {
+      for (int c = 0; c < head_dim; ++c) {
+        int64_t dst = (slot * num_kv_heads + h) * (int64_t)head_dim + c;
+        float xk = (float)bf16_bits_to_f64(key[(int64_t)t * key_token_stride + (int64_t)h * head_dim + c]);
+        float xv = (float)bf16_bits_to_f64(value[(int64_t)t * value_token_stride + (int64_t)h * head_dim + c]);
+        float rk = xk / k_scales[h];
+        float rv = xv / v_scales[h];
+        k_cache[dst] = (uint8_t)oracle_e4m3_encode(rk);
+        v_cache[dst] = (uint8_t)oracle_e4m3_encode(rv);
+      }
+    }
+  }
+  return bad ? -1 : 0;
+}
+
+/* Gather with dequantization: rows of value(code) * scale, in fp64 (exact). */
+static int gather_rows_e4m3(const uint8_t *cache, const int32_t *table_row, int kvh, int64_t a,
+                            int64_t b, int num_kv_heads, int head_dim, int block_size,
+                            int64_t num_blocks, double scale, double *rows) {
+  for (int64_t j = a; j < b; ++j) {
+    int64_t blk = table_row[j / block_size];
+    int64_t off = j % block_size;
+    if (blk < 0 || blk >= num_blocks) return -1;
+    const uint8_t *src = cache + ((blk * block_size + off) * num_kv_heads + kvh) * (int64_t)head_dim;
+    for (int c = 0; c < head_dim; ++c) rows[(j - a) * head_dim + c] = oracle_e4m3_value(src[c]) * scale;
+  }
+  return 0;
+}
+
+/* Decode over E4M3 pools: the decode definition on the dequantized cache. */
+int oracle_decode_fp8(const uint16_t *q, const uint8_t *k_cache, const uint8_t *v_cache,
+                      const float *k_scales, const float *v_scales,
+                      const int32_t *block_tables, int max_blocks_per_seq,
+                      const int32_t *seq_lens, int num_seqs, int num_q_heads, int num_kv_heads,
+                      int head_dim, int block_size, int64_t num_blocks, double scale,
+                      double *out, double *lse) {
+  int group = num_q_heads / num_kv_heads;
+  int bad = 0;
+#pragma omp parallel for schedule(dynamic, 1) reduction(| : bad)
+  for (int64_t pair = 0; pair < (int64_t)num_seqs * num_kv_heads; ++pair) {
+    int s = (int)(pair / num_kv_heads), kvh = (int)(pair % num_kv_heads);
+    int64_t n = seq_lens[s];
+    if (n < 0 || n > (int64_t)max_blocks_per_seq * block_size) {
+      bad = 1;
+      continue;
+    }
+    double *K = (double *)malloc(sizeof(double) * (size_t)(n > 0 ? n : 1) * head_dim);
+    double *V = (double *)malloc(sizeof(double) * (size_t)(n > 0 ? n : 1) * head_dim);
+    double *x = (double *)malloc(sizeof(double) * (size_t)(n > 0 ? n : 1));
+    double *qv = (double *)malloc(sizeof(double) * head_dim);
+    const int32_t *row = block_tables + (int64_t)s * max_blocks_per_seq;
+    if (gather_rows_e4m3(k_cache, row, kvh, 0, n, num_kv_heads, head_dim, block_size, num_blocks,
+                         (double)k_scales[kvh], K) ||
+        gather_rows_e4m3(v_cache, row, kvh, 0, n, num_kv_heads, head_dim, block_size, num_blocks,
+                         (double)v_scales[kvh], V)) {
+      bad = 1;
+    } else {
+      for (int g = 0; g < group; ++g) {
+        int h = kvh * group + g;
+        const uint16_t *qsrc = q + ((int64_t)s * num_q_heads + h) * head_dim;
+        for (int c = 0; c < head_dim; ++c) qv[c] = bf16_bits_to_f64(qsrc[c]);
+        double l;
+        attend(qv, K, V, n, head_dim, scale, x, out + ((int64_t)s * num_q_heads + h) * head_dim, &l);
+        if (lse) lse[(int64_t)s * num_q_heads + h] = l;
+      }
+    }
+    free(K);
+    free(V);
+    free(x);
+    free(qv);
+  }
+  return bad ? -1 : 0;
+}
+
 /* Threads the OpenMP runtime will use (reported beside CPU timings). */
 #ifdef _OPENMP
 #include <omp.h>
