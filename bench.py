@@ -365,8 +365,66 @@ def run_gpu(args, rank, world, local_rank):
         raise RuntimeError(f"device error flags {flags} after the timed region")
 
     e2e = run_e2e(args, w, reps, ws, dev, pa, dist)
+    fp8 = measure_fp8_decode(args, w, reps, ws, dev, pa) if (use_graphs and w.head_dim == 128) \
+        else None
     return dict(w=w, elapsed_ms=elapsed_ms, kv_all=kv_all, dec_ms=dec_ms, chunk_ms=chunk_ms,
-                clocks=clocks, e2e=e2e, launches=launches_per_step * K, graphs=use_graphs)
+                clocks=clocks, e2e=e2e, launches=launches_per_step * K, graphs=use_graphs,
+                fp8=fp8)
+
+
+def measure_fp8_decode(args, w, reps, ws, dev, pa):
+    """The same decode over E4M3 copies of each replica's pools (per-kv-head
+    scales max |x| / 448, quantized by pa_reshape_and_cache_fp8 at set-up),
+    timed like the bf16 kernel: back-to-back launches from graphs of R."""
+    import torch
+    R = len(reps)
+    nb, bs, Hkv, D = reps[0].k_cache.shape
+    P = args.partition_tokens
+    pools = []
+    for r in reps:
+        kf = torch.empty((nb, bs, Hkv, D), dtype=torch.uint8, device=dev)
+        vf = torch.empty_like(kf)
+        ks = (r.k_cache.float().abs().amax(dim=(0, 1, 3)) / 448.0).clamp_min(1e-8).contiguous()
+        vs = (r.v_cache.float().abs().amax(dim=(0, 1, 3)) / 448.0).clamp_min(1e-8).contiguous()
+        slots = torch.arange(nb * bs, dtype=torch.int64, device=dev)
+        pa.pa_reshape_and_cache_fp8(r.k_cache.view(nb * bs, Hkv, D), r.v_cache.view(nb * bs, Hkv, D),
+                                    kf, vf, slots, ks, vs)
+        pools.append((kf, vf, ks, vs))
+    torch.cuda.synchronize()
+
+    def dec(i):
+        r = reps[i]
+        out, q, _, _, bt, sl = decode_args(w, r)
+        kf, vf, ks, vs = pools[i]
+        pa.pa_decode_fp8(out, q, kf, vf, ks, vs, bt, sl, w.scale, partition_tokens=P,
+                         workspace=ws[i])
+
+    for i in range(max(3, args.warmup // 4)):
+        dec(i % R)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        for i in range(R):
+            dec(i)
+    g.replay()
+    torch.cuda.synchronize()
+    n = max(1, min(args.steps, args.kernel_steps) // R)
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(n):
+        g.replay()
+    b.record()
+    torch.cuda.synchronize()
+    ms = a.elapsed_time(b) / (n * R)
+    if pa.pa_device_error_flags() != 0:
+        raise RuntimeError("device error flags set by the E4M3 decode")
+    S, Hq = w.num_decode_seqs, w.num_q_heads
+    kv = kv_bytes_decode(w) // 2
+    alg = kv + 2 * S * Hq * D * 2 + sum((int(x) + 15) // 16 for x in w.decode_seq_lens) * 4 + S * 4
+    del pools
+    return {"launch_ms": ms, "bytes_per_launch": alg, "kernel": "decode_kernel<128, E4M3>",
+            "kv_bytes_per_token": 2 * Hkv * D, "tokens_per_s": S / (ms * 1e-3),
+            "achieved_gbs": alg / (ms * 1e-3) / 1e9,
+            "scales": "per kv head, max |x| / 448"}
 
 
 def run_e2e(args, w, reps, ws, dev, pa, dist):
@@ -620,6 +678,12 @@ def main():
         "gpu_launches": res["launches"],
         "clocks": res["clocks"],
     }
+    if res.get("fp8") is not None:
+        f = res["fp8"]
+        line["fp8_kv"] = dict(f, peak=hbm, frac=f["achieved_gbs"] / hbm,
+                              peak_source=f"{peak_src} (hbm_gbs)",
+                              tokens_per_s_vs_bf16=f["tokens_per_s"] /
+                              (w.num_decode_seqs / (res["dec_ms"] * 1e-3)))
     if res["chunk_ms"] is not None:
         fl = chunk_flops(w)
         line["prefill_chunk"] = {"tflops": fl / (res["chunk_ms"] * 1e-3) / 1e12,

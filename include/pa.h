@@ -148,6 +148,54 @@ int pa_decode(void *out, const void *q, const void *k_cache, const void *v_cache
               void *workspace, size_t workspace_bytes, void *stream);
 
 /*
+ * FP8 (E4M3) KV cache: the pools hold one byte per element, with one
+ * dequantization scale per kv head for K and one for V (pass the same value
+ * for every head to get a per-tensor scale).  Both engines of the pages ship
+ * an FP8 KV cache with per-tensor or per-head scales, and quantizing the
+ * cache is the "shrink the cache" lever ("The LLM inference engine playbook",
+ * Theme 3); decode reads half the bytes of a bf16 pool.
+ *
+ * E4M3: 1 sign bit, 4 exponent bits (bias 7), 3 mantissa bits; no infinity;
+ * the largest finite magnitude is 448; 0x7F / 0xFF are NaN.
+ *
+ * pa_reshape_and_cache_fp8 -- quantizing slot scatter: for every new token t
+ * with slot_mapping[t] >= 0 and every element x of key[t][h] (likewise V):
+ *   code = E4M3(x / k_scales[h])
+ * where the division is IEEE fp32 (correctly rounded) and E4M3() rounds to
+ * nearest, ties to even, saturating finite values beyond +-448 to +-448.
+ * Arguments as pa_reshape_and_cache, except
+ *   k_cache, v_cache  device, uint8 [num_blocks, block_size, num_kv_heads, head_dim]
+ *   k_scales, v_scales device, fp32 [num_kv_heads], positive and finite
+ */
+int pa_reshape_and_cache_fp8(const void *key, const void *value, int64_t key_token_stride,
+                             int64_t value_token_stride, void *k_cache, void *v_cache,
+                             const int64_t *slot_mapping, const float *k_scales,
+                             const float *v_scales, int num_tokens, int num_kv_heads,
+                             int head_dim, int block_size, int64_t num_blocks, void *stream);
+
+/* pa_copy_blocks for E4M3 pools (bytes; head_dim a multiple of 16). */
+int pa_copy_blocks_fp8(void *k_cache, void *v_cache, const int64_t *block_pairs, int num_pairs,
+                       int num_kv_heads, int head_dim, int block_size, int64_t num_blocks,
+                       void *stream);
+
+/*
+ * pa_decode over E4M3 pools: the attention of pa_decode with
+ *   K_s[j] = e4m3_value(k_cache[...]) * k_scales[h / group]
+ *   V_s[j] = e4m3_value(v_cache[...]) * v_scales[h / group]
+ * (the dequantized cache).  head_dim must be 128.  Same arguments, modes,
+ * workspace (sized by pa_decode_workspace_size) and outputs as pa_decode,
+ * plus the two scale arrays (device, fp32 [num_kv_heads]).  The contraction
+ * runs on f16 copies of the E4M3 values (exact) with the queries scaled by a
+ * power of two per sequence and kv head, fp32 accumulation.
+ */
+int pa_decode_fp8(void *out, const void *q, const void *k_cache, const void *v_cache,
+                  const float *k_scales, const float *v_scales, const int32_t *block_tables,
+                  int max_blocks_per_seq, const int32_t *seq_lens, int num_seqs,
+                  int num_q_heads, int num_kv_heads, int head_dim, int block_size,
+                  int64_t num_blocks, float scale, int partition_tokens, float *out_lse,
+                  void *workspace, size_t workspace_bytes, void *stream);
+
+/*
  * Log-sum-exp merge of partial attentions ("03 - Engines Papers", section 12
  * Cascade Inference, merged via LSE; split-K softmax reduction, "The LLM
  * inference engine playbook", Theme 4):

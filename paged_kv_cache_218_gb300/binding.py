@@ -51,6 +51,10 @@ _SIGS = {
     "pa_prefill_chunk": ([_P, _P, _P, _P, _P, _I, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _L, _F,
                           _P, _P], _I),
     "pa_validate_metadata": ([_P, _I, _P, _I, _P, _I, _P, _L, _I], _I),
+    "pa_reshape_and_cache_fp8": ([_P, _P, _L, _L, _P, _P, _P, _P, _P, _I, _I, _I, _I, _L, _P], _I),
+    "pa_copy_blocks_fp8": ([_P, _P, _P, _I, _I, _I, _I, _L, _P], _I),
+    "pa_decode_fp8": ([_P, _P, _P, _P, _P, _P, _P, _I, _P, _I, _I, _I, _I, _I, _L, _F, _I, _P, _P,
+                       _S, _P], _I),
     "pa_device_error_flags": ([ctypes.POINTER(ctypes.c_uint), _I], _I),
 }
 for _name, (_args, _res) in _SIGS.items():
@@ -128,6 +132,61 @@ def pa_copy_blocks(k_cache, v_cache, block_pairs, stream=None) -> None:
     nb, bs, Hkv, D = k_cache.shape
     _check("pa_copy_blocks", _lib.pa_copy_blocks(
         _ptr(k_cache), _ptr(v_cache), _ptr(block_pairs), block_pairs.shape[0], Hkv, D, bs, nb,
+        _stream(stream)))
+
+
+def pa_reshape_and_cache_fp8(key, value, k_cache, v_cache, slot_mapping, k_scales, v_scales,
+                             stream=None) -> None:
+    """Quantizing scatter of bf16 key/value [T, Hkv, D] into uint8 E4M3 pools
+    with per-kv-head fp32 scales: code = E4M3(x / scale[h])."""
+    _need(key, "key", torch.bfloat16, 3, contiguous=False)
+    _need(value, "value", torch.bfloat16, 3, contiguous=False)
+    for t, n in ((key, "key"), (value, "value")):
+        if t.stride(2) != 1 or t.stride(1) != t.shape[2]:
+            raise ValueError(f"{n} must be contiguous within a token")
+    _need(k_cache, "k_cache", torch.uint8, 4)
+    _need(v_cache, "v_cache", torch.uint8, 4)
+    _need(slot_mapping, "slot_mapping", torch.int64, 1)
+    _need(k_scales, "k_scales", torch.float32, 1)
+    _need(v_scales, "v_scales", torch.float32, 1)
+    T, Hkv, D = key.shape
+    nb, bs = k_cache.shape[0], k_cache.shape[1]
+    _check("pa_reshape_and_cache_fp8", _lib.pa_reshape_and_cache_fp8(
+        _ptr(key), _ptr(value), key.stride(0), value.stride(0), _ptr(k_cache), _ptr(v_cache),
+        _ptr(slot_mapping), _ptr(k_scales), _ptr(v_scales), T, Hkv, D, bs, nb, _stream(stream)))
+
+
+def pa_copy_blocks_fp8(k_cache, v_cache, block_pairs, stream=None) -> None:
+    """Whole-block copies src -> dst of uint8 E4M3 pools; block_pairs int64 [n, 2]."""
+    _need(k_cache, "k_cache", torch.uint8, 4)
+    _need(v_cache, "v_cache", torch.uint8, 4)
+    _need(block_pairs, "block_pairs", torch.int64, 2)
+    nb, bs, Hkv, D = k_cache.shape
+    _check("pa_copy_blocks_fp8", _lib.pa_copy_blocks_fp8(
+        _ptr(k_cache), _ptr(v_cache), _ptr(block_pairs), block_pairs.shape[0], Hkv, D, bs, nb,
+        _stream(stream)))
+
+
+def pa_decode_fp8(out, q, k_cache, v_cache, k_scales, v_scales, block_tables, seq_lens, scale,
+                  partition_tokens=0, out_lse=None, workspace=None, stream=None) -> None:
+    """pa_decode over uint8 E4M3 pools with per-kv-head fp32 scales."""
+    _need(out, "out", torch.bfloat16, 3)
+    _need(q, "q", torch.bfloat16, 3)
+    _need(k_cache, "k_cache", torch.uint8, 4)
+    _need(v_cache, "v_cache", torch.uint8, 4)
+    _need(k_scales, "k_scales", torch.float32, 1)
+    _need(v_scales, "v_scales", torch.float32, 1)
+    _need(block_tables, "block_tables", torch.int32, 2)
+    _need(seq_lens, "seq_lens", torch.int32, 1)
+    if out_lse is not None:
+        _need(out_lse, "out_lse", torch.float32, 2)
+    S, Hq, D = q.shape
+    nb, bs, Hkv, _ = k_cache.shape
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check("pa_decode_fp8", _lib.pa_decode_fp8(
+        _ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(k_scales), _ptr(v_scales),
+        _ptr(block_tables), block_tables.shape[1], _ptr(seq_lens), S, Hq, Hkv, D, bs, nb,
+        float(scale), int(partition_tokens), _ptr(out_lse), _ptr(workspace), ws_bytes,
         _stream(stream)))
 
 

@@ -68,22 +68,26 @@ bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p
 // rows == 0: the same pool seen as (D, tokens, heads), box = 64 columns x 16
 // tokens x Hkv heads -- one whole block, every head, in a single load that
 // lands as [head][token][64 columns].
+// elem = 1: an E4M3 pool (bytes); only the all-heads view, whose box is a
+// whole 128-byte token row (head_dim 128) x 16 tokens x Hkv heads.
 int encode_pool_map_uncached(CUtensorMap* m, const void* pool, int64_t num_blocks, int Hkv, int D,
-                             int rows) {
+                             int rows, int elem) {
   cuuint64_t dims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(Hkv),
                         static_cast<cuuint64_t>(num_blocks) * kBlockSize};
-  cuuint64_t strides[2] = {static_cast<cuuint64_t>(D) * 2, static_cast<cuuint64_t>(Hkv) * D * 2};
-  cuuint32_t box[3] = {64, 1, static_cast<cuuint32_t>(rows)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(D) * elem,
+                           static_cast<cuuint64_t>(Hkv) * D * elem};
+  cuuint32_t box[3] = {static_cast<cuuint32_t>(128 / elem), 1, static_cast<cuuint32_t>(rows)};
   if (rows == 0) {
     dims[1] = static_cast<cuuint64_t>(num_blocks) * kBlockSize;
     dims[2] = static_cast<cuuint64_t>(Hkv);
-    strides[0] = static_cast<cuuint64_t>(Hkv) * D * 2;
-    strides[1] = static_cast<cuuint64_t>(D) * 2;
+    strides[0] = static_cast<cuuint64_t>(Hkv) * D * elem;
+    strides[1] = static_cast<cuuint64_t>(D) * elem;
     box[1] = kBlockSize;
     box[2] = static_cast<cuuint32_t>(Hkv);
   }
   cuuint32_t estr[3] = {1, 1, 1};
-  CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(pool), dims,
+  CUresult r = g_encode(m, elem == 1 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+                        3, const_cast<void*>(pool), dims,
                         strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                         CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
@@ -96,7 +100,7 @@ int encode_pool_map_uncached(CUtensorMap* m, const void* pool, int64_t num_block
 struct PoolMapEntry {
   const void* pool;
   int64_t num_blocks;
-  int Hkv, D, rows;
+  int Hkv, D, rows, elem;
   CUtensorMap map;
 };
 constexpr int kPoolMapCache = 32;
@@ -105,16 +109,17 @@ PoolMapEntry g_map_cache[kPoolMapCache];
 int g_map_next = 0;
 
 int encode_pool_map(CUtensorMap* m, const void* pool, int64_t num_blocks, int Hkv, int D,
-                    int rows) {
+                    int rows, int elem = 2) {
   std::lock_guard<std::mutex> lock(g_map_mu);
   for (int i = 0; i < kPoolMapCache; ++i) {
     const PoolMapEntry& e = g_map_cache[i];
-    if (e.pool == pool && e.num_blocks == num_blocks && e.Hkv == Hkv && e.D == D && e.rows == rows) {
+    if (e.pool == pool && e.num_blocks == num_blocks && e.Hkv == Hkv && e.D == D &&
+        e.rows == rows && e.elem == elem) {
       *m = e.map;
       return PA_OK;
     }
   }
-  if (int rc = encode_pool_map_uncached(m, pool, num_blocks, Hkv, D, rows)) return rc;
+  if (int rc = encode_pool_map_uncached(m, pool, num_blocks, Hkv, D, rows, elem)) return rc;
   PoolMapEntry& e = g_map_cache[g_map_next];
   g_map_next = (g_map_next + 1) % kPoolMapCache;
   e.pool = pool;
@@ -122,6 +127,7 @@ int encode_pool_map(CUtensorMap* m, const void* pool, int64_t num_blocks, int Hk
   e.Hkv = Hkv;
   e.D = D;
   e.rows = rows;
+  e.elem = elem;
   e.map = *m;
   return PA_OK;
 }
@@ -178,6 +184,53 @@ __global__ void reshape_and_cache_kernel(const uint4* __restrict__ key,
   }
   k_cache[slot * vec_per_token + c] = key[t * key_stride16 + c];
   v_cache[slot * vec_per_token + c] = value[t * value_stride16 + c];
+}
+
+// Quantizing scatter into E4M3 pools: one thread turns 8 bf16 of K and of V
+// for one (token, head) into 8 bytes each: code = RNE_sat(x / scale[head]),
+// the division in IEEE fp32, then round to nearest even onto the E4M3 grid,
+// finite values beyond +-448 saturating to +-448.
+__global__ void reshape_and_cache_fp8_kernel(const uint4* __restrict__ key,
+                                             const uint4* __restrict__ value, int64_t key_stride16,
+                                             int64_t value_stride16, uint2* __restrict__ k_cache,
+                                             uint2* __restrict__ v_cache,
+                                             const int64_t* __restrict__ slots,
+                                             const float* __restrict__ k_scales,
+                                             const float* __restrict__ v_scales, int num_tokens,
+                                             int vec_per_token, int vec_per_head,
+                                             int64_t num_slots, unsigned int* err) {
+  griddep_launch_dependents();
+  griddep_wait();
+  const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (i >= static_cast<int64_t>(num_tokens) * vec_per_token) return;
+  const int t = static_cast<int>(i / vec_per_token);
+  const int c = static_cast<int>(i % vec_per_token);
+  const int64_t slot = slots[t];
+  if (slot < 0) return;
+  if (slot >= num_slots) {
+    if (c == 0) atomicOr(err, PA_DEVERR_SLOT);
+    return;
+  }
+  const int h = c / vec_per_head;
+  auto quant8 = [](uint4 x, float sc) {
+    const uint32_t w[4] = {x.x, x.y, x.z, x.w};
+    uint32_t out[2];
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+      uint32_t r = 0;
+#pragma unroll
+      for (int p = 0; p < 2; ++p) {
+        const uint32_t u = w[2 * k + p];
+        const float lo = __fdiv_rn(__uint_as_float(u << 16), sc);
+        const float hi = __fdiv_rn(__uint_as_float(u & 0xffff0000u), sc);
+        r |= static_cast<uint32_t>(f32x2_to_e4m3x2(lo, hi)) << (16 * p);
+      }
+      out[k] = r;
+    }
+    return make_uint2(out[0], out[1]);
+  };
+  k_cache[slot * vec_per_token + c] = quant8(key[t * key_stride16 + c], k_scales[h]);
+  v_cache[slot * vec_per_token + c] = quant8(value[t * value_stride16 + c], v_scales[h]);
 }
 
 __global__ void copy_blocks_kernel(uint4* __restrict__ k_cache, uint4* __restrict__ v_cache,
@@ -338,12 +391,56 @@ int pa_reshape_and_cache(const void* key, const void* value, int64_t key_token_s
   return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
 
-int pa_copy_blocks(void* k_cache, void* v_cache, const int64_t* block_pairs, int num_pairs,
-                   int num_kv_heads, int head_dim, int block_size, int64_t num_blocks,
-                   void* stream) {
-  if (num_pairs < 0 || num_kv_heads <= 0 || head_dim <= 0 || num_blocks <= 0) return PA_ERR_INVALID;
+int pa_reshape_and_cache_fp8(const void* key, const void* value, int64_t key_token_stride,
+                             int64_t value_token_stride, void* k_cache, void* v_cache,
+                             const int64_t* slot_mapping, const float* k_scales,
+                             const float* v_scales, int num_tokens, int num_kv_heads,
+                             int head_dim, int block_size, int64_t num_blocks, void* stream) {
+  if (num_tokens < 0 || num_kv_heads <= 0 || head_dim <= 0 || num_blocks <= 0) return PA_ERR_INVALID;
   if (block_size != kBlockSize) return PA_ERR_UNSUPPORTED;
   if (head_dim % 8 != 0) return PA_ERR_UNSUPPORTED;
+  if (num_tokens == 0) return PA_OK;
+  if (!key || !value || !k_cache || !v_cache || !slot_mapping || !k_scales || !v_scales)
+    return PA_ERR_INVALID;
+  const int64_t row = static_cast<int64_t>(num_kv_heads) * head_dim;
+  if (key_token_stride < row || value_token_stride < row || key_token_stride % 8 ||
+      value_token_stride % 8)
+    return PA_ERR_INVALID;
+  if (!aligned(key, 16) || !aligned(value, 16) || !aligned(k_cache, 8) || !aligned(v_cache, 8) ||
+      !aligned(slot_mapping, 8) || !aligned(k_scales, 4) || !aligned(v_scales, 4))
+    return PA_ERR_INVALID;
+  DeviceInfo* d;
+  if (int rc = current_device_info(&d)) return rc;
+  const int vec = static_cast<int>(row / 8);
+  const int64_t total = static_cast<int64_t>(num_tokens) * vec;
+  const int threads = 256;
+  const int64_t blocks = (total + threads - 1) / threads;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(blocks));
+  cfg.blockDim = dim3(threads);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = static_cast<cudaStream_t>(stream);
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (cudaLaunchKernelEx(&cfg, reshape_and_cache_fp8_kernel, static_cast<const uint4*>(key),
+                         static_cast<const uint4*>(value), key_token_stride / 8,
+                         value_token_stride / 8, static_cast<uint2*>(k_cache),
+                         static_cast<uint2*>(v_cache), slot_mapping, k_scales, v_scales,
+                         num_tokens, vec, head_dim / 8, num_blocks * block_size,
+                         d->err) != cudaSuccess)
+    return PA_ERR_CUDA;
+  return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+
+static int copy_blocks_bytes(void* k_cache, void* v_cache, const int64_t* block_pairs,
+                             int num_pairs, int num_kv_heads, int head_dim, int block_size,
+                             int64_t num_blocks, int elem, void* stream) {
+  if (num_pairs < 0 || num_kv_heads <= 0 || head_dim <= 0 || num_blocks <= 0) return PA_ERR_INVALID;
+  if (block_size != kBlockSize) return PA_ERR_UNSUPPORTED;
+  if ((head_dim * elem) % 16 != 0) return PA_ERR_UNSUPPORTED;
   if (num_pairs == 0) return PA_OK;
   if (num_pairs > 65535) return PA_ERR_UNSUPPORTED;
   if (!k_cache || !v_cache || !block_pairs) return PA_ERR_INVALID;
@@ -351,12 +448,26 @@ int pa_copy_blocks(void* k_cache, void* v_cache, const int64_t* block_pairs, int
     return PA_ERR_INVALID;
   DeviceInfo* d;
   if (int rc = current_device_info(&d)) return rc;
-  const int64_t vec = static_cast<int64_t>(block_size) * num_kv_heads * head_dim / 8;
+  const int64_t vec = static_cast<int64_t>(block_size) * num_kv_heads * head_dim * elem / 16;
   dim3 grid(static_cast<unsigned>((vec + 255) / 256 < 64 ? (vec + 255) / 256 : 64), num_pairs);
   copy_blocks_kernel<<<grid, 256, 0, static_cast<cudaStream_t>(stream)>>>(
       static_cast<uint4*>(k_cache), static_cast<uint4*>(v_cache), block_pairs, vec, num_blocks,
       d->err);
   return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+
+int pa_copy_blocks(void* k_cache, void* v_cache, const int64_t* block_pairs, int num_pairs,
+                   int num_kv_heads, int head_dim, int block_size, int64_t num_blocks,
+                   void* stream) {
+  return copy_blocks_bytes(k_cache, v_cache, block_pairs, num_pairs, num_kv_heads, head_dim,
+                           block_size, num_blocks, 2, stream);
+}
+
+int pa_copy_blocks_fp8(void* k_cache, void* v_cache, const int64_t* block_pairs, int num_pairs,
+                       int num_kv_heads, int head_dim, int block_size, int64_t num_blocks,
+                       void* stream) {
+  return copy_blocks_bytes(k_cache, v_cache, block_pairs, num_pairs, num_kv_heads, head_dim,
+                           block_size, num_blocks, 1, stream);
 }
 
 static int decode_mode(int partition_tokens) {
@@ -392,24 +503,30 @@ size_t pa_decode_workspace_size(int num_seqs, int num_q_heads, int num_kv_heads,
   return balanced_workspace_bytes(decode_grid(num_sms, kModeBalanced), num_q_heads, head_dim);
 }
 
-int pa_decode(void* out, const void* q, const void* k_cache, const void* v_cache,
-              const int32_t* block_tables, int max_blocks_per_seq, const int32_t* seq_lens,
-              int num_seqs, int num_q_heads, int num_kv_heads, int head_dim, int block_size,
-              int64_t num_blocks, float scale, int partition_tokens, float* out_lse,
-              void* workspace, size_t workspace_bytes, void* stream) {
+// pa_decode and pa_decode_fp8: the same launch; kv_fp8 selects E4M3 pools.
+static int decode_impl(void* out, const void* q, const void* k_cache, const void* v_cache,
+                       const float* k_scales, const float* v_scales, bool kv_fp8,
+                       const int32_t* block_tables, int max_blocks_per_seq,
+                       const int32_t* seq_lens, int num_seqs, int num_q_heads,
+                       int num_kv_heads, int head_dim, int block_size, int64_t num_blocks,
+                       float scale, int partition_tokens, float* out_lse, void* workspace,
+                       size_t workspace_bytes, void* stream) {
   if (int rc = check_shape(num_q_heads, num_kv_heads, head_dim, block_size)) return rc;
+  if (kv_fp8 && head_dim != 128) return PA_ERR_UNSUPPORTED;
   if (num_seqs < 0 || max_blocks_per_seq <= 0 || num_blocks <= 0) return PA_ERR_INVALID;
   if (num_blocks * kBlockSize > (int64_t)INT32_MAX) return PA_ERR_UNSUPPORTED;
   if (!(scale > 0.f) || !isfinite(scale)) return PA_ERR_INVALID;
   if (num_seqs == 0) return PA_OK;
   if (!out || !q || !k_cache || !v_cache || !block_tables || !seq_lens) return PA_ERR_INVALID;
+  if (kv_fp8 && (!k_scales || !v_scales || !aligned(k_scales, 4) || !aligned(v_scales, 4)))
+    return PA_ERR_INVALID;
   if (!aligned(out, 16) || !aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) ||
       !aligned(block_tables, 4) || !aligned(seq_lens, 4) || (out_lse && !aligned(out_lse, 4)))
     return PA_ERR_INVALID;
   const int mode = decode_mode(partition_tokens);
   if (mode == kModeFixedSplit && partition_tokens % block_size) return PA_ERR_INVALID;
   if (mode == kModeBalanced && num_seqs > kMaxSeqsBalanced) return PA_ERR_UNSUPPORTED;
-  if (!decode_supported(head_dim, num_kv_heads, num_q_heads, mode, num_seqs))
+  if (!decode_supported(head_dim, num_kv_heads, num_q_heads, mode, num_seqs, kv_fp8))
     return PA_ERR_UNSUPPORTED;
   DeviceInfo* d;
   if (int rc = current_device_info(&d)) return rc;
@@ -429,6 +546,9 @@ int pa_decode(void* out, const void* q, const void* k_cache, const void* v_cache
   a.group = num_q_heads / num_kv_heads;
   a.scale_log2 = scale * 1.4426950408889634f;
   a.mode = mode;
+  a.kv_fp8 = kv_fp8 ? 1 : 0;
+  a.k_scales = k_scales;
+  a.v_scales = v_scales;
   int grid = decode_grid(d->num_sms, mode);
   if (mode == kModeSinglePass) {
     a.part_blocks = max_blocks_per_seq;
@@ -455,8 +575,9 @@ int pa_decode(void* out, const void* q, const void* k_cache, const void* v_cache
   }
 
   CUtensorMap tm_k, tm_v;
-  if (encode_pool_map(&tm_k, k_cache, num_blocks, num_kv_heads, head_dim, 0) ||
-      encode_pool_map(&tm_v, v_cache, num_blocks, num_kv_heads, head_dim, 0))
+  const int elem = kv_fp8 ? 1 : 2;
+  if (encode_pool_map(&tm_k, k_cache, num_blocks, num_kv_heads, head_dim, 0, elem) ||
+      encode_pool_map(&tm_v, v_cache, num_blocks, num_kv_heads, head_dim, 0, elem))
     return PA_ERR_CUDA;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (launch_decode(a, &tm_k, &tm_v, head_dim, grid, st) != cudaSuccess) return PA_ERR_CUDA;
@@ -478,6 +599,29 @@ int pa_decode(void* out, const void* q, const void* k_cache, const void* v_cache
     if (launch_merge(m, st) != cudaSuccess) return PA_ERR_CUDA;
   }
   return PA_OK;
+}
+
+int pa_decode(void* out, const void* q, const void* k_cache, const void* v_cache,
+              const int32_t* block_tables, int max_blocks_per_seq, const int32_t* seq_lens,
+              int num_seqs, int num_q_heads, int num_kv_heads, int head_dim, int block_size,
+              int64_t num_blocks, float scale, int partition_tokens, float* out_lse,
+              void* workspace, size_t workspace_bytes, void* stream) {
+  return decode_impl(out, q, k_cache, v_cache, nullptr, nullptr, false, block_tables,
+                     max_blocks_per_seq, seq_lens, num_seqs, num_q_heads, num_kv_heads, head_dim,
+                     block_size, num_blocks, scale, partition_tokens, out_lse, workspace,
+                     workspace_bytes, stream);
+}
+
+int pa_decode_fp8(void* out, const void* q, const void* k_cache, const void* v_cache,
+                  const float* k_scales, const float* v_scales, const int32_t* block_tables,
+                  int max_blocks_per_seq, const int32_t* seq_lens, int num_seqs,
+                  int num_q_heads, int num_kv_heads, int head_dim, int block_size,
+                  int64_t num_blocks, float scale, int partition_tokens, float* out_lse,
+                  void* workspace, size_t workspace_bytes, void* stream) {
+  return decode_impl(out, q, k_cache, v_cache, k_scales, v_scales, true, block_tables,
+                     max_blocks_per_seq, seq_lens, num_seqs, num_q_heads, num_kv_heads, head_dim,
+                     block_size, num_blocks, scale, partition_tokens, out_lse, workspace,
+                     workspace_bytes, stream);
 }
 
 // Static scratch of pa_decode_noalloc: the balanced split's merge tickets and

@@ -73,9 +73,9 @@ struct Layout {
 };
 
 __host__ __device__ inline Layout make_layout(int D, int Hkv, int Hq, int wph, int stages,
-                                              int pre_ints) {
+                                              int pre_ints, int elem_bytes) {
   Layout L;
-  L.head_bytes = (D / 64) * kBoxBytes;
+  L.head_bytes = kBlockSize * D * elem_bytes;
   L.stage_bytes = 2 * Hkv * L.head_bytes;
   L.stages = stages;
   L.q_bytes = (Hq * D * 2 + 127) / 128 * 128;
@@ -241,6 +241,124 @@ __device__ __forceinline__ void attend_block(uint32_t kbase, uint32_t vbase, uin
   }
 }
 
+// One 16-token block of E4M3 K/V for one kv head (head_dim 128).  The stage
+// holds, for K and then for V, one box [head][token][128 bytes] with the
+// 128-byte swizzle.  A lane converts its own bytes to f16 in registers
+// (exactly: every E4M3 value is an f16 value) and the contractions run as f16
+// warp MMAs.  The head dimension is visited in a permuted order, the same for
+// the query fragments (a dot product does not depend on the order), so that a
+// lane's bytes are contiguous:
+//  * S^T = K Q^T: lane (g, c) holds, at k-step ks, dims 32c + 4ks + {0, 1}
+//    (fragment columns 2c, 2c+1) and 32c + 4ks + {2, 3} (columns 2c+8, 2c+9)
+//    of tokens g and g + 8: two 16-byte loads per token row;
+//  * O^T += V^T P^T: row g of m-tile mt is dim 16g + 2mt and row g + 8 is dim
+//    16g + 2mt + 1 (out_dim<true>), so lane (g, c) needs dims [16g, 16g + 16)
+//    of tokens 2c, 2c+1, 2c+8, 2c+9: one 16-byte load per token, and byte
+//    pairs of two tokens are interleaved with prmt before the conversion.
+// The scores come out in units of sl2 (the query's power-of-two scale and the
+// K scale folded in); the V scale is applied to the finished output.
+template <int D>
+__device__ __forceinline__ void attend_block_fp8(uint32_t kbase, uint32_t vbase,
+                                                 const uint32_t (&qf)[D / 16][2],
+                                                 float (&o)[D / 16][4], float& m0, float& m1,
+                                                 float& l0, float& l1, int valid, float sl2,
+                                                 int lane) {
+  static_assert(D == 128, "the E4M3 path has 128-byte token rows");
+  constexpr int KS = D / 16;
+  const int g = lane >> 2, c = lane & 3;
+  uint32_t kw[2][8];
+#pragma unroll
+  for (int r = 0; r < 2; ++r) {
+    const int tok = g + 8 * r;
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const uint4 v = lds128(kbase + tok * 128 + (((2 * c + h) ^ (tok & 7)) << 4));
+      kw[r][4 * h + 0] = v.x;
+      kw[r][4 * h + 1] = v.y;
+      kw[r][4 * h + 2] = v.z;
+      kw[r][4 * h + 3] = v.w;
+    }
+  }
+  float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+  for (int ks = 0; ks < KS; ++ks) {
+    uint32_t ka[4];
+    ka[0] = e4m3x2_to_f16x2(kw[0][ks]);
+    ka[1] = e4m3x2_to_f16x2(kw[1][ks]);
+    ka[2] = e4m3x2_to_f16x2(kw[0][ks] >> 16);
+    ka[3] = e4m3x2_to_f16x2(kw[1][ks] >> 16);
+    if (ks & 1)
+      mma_f16_16816(sb, ka, qf[ks][0], qf[ks][1]);
+    else
+      mma_f16_16816(sa, ka, qf[ks][0], qf[ks][1]);
+  }
+  const int t0 = lane >> 2;
+  const bool v0 = t0 < valid, v1 = t0 + 8 < valid;
+  const float x0 = v0 ? (sa[0] + sb[0]) * sl2 : -INFINITY;
+  const float x1 = v0 ? (sa[1] + sb[1]) * sl2 : -INFINITY;
+  const float x2 = v1 ? (sa[2] + sb[2]) * sl2 : -INFINITY;
+  const float x3 = v1 ? (sa[3] + sb[3]) * sl2 : -INFINITY;
+  float mxa = fmaxf(x0, x2), mxb = fmaxf(x1, x3);
+#pragma unroll
+  for (int off = 4; off < 32; off <<= 1) {
+    mxa = fmaxf(mxa, __shfl_xor_sync(0xffffffffu, mxa, off));
+    mxb = fmaxf(mxb, __shfl_xor_sync(0xffffffffu, mxb, off));
+  }
+  const float mna = fmaxf(m0, mxa), mnb = fmaxf(m1, mxb);
+  const float aa = fast_exp2(m0 - mna), ab = fast_exp2(m1 - mnb);
+  const float pa0 = fast_exp2(x0 - mna), pb0 = fast_exp2(x1 - mnb);
+  const float pa1 = fast_exp2(x2 - mna), pb1 = fast_exp2(x3 - mnb);
+  l0 = l0 * aa + pa0 + pa1;
+  l1 = l1 * ab + pb0 + pb1;
+  m0 = mna;
+  m1 = mnb;
+#pragma unroll
+  for (int mt = 0; mt < KS; ++mt) {
+    o[mt][0] *= aa;
+    o[mt][1] *= ab;
+    o[mt][2] *= aa;
+    o[mt][3] *= ab;
+  }
+  const uint32_t b0 = movmatrix_trans(pack_f16x2(pa0, pb0));
+  const uint32_t b1 = movmatrix_trans(pack_f16x2(pa1, pb1));
+  uint32_t keep01 = 0xffffffffu, keep23 = 0xffffffffu;
+  if (valid < 16) {  // masked tokens have p = 0, but their V bytes may hold anything
+    const int q2 = c * 2;
+    keep01 = (q2 < valid ? 0x0000ffffu : 0u) | (q2 + 1 < valid ? 0xffff0000u : 0u);
+    keep23 = (q2 + 8 < valid ? 0x0000ffffu : 0u) | (q2 + 9 < valid ? 0xffff0000u : 0u);
+  }
+  uint32_t vw[4][4];
+#pragma unroll
+  for (int r = 0; r < 4; ++r) {
+    const int tok = 2 * c + (r & 1) + 8 * (r >> 1);
+    const uint4 v = lds128(vbase + tok * 128 + ((g ^ (tok & 7)) << 4));
+    vw[r][0] = v.x;
+    vw[r][1] = v.y;
+    vw[r][2] = v.z;
+    vw[r][3] = v.w;
+  }
+#pragma unroll
+  for (int mt = 0; mt < KS; ++mt) {
+    const int j = mt >> 1;
+    const uint32_t sel = (mt & 1) ? 0x7362u : 0x5140u;  // bytes 2mt, 2mt+1 of two tokens
+    const uint32_t t01 = prmt(vw[0][j], vw[1][j], sel);
+    const uint32_t t23 = prmt(vw[2][j], vw[3][j], sel);
+    uint32_t va[4];
+    va[0] = e4m3x2_to_f16x2(t01) & keep01;
+    va[1] = e4m3x2_to_f16x2(t01 >> 16) & keep01;
+    va[2] = e4m3x2_to_f16x2(t23) & keep23;
+    va[3] = e4m3x2_to_f16x2(t23 >> 16) & keep23;
+    mma_f16_16816(o[mt], va, b0, b1);
+  }
+}
+
+// Head-dimension index of output fragment row g (+8 when half = 1) of m-tile
+// mt: natural order for bf16, the permuted order of attend_block_fp8 for E4M3.
+template <bool KV8>
+__device__ __forceinline__ int out_dim(int mt, int g, int half) {
+  return KV8 ? 16 * g + 2 * mt + half : mt * 16 + g + 8 * half;
+}
+
 // Log-sum-exp merge of a sequence's partial pieces, held in the slots of CTAs
 // c_first (its "after" slot) and c_first+1 .. c_first+npieces-1 ("before"
 // slots); writes the final bf16 output (and lse).  Each thread owns kNI float4
@@ -326,7 +444,7 @@ __device__ __noinline__ void merge_pieces(const DecodeArgs& a, int s, long long 
   }
 }
 
-template <int D>
+template <int D, bool KV8>
 __global__ void __launch_bounds__(kThreads, 1)
     decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                   const DecodeArgs a) {
@@ -338,7 +456,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int Hkv = a.num_kv_heads, G = a.group, Hq = a.num_q_heads;
   const int wph = a.warps_per_head;
-  const Layout L = make_layout(D, Hkv, Hq, wph, a.stages, 0);
+  const Layout L = make_layout(D, Hkv, Hq, wph, a.stages, 0, KV8 ? 1 : 2);
   float* obuf = reinterpret_cast<float*>(smem + L.obuf_off);
   float* mlbuf = reinterpret_cast<float*>(smem + L.ml_off);
   int* misc = reinterpret_cast<int*>(smem + L.misc_off);
@@ -500,10 +618,15 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t kdst = sbase + st * L.stage_bytes;
           const uint32_t vdst = kdst + Hkv * L.head_bytes;
           const int y = blk * kBlockSize;
+          if constexpr (KV8) {  // E4M3: a token row of a head is 128 bytes, one box
+            tma_load_3d(kdst, &tm_k, 0, y, 0, fb, pol);
+            tma_load_3d(vdst, &tm_v, 0, y, 0, fb, pol);
+          } else {
 #pragma unroll
-          for (int h = 0; h < D / 64; ++h) {
-            tma_load_3d(kdst + h * Hkv * kBoxBytes, &tm_k, h * 64, y, 0, fb, pol);
-            tma_load_3d(vdst + h * Hkv * kBoxBytes, &tm_v, h * 64, y, 0, fb, pol);
+            for (int h = 0; h < D / 64; ++h) {
+              tma_load_3d(kdst + h * Hkv * kBoxBytes, &tm_k, h * 64, y, 0, fb, pol);
+              tma_load_3d(vdst + h * Hkv * kBoxBytes, &tm_v, h * 64, y, 0, fb, pol);
+            }
           }
         }
       }
@@ -538,6 +661,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const bool active = warp < active_warps;
   const int hw = warp % Hkv;   // this warp's kv head
+  const float vsc = KV8 && active ? a.v_scales[hw] : 1.f;  // E4M3: V dequantization scale
   const int sub = warp / Hkv;  // which of the head's warps
   const int q4 = lane & 3;
   const int d0 = lane >> 2;
@@ -553,6 +677,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   while (next_piece(a, pre, cur, pc, ctid == 0)) {
     const long long head0 = static_cast<long long>(pc.s) * Hq + hw * G;
     uint32_t qf[KS][2];
+    float sl2 = a.scale_log2;  // scores to log2 units (E4M3: scales folded in)
     if (active) {
       // query fragments of the group (B operand: k = dim, n = head) from the
       // piece's staged query rows
@@ -562,16 +687,54 @@ __global__ void __launch_bounds__(kThreads, 1)
         *abort_flag = 1;
       }
       const uint32_t qrow = sbase + L.q_off + k * L.q_bytes + (hw * G + hq) * D * 2;
+      if constexpr (KV8) {
+        // f16 fragments in the permuted dim order of attend_block_fp8:
+        // k-step ks takes dims 32c + 4ks + {0,1} and {2,3}.  The group's
+        // queries are scaled by one power of two 2^e that puts their largest
+        // magnitude in [2^14, 2^15): exact in fp32, no f16 overflow; 2^-e and
+        // the K scale go into sl2.
+        uint32_t w[KS][2];
+        float mx = 0.f;
 #pragma unroll
-      for (int ks = 0; ks < KS; ++ks) {
-        const uint32_t c = (ks * 16 + q4 * 2) * 2;
-        uint32_t x0 = 0u, x1 = 0u;
-        if (hq < G) {
-          asm volatile("ld.shared.b32 %0, [%1];" : "=r"(x0) : "r"(qrow + c));
-          asm volatile("ld.shared.b32 %0, [%1];" : "=r"(x1) : "r"(qrow + c + 16));
+        for (int ks = 0; ks < KS; ++ks) {
+          uint32_t x0 = 0u, x1 = 0u;
+          if (hq < G)
+            asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];"
+                         : "=r"(x0), "=r"(x1)
+                         : "r"(qrow + (32 * q4 + 4 * ks) * 2));
+          w[ks][0] = x0;
+          w[ks][1] = x1;
+          mx = fmaxf(mx, fmaxf(fmaxf(fabsf(__uint_as_float(x0 << 16)),
+                                     fabsf(__uint_as_float(x0 & 0xffff0000u))),
+                               fmaxf(fabsf(__uint_as_float(x1 << 16)),
+                                     fabsf(__uint_as_float(x1 & 0xffff0000u)))));
         }
-        qf[ks][0] = x0;
-        qf[ks][1] = x1;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+        int ex = 0;
+        if (mx > 0.f && isfinite(mx)) frexpf(mx, &ex);  // mx < 2^ex
+        const int e = ex == 0 ? 0 : min(126, max(-126, 15 - ex));
+        const float p2 = ldexpf(1.f, e);
+#pragma unroll
+        for (int ks = 0; ks < KS; ++ks) {
+          qf[ks][0] = pack_f16x2(__uint_as_float(w[ks][0] << 16) * p2,
+                                 __uint_as_float(w[ks][0] & 0xffff0000u) * p2);
+          qf[ks][1] = pack_f16x2(__uint_as_float(w[ks][1] << 16) * p2,
+                                 __uint_as_float(w[ks][1] & 0xffff0000u) * p2);
+        }
+        sl2 = a.scale_log2 * a.k_scales[hw] * ldexpf(1.f, -e);
+      } else {
+#pragma unroll
+        for (int ks = 0; ks < KS; ++ks) {
+          const uint32_t c = (ks * 16 + q4 * 2) * 2;
+          uint32_t x0 = 0u, x1 = 0u;
+          if (hq < G) {
+            asm volatile("ld.shared.b32 %0, [%1];" : "=r"(x0) : "r"(qrow + c));
+            asm volatile("ld.shared.b32 %0, [%1];" : "=r"(x1) : "r"(qrow + c + 16));
+          }
+          qf[ks][0] = x0;
+          qf[ks][1] = x1;
+        }
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(bar_qempty + k * 8);
@@ -593,9 +756,15 @@ __global__ void __launch_bounds__(kThreads, 1)
           continue;
         }
         const int valid = min(kBlockSize, pc.len - j * kBlockSize);
-        const uint32_t kb = sbase + st * L.stage_bytes + hw * kBoxBytes;
-        attend_block<D>(kb, kb + Hkv * L.head_bytes, Hkv * kBoxBytes, qf, o, m0, m1, l0, l1,
-                        valid, a.scale_log2, lane);
+        if constexpr (KV8) {
+          const uint32_t kb = sbase + st * L.stage_bytes + hw * L.head_bytes;
+          attend_block_fp8<D>(kb, kb + Hkv * L.head_bytes, qf, o, m0, m1, l0, l1, valid, sl2,
+                              lane);
+        } else {
+          const uint32_t kb = sbase + st * L.stage_bytes + hw * kBoxBytes;
+          attend_block<D>(kb, kb + Hkv * L.head_bytes, Hkv * kBoxBytes, qf, o, m0, m1, l0, l1,
+                          valid, a.scale_log2, lane);
+        }
         __syncwarp();
         if (lane == 0) mbar_arrive(bar_empty + st * 8);
       }
@@ -637,17 +806,21 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       fa = f[0];
       fb = f[1];
+      if constexpr (KV8) {
+        fa *= vsc;
+        fb *= vsc;
+      }
       lsea = ls[0];
       lseb = ls[1];
       if (active) {
         float* ob = obuf + warp * kMaxGroup * (D + 4);
 #pragma unroll
         for (int mt = 0; mt < KS; ++mt) {
-          const int d = mt * 16 + d0;
+          const int d = out_dim<KV8>(mt, d0, 0), d8 = out_dim<KV8>(mt, d0, 1);
           ob[(2 * q4) * (D + 4) + d] = o[mt][0] * fa;
           ob[(2 * q4 + 1) * (D + 4) + d] = o[mt][1] * fb;
-          ob[(2 * q4) * (D + 4) + d + 8] = o[mt][2] * fa;
-          ob[(2 * q4 + 1) * (D + 4) + d + 8] = o[mt][3] * fb;
+          ob[(2 * q4) * (D + 4) + d8] = o[mt][2] * fa;
+          ob[(2 * q4 + 1) * (D + 4) + d8] = o[mt][3] * fb;
         }
       }
       named_barrier(1, kConsumerThreads);
@@ -655,14 +828,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (active && sub == 0) {
 #pragma unroll
         for (int mt = 0; mt < KS; ++mt) {
-          const int d = mt * 16 + d0;
+          const int d = out_dim<KV8>(mt, d0, 0), d8 = out_dim<KV8>(mt, d0, 1);
           float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
           for (int w2 = 0; w2 < wph; ++w2) {
             const float* ob = obuf + (w2 * Hkv + hw) * kMaxGroup * (D + 4);
             s0 += ob[(2 * q4) * (D + 4) + d];
             s1 += ob[(2 * q4 + 1) * (D + 4) + d];
-            s2 += ob[(2 * q4) * (D + 4) + d + 8];
-            s3 += ob[(2 * q4 + 1) * (D + 4) + d + 8];
+            s2 += ob[(2 * q4) * (D + 4) + d8];
+            s3 += ob[(2 * q4 + 1) * (D + 4) + d8];
           }
           o[mt][0] = s0;
           o[mt][1] = s1;
@@ -674,6 +847,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else {
       fa = l0 > 0.f ? 1.f / l0 : 0.f;
       fb = l1 > 0.f ? 1.f / l1 : 0.f;
+      if constexpr (KV8) {
+        fa *= vsc;
+        fb *= vsc;
+      }
       lsea = l0 > 0.f ? (m0 + __log2f(l0)) * kLn2 : -INFINITY;
       lseb = l1 > 0.f ? (m1 + __log2f(l1)) * kLn2 : -INFINITY;
 #pragma unroll
@@ -684,21 +861,21 @@ __global__ void __launch_bounds__(kThreads, 1)
         o[mt][3] *= fb;
       }
     }
-    // lanes own o^T[d = mt*16 + d0 (+8)][head 2*q4 (+1)] of kv head hw
+    // lanes own o^T[out_dim(mt, d0, 0 / 1)][head 2*q4 (+1)] of kv head hw
     const bool writer = active && sub == 0;
     const int ha = 2 * q4, hb = 2 * q4 + 1;
     if (pc.kind == kFinal) {
       if (writer) {
 #pragma unroll
         for (int mt = 0; mt < KS; ++mt) {
-          const int d = mt * 16 + d0;
+          const int d = out_dim<KV8>(mt, d0, 0), d8 = out_dim<KV8>(mt, d0, 1);
           if (ha < G) {
             a.out[(head0 + ha) * D + d] = __float2bfloat16(o[mt][0]);
-            a.out[(head0 + ha) * D + d + 8] = __float2bfloat16(o[mt][2]);
+            a.out[(head0 + ha) * D + d8] = __float2bfloat16(o[mt][2]);
           }
           if (hb < G) {
             a.out[(head0 + hb) * D + d] = __float2bfloat16(o[mt][1]);
-            a.out[(head0 + hb) * D + d + 8] = __float2bfloat16(o[mt][3]);
+            a.out[(head0 + hb) * D + d8] = __float2bfloat16(o[mt][3]);
           }
         }
         if (a.out_lse && d0 == 0) {
@@ -710,17 +887,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (writer) {
 #pragma unroll
         for (int mt = 0; mt < KS; ++mt) {
-          const int d = mt * 16 + d0;
+          const int d = out_dim<KV8>(mt, d0, 0), d8 = out_dim<KV8>(mt, d0, 1);
           if (ha < G) {
             const long long row = (head0 + ha) * a.max_parts + pc.part;
             a.part_o[row * D + d] = o[mt][0];
-            a.part_o[row * D + d + 8] = o[mt][2];
+            a.part_o[row * D + d8] = o[mt][2];
             if (mt == 0 && d0 == 0) a.part_lse[row] = lsea;
           }
           if (hb < G) {
             const long long row = (head0 + hb) * a.max_parts + pc.part;
             a.part_o[row * D + d] = o[mt][1];
-            a.part_o[row * D + d + 8] = o[mt][3];
+            a.part_o[row * D + d8] = o[mt][3];
             if (mt == 0 && d0 == 0) a.part_lse[row] = lseb;
           }
         }
@@ -732,14 +909,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int hga = hw * G + ha, hgb = hw * G + hb;
 #pragma unroll
         for (int mt = 0; mt < KS; ++mt) {
-          const int d = mt * 16 + d0;
+          const int d = out_dim<KV8>(mt, d0, 0), d8 = out_dim<KV8>(mt, d0, 1);
           if (ha < G) {
             slot[hga * D + d] = o[mt][0];
-            slot[hga * D + d + 8] = o[mt][2];
+            slot[hga * D + d8] = o[mt][2];
           }
           if (hb < G) {
             slot[hgb * D + d] = o[mt][1];
-            slot[hgb * D + d + 8] = o[mt][3];
+            slot[hgb * D + d8] = o[mt][3];
           }
         }
         if (d0 == 0) {
@@ -781,11 +958,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 int warps_per_head(int Hkv) { return Hkv >= kConsumerWarps ? 1 : kConsumerWarps / Hkv; }
 
-int pick_stages(int D, int Hkv, int Hq, int pre_ints) {
+int pick_stages(int D, int Hkv, int Hq, int pre_ints, int elem_bytes) {
   const int wph = warps_per_head(Hkv);
   const int budget = 227 * 1024 - 1024;  // minus alignment slack
   int st = kMaxStages;
-  while (st > 2 && make_layout(D, Hkv, Hq, wph, st, pre_ints).total > budget) --st;
+  while (st > 2 && make_layout(D, Hkv, Hq, wph, st, pre_ints, elem_bytes).total > budget) --st;
   return st;
 }
 
@@ -806,33 +983,37 @@ int decode_grid(int num_sms, int mode) {
   return num_sms;
 }
 
-bool decode_supported(int head_dim, int num_kv_heads, int num_q_heads, int mode, int num_seqs) {
+bool decode_supported(int head_dim, int num_kv_heads, int num_q_heads, int mode, int num_seqs,
+                      bool kv_fp8) {
   if (num_kv_heads > kConsumerWarps) return false;
+  if (kv_fp8 && head_dim != 128) return false;
   const int pre = mode == kModeBalanced ? num_seqs + 1 : 0;
   const int wph = warps_per_head(num_kv_heads);
-  return make_layout(head_dim, num_kv_heads, num_q_heads, wph, 2, pre).total <=
+  return make_layout(head_dim, num_kv_heads, num_q_heads, wph, 2, pre, kv_fp8 ? 1 : 2).total <=
          227 * 1024 - 1024;
 }
 
 cudaError_t launch_decode(DecodeArgs a, const CUtensorMap* tm_k, const CUtensorMap* tm_v,
                           int head_dim, int grid, cudaStream_t stream) {
   const int pre = a.mode == kModeBalanced ? a.num_seqs + 1 : 0;
+  const int elem = a.kv_fp8 ? 1 : 2;
   a.warps_per_head = warps_per_head(a.num_kv_heads);
-  a.stages = pick_stages(head_dim, a.num_kv_heads, a.num_q_heads, pre);
+  a.stages = pick_stages(head_dim, a.num_kv_heads, a.num_q_heads, pre, elem);
   const size_t smem = make_layout(head_dim, a.num_kv_heads, a.num_q_heads, a.warps_per_head,
-                                  a.stages, pre).total + 1024;
+                                  a.stages, pre, elem).total + 1024;
   void (*kern)(const CUtensorMap, const CUtensorMap, const DecodeArgs) =
-      head_dim == 128 ? decode_kernel<128> : decode_kernel<64>;
+      a.kv_fp8 ? decode_kernel<128, true>
+               : (head_dim == 128 ? decode_kernel<128, false> : decode_kernel<64, false>);
   // raise the kernel's dynamic shared-memory limit once per device
   static std::mutex mu;
-  static int set_for[2][64] = {};
+  static int set_for[3][64] = {};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
   {
     std::lock_guard<std::mutex> lock(mu);
-    int& done = set_for[head_dim == 128 ? 1 : 0][dev];
+    int& done = set_for[a.kv_fp8 ? 2 : (head_dim == 128 ? 1 : 0)][dev];
     if (done < static_cast<int>(smem)) {
       e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                227 * 1024);

@@ -42,6 +42,9 @@ struct DecodeArgs {
   int slot_floats;   // balanced: floats per partial slot
   int warps_per_head;  // set by the launcher
   int stages;          // set by the launcher
+  int kv_fp8;          // pools hold E4M3 bytes (head_dim 128) with per-kv-head scales
+  const float* k_scales;  // E4M3: [Hkv] dequantization scales of K and V
+  const float* v_scales;
 };
 
 struct MergeArgs {
@@ -87,7 +90,8 @@ size_t balanced_workspace_bytes(int grid, int num_q_heads, int head_dim);
 cudaError_t launch_decode(DecodeArgs a, const CUtensorMap* tm_k, const CUtensorMap* tm_v,
                           int head_dim, int grid, cudaStream_t stream);
 int decode_grid(int num_sms, int mode);
-bool decode_supported(int head_dim, int num_kv_heads, int num_q_heads, int mode, int num_seqs);
+bool decode_supported(int head_dim, int num_kv_heads, int num_q_heads, int mode, int num_seqs,
+                      bool kv_fp8);
 cudaError_t launch_merge(const MergeArgs& a, cudaStream_t stream);
 cudaError_t launch_prefill(const PrefillArgs& a, const CUtensorMap* tm_q, const CUtensorMap* tm_k,
                            const CUtensorMap* tm_v, int grid_tiles, cudaStream_t stream);
