@@ -596,6 +596,55 @@ def reference_arm(args):
                     "d2h_bytes_per_step": 0}}
 
 
+def profile_case(args):
+    """Three launches of one kernel on a small case, for an ncu capture (ncu
+    is run on this command; see profiles/): the decode (bf16 or E4M3) on the
+    Llama-3-8B-shaped layer, or the Sarathi prefill chunk."""
+    import numpy as np
+    import torch
+
+    from paged_kv_cache_218_gb300 import binding as pa
+    from paged_kv_cache_218_gb300 import workload as W
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    w = W.sarathi_hybrid() if args.profile_case == "prefill" else W.llama3_8b_layer()
+    r = Replica(w, dev)
+    pa.pa_reshape_and_cache(r.key, r.value, r.k_cache, r.v_cache, r.slot_mapping)
+    S, Hq, D = w.num_decode_seqs, w.num_q_heads, w.head_dim
+    if args.profile_case == "prefill":
+        T = int(w.cu_q_lens[w.num_chunks])
+        max_q = int(max(w.cu_q_lens[1:] - w.cu_q_lens[:-1]))
+        for _ in range(3):
+            pa.pa_prefill_chunk(r.out_chunk, r.q[:T], r.k_cache, r.v_cache,
+                                r.block_tables[:w.num_chunks], r.cu, r.qs,
+                                r.seq_lens[:w.num_chunks], max_q, w.scale)
+    else:
+        ws = pa.alloc_workspace(pa.pa_decode_workspace_size(S, Hq, w.num_kv_heads, D,
+                                                            w.max_blocks_per_seq, 16, 0), dev)
+        args_d = decode_args(w, r)
+        if args.profile_case == "decode":
+            for _ in range(3):
+                pa.pa_decode(*args_d, w.scale, partition_tokens=0, workspace=ws)
+        else:
+            nb, bs, Hkv, _ = r.k_cache.shape
+            kf = torch.empty((nb, bs, Hkv, D), dtype=torch.uint8, device=dev)
+            vf = torch.empty_like(kf)
+            ks = (r.k_cache.float().abs().amax(dim=(0, 1, 3)) / 448.0).contiguous()
+            vs = (r.v_cache.float().abs().amax(dim=(0, 1, 3)) / 448.0).contiguous()
+            pa.pa_reshape_and_cache_fp8(r.k_cache.view(nb * bs, Hkv, D),
+                                        r.v_cache.view(nb * bs, Hkv, D), kf, vf,
+                                        torch.arange(nb * bs, dtype=torch.int64, device=dev),
+                                        ks, vs)
+            out, q, _, _, bt, sl = args_d
+            for _ in range(3):
+                pa.pa_decode_fp8(out, q, kf, vf, ks, vs, bt, sl, w.scale, partition_tokens=0,
+                                 workspace=ws)
+    torch.cuda.synchronize()
+    if pa.pa_device_error_flags() != 0:
+        raise RuntimeError("device error flags set")
+    print("ok")
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
@@ -612,7 +661,12 @@ def main():
                     help="decode-only launches timed for the roofline's kernel duration")
     ap.add_argument("--no-graphs", action="store_true",
                     help="launch every kernel from Python instead of replaying CUDA graphs")
+    ap.add_argument("--profile-case", default=None, choices=["decode", "decode_fp8", "prefill"],
+                    help="run three launches of one kernel on a small case (for ncu) and exit")
     args = ap.parse_args()
+    if args.profile_case:
+        profile_case(args)
+        return
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
     if args.partition_tokens is None:
