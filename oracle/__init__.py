@@ -278,3 +278,38 @@ def decode_fp8(q, k_cache, v_cache, k_scales, v_scales, block_tables, seq_lens, 
                                    float(scale), _ptr(out), _ptr(lse))
     _check(rc, "decode_fp8")
     return out, lse
+
+
+# ----------------------------------------------------------------- cascade
+
+def cascade_decode(q, k_cache, v_cache, block_tables, seq_lens, group_offsets, prefix_tables,
+                   shared_blocks, scale):
+    """Cascade decode in the steps of the pages' two-level attention
+    ("03 - Engines Papers", section 12): per sequence, attention over its
+    group's shared prefix (tokens [0, min(len, 16 * shared)) through the
+    group's prefix table), attention over its private suffix (tokens
+    [16 * shared, len) through its own table), and their log-sum-exp merge.
+    Returns (out [S, Hq, D], lse [S, Hq])."""
+    bt = np.asarray(block_tables, dtype=np.int32)
+    sl = np.asarray(seq_lens, dtype=np.int32)
+    go = np.asarray(group_offsets, dtype=np.int64)
+    pt = np.asarray(prefix_tables, dtype=np.int32).reshape(len(go) - 1, -1)
+    sb = np.asarray(shared_blocks, dtype=np.int64)
+    S, mb = bt.shape
+    pre_bt = np.full((S, max(pt.shape[1], 1)), -1, dtype=np.int32)
+    pre_len = np.zeros(S, dtype=np.int32)
+    suf_bt = np.full((S, mb), -1, dtype=np.int32)
+    suf_len = np.zeros(S, dtype=np.int32)
+    for g in range(len(go) - 1):
+        for s in range(go[g], go[g + 1]):
+            k = int(min(sb[s], -(-int(sl[s]) // 16)))
+            pre_bt[s, :pt.shape[1]] = pt[g]
+            pre_len[s] = min(int(sl[s]), 16 * int(sb[s]))
+            rest = bt[s, k:]
+            suf_bt[s, :len(rest)] = rest
+            suf_len[s] = int(sl[s]) - 16 * k if int(sl[s]) > 16 * k else 0
+    o_pre, l_pre = decode(q, k_cache, v_cache, pre_bt, pre_len, scale)
+    o_suf, l_suf = decode(q, k_cache, v_cache, suf_bt, suf_len, scale)
+    part_o = np.stack([o_pre, o_suf], axis=2)
+    part_lse = np.stack([l_pre, l_suf], axis=2)
+    return merge(part_o, part_lse, np.full(S, 2, dtype=np.int32))

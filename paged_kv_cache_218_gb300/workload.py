@@ -447,3 +447,45 @@ def unique_kv_bytes(block_tables, seq_lens, kv_heads: int, head_dim: int,
             blk = int(block_tables[s, j])
             best[blk] = max(best.get(blk, 0), min(block_size, n - j * block_size))
     return int(sum(best.values())) * kv_bytes_per_token(1, kv_heads, head_dim, elem_bytes)
+
+
+def cascade_groups(w: "Workload", group: int):
+    """Cascade metadata for a batch whose consecutive sequences form groups of
+    ``group`` sharing prefix blocks (the copy-on-write mix): the group's
+    prefix table is, at each block index, the physical block most members of
+    the group hold there (ties: the lowest id), as long as at least two
+    members agree (a lone member's block is not shared); a sequence's
+    shared-block count is the length of the leading run of its table that
+    equals the prefix table.  Returns (group_offsets int32 [G + 1],
+    prefix_tables int32 [G, P], shared_blocks int32 [S])."""
+    bt = w.decode_block_tables
+    lens = w.decode_seq_lens
+    S = bt.shape[0]
+    G = -(-S // group)
+    offsets = np.minimum(np.arange(G + 1) * group, S).astype(np.int32)
+    rows = []
+    for g in range(G):
+        members = range(offsets[g], offsets[g + 1])
+        pref = []
+        for j in range(bt.shape[1]):
+            ids = [int(bt[s, j]) for s in members if j < _blocks_for(int(lens[s]))]
+            if len(ids) < 2:
+                break
+            vals, counts = np.unique(ids, return_counts=True)
+            if counts.max() < 2:
+                break
+            pref.append(int(vals[np.argmax(counts)]))
+        rows.append(pref)
+    P = max(1, max(len(r) for r in rows))
+    prefix = np.full((G, P), -1, dtype=np.int32)
+    for g, r in enumerate(rows):
+        prefix[g, :len(r)] = r
+    shared = np.zeros(S, dtype=np.int32)
+    for g in range(G):
+        r = rows[g]
+        for s in range(offsets[g], offsets[g + 1]):
+            k = 0
+            while k < len(r) and k < _blocks_for(int(lens[s])) and bt[s, k] == r[k]:
+                k += 1
+            shared[s] = k
+    return offsets, prefix, shared
