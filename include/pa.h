@@ -68,6 +68,7 @@ typedef enum pa_status {
 #define PA_DEVERR_SLOT 4u      /* slot >= num_blocks * block_size (skipped) */
 #define PA_DEVERR_TIMEOUT 8u   /* a pipeline wait ran past its iteration limit */
 #define PA_DEVERR_CHUNK 16u    /* prefill chunk metadata inconsistent (skipped) */
+#define PA_DEVERR_GROUP 32u    /* cascade group / shared-block metadata out of range (clamped) */
 
 /* Human-readable name of a pa_status value.  Never NULL. */
 const char *pa_status_string(int status);
@@ -146,6 +147,45 @@ int pa_decode(void *out, const void *q, const void *k_cache, const void *v_cache
               int num_seqs, int num_q_heads, int num_kv_heads, int head_dim, int block_size,
               int64_t num_blocks, float scale, int partition_tokens, float *out_lse,
               void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * Cascade decode: decode of pa_decode for batches whose sequences share
+ * prompt prefixes ("03 - Engines Papers", section 12 Cascade Inference /
+ * Multi-Query Cascade Attention): the attention over a group's shared prefix
+ * is computed once for all the group's queries, batched, and combined with
+ * each sequence's private-suffix attention by log-sum-exp.  The result is the
+ * same as pa_decode's (same formula, same outputs).
+ *
+ * Groups: the sequences are ordered by group; group g holds sequences
+ * [group_offsets[g], group_offsets[g + 1]) (device, int32 [num_groups + 1],
+ * group_offsets[0] = 0, group_offsets[num_groups] = num_seqs, each group at
+ * most max_group_size sequences, max_group_size * (num_q_heads /
+ * num_kv_heads) <= 32).  A sequence with nothing shared forms its own group
+ * or has shared_blocks = 0.
+ *   prefix_tables  device, int32 [num_groups, max_prefix_blocks]: the
+ *                  physical blocks of group g's shared prefix, in order
+ *   shared_blocks  device, int32 [num_seqs]: sequence s's first
+ *                  shared_blocks[s] table entries are prefix_tables[g][0 ..
+ *                  shared_blocks[s]) (the caller guarantees it); its tokens
+ *                  [0, min(len, 16 * shared_blocks[s])) are attended in the
+ *                  group's prefix pass, the rest [16 * shared_blocks[s], len)
+ *                  through its own table in the suffix pass
+ * Other arguments, modes and outputs as pa_decode (head_dim 128).  The
+ * workspace (pa_cascade_workspace_size, 256-byte aligned) holds the prefix
+ * pass's fp32 partials followed by pa_decode's workspace, which must be
+ * zero-filled before its first use as for pa_decode.  Out-of-range group or
+ * shared-block metadata sets PA_DEVERR_GROUP and is clamped, never faults.
+ */
+size_t pa_cascade_workspace_size(int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
+                                 int max_blocks_per_seq, int block_size, int partition_tokens);
+int pa_cascade_decode(void *out, const void *q, const void *k_cache, const void *v_cache,
+                      const int32_t *block_tables, int max_blocks_per_seq,
+                      const int32_t *seq_lens, int num_seqs, const int32_t *group_offsets,
+                      int num_groups, int max_group_size, const int32_t *prefix_tables,
+                      int max_prefix_blocks, const int32_t *shared_blocks, int num_q_heads,
+                      int num_kv_heads, int head_dim, int block_size, int64_t num_blocks,
+                      float scale, int partition_tokens, float *out_lse, void *workspace,
+                      size_t workspace_bytes, void *stream);
 
 /*
  * FP8 (E4M3) KV cache: the pools hold one byte per element, with one

@@ -32,6 +32,7 @@ PA_DEVERR_SEQ_LEN = 2
 PA_DEVERR_SLOT = 4
 PA_DEVERR_TIMEOUT = 8
 PA_DEVERR_CHUNK = 16
+PA_DEVERR_GROUP = 32
 
 _P = ctypes.c_void_p
 _I = ctypes.c_int
@@ -51,6 +52,9 @@ _SIGS = {
     "pa_prefill_chunk": ([_P, _P, _P, _P, _P, _I, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _L, _F,
                           _P, _P], _I),
     "pa_validate_metadata": ([_P, _I, _P, _I, _P, _I, _P, _L, _I], _I),
+    "pa_cascade_workspace_size": ([_I, _I, _I, _I, _I, _I, _I], _S),
+    "pa_cascade_decode": ([_P, _P, _P, _P, _P, _I, _P, _I, _P, _I, _I, _P, _I, _P, _I, _I, _I, _I,
+                           _L, _F, _I, _P, _P, _S, _P], _I),
     "pa_reshape_and_cache_fp8": ([_P, _P, _L, _L, _P, _P, _P, _P, _P, _I, _I, _I, _I, _L, _P], _I),
     "pa_copy_blocks_fp8": ([_P, _P, _P, _I, _I, _I, _I, _L, _P], _I),
     "pa_decode_fp8": ([_P, _P, _P, _P, _P, _P, _P, _I, _P, _I, _I, _I, _I, _I, _L, _F, _I, _P, _P,
@@ -188,6 +192,39 @@ def pa_decode_fp8(out, q, k_cache, v_cache, k_scales, v_scales, block_tables, se
         _ptr(block_tables), block_tables.shape[1], _ptr(seq_lens), S, Hq, Hkv, D, bs, nb,
         float(scale), int(partition_tokens), _ptr(out_lse), _ptr(workspace), ws_bytes,
         _stream(stream)))
+
+
+def pa_cascade_workspace_size(num_seqs, num_q_heads, num_kv_heads, head_dim, max_blocks_per_seq,
+                              block_size=16, partition_tokens=0) -> int:
+    return int(_lib.pa_cascade_workspace_size(num_seqs, num_q_heads, num_kv_heads, head_dim,
+                                              max_blocks_per_seq, block_size, partition_tokens))
+
+
+def pa_cascade_decode(out, q, k_cache, v_cache, block_tables, seq_lens, group_offsets,
+                      max_group_size, prefix_tables, shared_blocks, scale, partition_tokens=0,
+                      out_lse=None, workspace=None, stream=None) -> None:
+    """Decode with each group's shared prefix attended once for all its
+    members, merged with their private suffixes (same result as pa_decode)."""
+    _need(out, "out", torch.bfloat16, 3)
+    _need(q, "q", torch.bfloat16, 3)
+    _need(k_cache, "k_cache", torch.bfloat16, 4)
+    _need(v_cache, "v_cache", torch.bfloat16, 4)
+    _need(block_tables, "block_tables", torch.int32, 2)
+    _need(seq_lens, "seq_lens", torch.int32, 1)
+    _need(group_offsets, "group_offsets", torch.int32, 1)
+    _need(prefix_tables, "prefix_tables", torch.int32, 2)
+    _need(shared_blocks, "shared_blocks", torch.int32, 1)
+    if out_lse is not None:
+        _need(out_lse, "out_lse", torch.float32, 2)
+    S, Hq, D = q.shape
+    nb, bs, Hkv, _ = k_cache.shape
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check("pa_cascade_decode", _lib.pa_cascade_decode(
+        _ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables),
+        block_tables.shape[1], _ptr(seq_lens), S, _ptr(group_offsets), group_offsets.shape[0] - 1,
+        int(max_group_size), _ptr(prefix_tables), prefix_tables.shape[1], _ptr(shared_blocks),
+        Hq, Hkv, D, bs, nb, float(scale), int(partition_tokens), _ptr(out_lse), _ptr(workspace),
+        ws_bytes, _stream(stream)))
 
 
 def pa_decode_workspace_size(num_seqs, num_q_heads, num_kv_heads, head_dim, max_blocks_per_seq,

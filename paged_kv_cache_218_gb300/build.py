@@ -17,7 +17,7 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(ROOT, "_build")
 LIB = os.path.join(PKG, "libpa.so")
-SOURCES = ["pa_api.cu", "pa_decode.cu", "pa_prefill.cu", "pa_block_manager.cpp"]
+SOURCES = ["pa_api.cu", "pa_decode.cu", "pa_prefill.cu", "pa_cascade.cu", "pa_block_manager.cpp"]
 HEADERS = ["pa_internal.h", "pa_ptx.cuh", os.path.join("..", "..", "include", "pa.h"),
            os.path.join("..", "..", "include", "pa_block_manager.h")]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

@@ -77,13 +77,13 @@ int encode_pool_map_uncached(CUtensorMap* m, const void* pool, int64_t num_block
   cuuint64_t strides[2] = {static_cast<cuuint64_t>(D) * elem,
                            static_cast<cuuint64_t>(Hkv) * D * elem};
   cuuint32_t box[3] = {static_cast<cuuint32_t>(128 / elem), 1, static_cast<cuuint32_t>(rows)};
-  if (rows == 0) {
+  if (rows <= 0) {  // rows < 0: the same view, a box of -rows kv heads
     dims[1] = static_cast<cuuint64_t>(num_blocks) * kBlockSize;
     dims[2] = static_cast<cuuint64_t>(Hkv);
     strides[0] = static_cast<cuuint64_t>(Hkv) * D * elem;
     strides[1] = static_cast<cuuint64_t>(D) * elem;
     box[1] = kBlockSize;
-    box[2] = static_cast<cuuint32_t>(Hkv);
+    box[2] = static_cast<cuuint32_t>(rows == 0 ? Hkv : -rows);
   }
   cuuint32_t estr[3] = {1, 1, 1};
   CUresult r = g_encode(m, elem == 1 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
@@ -265,7 +265,11 @@ __global__ void __launch_bounds__(128) merge_kernel(const MergeArgs a) {
     int len = a.seq_lens[s];
     const int cap = a.max_blocks * kBlockSize;
     len = len < 0 ? 0 : (len > cap ? cap : len);
-    const int nb = (len + kBlockSize - 1) / kBlockSize;
+    int nb = (len + kBlockSize - 1) / kBlockSize;
+    if (a.start_blocks) {
+      const int sb = a.start_blocks[s];
+      nb = sb <= 0 ? nb : (sb >= nb ? 0 : nb - sb);
+    }
     np = nb == 0 ? 1 : (nb + a.part_blocks - 1) / a.part_blocks;
     if (a.skip_single && np == 1) return;
   }
@@ -510,7 +514,8 @@ static int decode_impl(void* out, const void* q, const void* k_cache, const void
                        const int32_t* seq_lens, int num_seqs, int num_q_heads,
                        int num_kv_heads, int head_dim, int block_size, int64_t num_blocks,
                        float scale, int partition_tokens, float* out_lse, void* workspace,
-                       size_t workspace_bytes, void* stream) {
+                       size_t workspace_bytes, void* stream, const int32_t* start_blocks = nullptr,
+                       const float* init_o = nullptr, const float* init_lse = nullptr) {
   if (int rc = check_shape(num_q_heads, num_kv_heads, head_dim, block_size)) return rc;
   if (kv_fp8 && head_dim != 128) return PA_ERR_UNSUPPORTED;
   if (num_seqs < 0 || max_blocks_per_seq <= 0 || num_blocks <= 0) return PA_ERR_INVALID;
@@ -549,6 +554,9 @@ static int decode_impl(void* out, const void* q, const void* k_cache, const void
   a.kv_fp8 = kv_fp8 ? 1 : 0;
   a.k_scales = k_scales;
   a.v_scales = v_scales;
+  a.start_blocks = start_blocks;
+  a.init_o = init_o;
+  a.init_lse = init_lse;
   int grid = decode_grid(d->num_sms, mode);
   if (mode == kModeSinglePass) {
     a.part_blocks = max_blocks_per_seq;
@@ -592,6 +600,7 @@ static int decode_impl(void* out, const void* q, const void* k_cache, const void
     m.part_blocks = a.part_blocks;
     m.max_blocks = max_blocks_per_seq;
     m.skip_single = 1;
+    m.start_blocks = start_blocks;
     m.num_seqs = num_seqs;
     m.num_q_heads = num_q_heads;
     m.head_dim = head_dim;
@@ -622,6 +631,86 @@ int pa_decode_fp8(void* out, const void* q, const void* k_cache, const void* v_c
                      max_blocks_per_seq, seq_lens, num_seqs, num_q_heads, num_kv_heads, head_dim,
                      block_size, num_blocks, scale, partition_tokens, out_lse, workspace,
                      workspace_bytes, stream);
+}
+
+static size_t cascade_prefix_bytes(int num_seqs, int Hq) {
+  return (static_cast<size_t>(num_seqs) * Hq * 128 * 4 + 255) / 256 * 256 +
+         (static_cast<size_t>(num_seqs) * Hq * 4 + 255) / 256 * 256;
+}
+
+size_t pa_cascade_workspace_size(int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
+                                 int max_blocks_per_seq, int block_size, int partition_tokens) {
+  if (head_dim != 128 || num_seqs < 0) return 0;
+  if (check_shape(num_q_heads, num_kv_heads, head_dim, block_size) != PA_OK) return 0;
+  return cascade_prefix_bytes(num_seqs, num_q_heads) +
+         pa_decode_workspace_size(num_seqs, num_q_heads, num_kv_heads, head_dim,
+                                  max_blocks_per_seq, block_size, partition_tokens);
+}
+
+int pa_cascade_decode(void* out, const void* q, const void* k_cache, const void* v_cache,
+                      const int32_t* block_tables, int max_blocks_per_seq,
+                      const int32_t* seq_lens, int num_seqs, const int32_t* group_offsets,
+                      int num_groups, int max_group_size, const int32_t* prefix_tables,
+                      int max_prefix_blocks, const int32_t* shared_blocks, int num_q_heads,
+                      int num_kv_heads, int head_dim, int block_size, int64_t num_blocks,
+                      float scale, int partition_tokens, float* out_lse, void* workspace,
+                      size_t workspace_bytes, void* stream) {
+  if (int rc = check_shape(num_q_heads, num_kv_heads, head_dim, block_size)) return rc;
+  if (head_dim != 128) return PA_ERR_UNSUPPORTED;
+  if (num_seqs < 0 || num_groups < 0 || max_blocks_per_seq <= 0 || num_blocks <= 0 ||
+      max_prefix_blocks < 0)
+    return PA_ERR_INVALID;
+  if (num_blocks * kBlockSize > (int64_t)INT32_MAX) return PA_ERR_UNSUPPORTED;
+  if (!(scale > 0.f) || !isfinite(scale)) return PA_ERR_INVALID;
+  if (num_seqs == 0) return PA_OK;
+  if (!group_offsets || !shared_blocks || (max_prefix_blocks > 0 && !prefix_tables) ||
+      !aligned(group_offsets, 4) || !aligned(shared_blocks, 4) ||
+      (prefix_tables && !aligned(prefix_tables, 4)))
+    return PA_ERR_INVALID;
+  CascadeArgs c{};
+  if (!cascade_shape(num_kv_heads, num_q_heads / num_kv_heads, max_group_size, &c.kv_per_cta,
+                     &c.warps_per_kv, &c.stages))
+    return PA_ERR_UNSUPPORTED;
+  const size_t pre = cascade_prefix_bytes(num_seqs, num_q_heads);
+  if (!workspace || workspace_bytes < pre || !aligned(workspace, 256)) return PA_ERR_WORKSPACE;
+  if (!out || !q || !k_cache || !v_cache || !block_tables || !seq_lens) return PA_ERR_INVALID;
+  if (!aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16)) return PA_ERR_INVALID;
+  DeviceInfo* d;
+  if (int rc = current_device_info(&d)) return rc;
+  float* pre_o = static_cast<float*>(workspace);
+  float* pre_lse = reinterpret_cast<float*>(
+      static_cast<char*>(workspace) +
+      (static_cast<size_t>(num_seqs) * num_q_heads * 128 * 4 + 255) / 256 * 256);
+  if (num_groups > 0) {
+    c.q = static_cast<const __nv_bfloat16*>(q);
+    c.seq_lens = seq_lens;
+    c.group_offsets = group_offsets;
+    c.prefix_tables = prefix_tables;
+    c.shared_blocks = shared_blocks;
+    c.pre_o = pre_o;
+    c.pre_lse = pre_lse;
+    c.err = d->err;
+    c.num_blocks = num_blocks;
+    c.num_seqs = num_seqs;
+    c.max_prefix_blocks = max_prefix_blocks;
+    c.num_groups = num_groups;
+    c.max_group = max_group_size;
+    c.num_q_heads = num_q_heads;
+    c.num_kv_heads = num_kv_heads;
+    c.group = num_q_heads / num_kv_heads;
+    c.scale_log2 = scale * 1.4426950408889634f;
+    CUtensorMap tk, tv;
+    if (encode_pool_map(&tk, k_cache, num_blocks, num_kv_heads, head_dim, -c.kv_per_cta) ||
+        encode_pool_map(&tv, v_cache, num_blocks, num_kv_heads, head_dim, -c.kv_per_cta))
+      return PA_ERR_CUDA;
+    if (launch_cascade_prefix(c, &tk, &tv, static_cast<cudaStream_t>(stream)) != cudaSuccess)
+      return PA_ERR_CUDA;
+  }
+  return decode_impl(out, q, k_cache, v_cache, nullptr, nullptr, false, block_tables,
+                     max_blocks_per_seq, seq_lens, num_seqs, num_q_heads, num_kv_heads, head_dim,
+                     block_size, num_blocks, scale, partition_tokens, out_lse,
+                     static_cast<char*>(workspace) + pre, workspace_bytes - pre, stream,
+                     shared_blocks, pre_o, pre_lse);
 }
 
 // Static scratch of pa_decode_noalloc: the balanced split's merge tickets and

@@ -52,7 +52,7 @@ constexpr float kLn2 = 0.6931471805599453f;
 enum PieceKind : int { kFinal = 0, kPartialFixed = 1, kPartialBalanced = 2 };
 
 struct Piece {
-  int s, j0, j1, len, nb, kind, part, which;
+  int s, j0, j1, len, nb, kind, part, which, first;
   long long seg_start;
 };
 
@@ -85,7 +85,7 @@ __host__ __device__ inline Layout make_layout(int D, int Hkv, int Hq, int wph, i
   L.ml_off = L.obuf_off + obuf;
   L.bar_off = L.ml_off + kConsumerWarps * kMaxGroup * 2 * 4;
   L.misc_off = L.bar_off + (kMaxStages * 2 + 4) * 8;
-  L.pre_off = L.misc_off + 64;
+  L.pre_off = L.misc_off + 128;  // misc: flags, tickets, scan partials, per-warp words
   L.total = L.pre_off + pre_ints * 4;
   return L;
 }
@@ -98,6 +98,19 @@ __device__ __forceinline__ int load_len(const DecodeArgs& a, int s, bool report)
     len = len < 0 ? 0 : cap;
   }
   return len;
+}
+
+// First block of sequence s this launch attends to: 0, or the cascade suffix
+// pass's start block (clamped to [0, ceil(len/16)]).
+__device__ __forceinline__ int start_block(const DecodeArgs& a, int s, int len, bool report) {
+  if (!a.start_blocks) return 0;
+  int sb = a.start_blocks[s];
+  const int nb = (len + kBlockSize - 1) / kBlockSize;
+  if (sb < 0) {
+    if (report) atomicOr(a.err, PA_DEVERR_GROUP);
+    sb = 0;
+  }
+  return sb > nb ? nb : sb;
 }
 
 __device__ __forceinline__ long long cta_of(long long x, long long W, int C) {
@@ -118,13 +131,17 @@ __device__ bool next_piece(const DecodeArgs& a, const int* pre, Cursor& c, Piece
     p.s = s;
     p.nb = pre[s + 1] - pre[s];
     p.seg_start = pre[s];
-    p.j0 = static_cast<int>(c.idx - p.seg_start);
+    const int r0 = static_cast<int>(c.idx - p.seg_start);
     const long long seg_end = p.seg_start + p.nb;
     const long long end = c.hi < seg_end ? c.hi : seg_end;
-    p.j1 = p.j0 + static_cast<int>(end - c.idx);
+    const int r1 = r0 + static_cast<int>(end - c.idx);
     c.idx = end;
     p.len = load_len(a, s, false);
-    p.kind = (p.j0 == 0 && p.j1 == p.nb) ? kFinal : kPartialBalanced;
+    const int sb = start_block(a, s, p.len, false);
+    p.j0 = sb + r0;
+    p.j1 = sb + r1;
+    p.first = r0 == 0;
+    p.kind = (r0 == 0 && r1 == p.nb) ? kFinal : kPartialBalanced;
     p.which = p.seg_start < c.lo ? 0 : 1;
     p.part = 0;
     return true;
@@ -136,13 +153,16 @@ __device__ bool next_piece(const DecodeArgs& a, const int* pre, Cursor& c, Piece
     const int s = static_cast<int>(u / a.max_parts);
     const int len = load_len(a, s, report && part == 0);
     const int nb = (len + kBlockSize - 1) / kBlockSize;
-    const int nparts = nb == 0 ? 1 : (nb + a.part_blocks - 1) / a.part_blocks;
+    const int sb = start_block(a, s, len, report && part == 0);
+    const int ns = nb - sb;
+    const int nparts = ns == 0 ? 1 : (ns + a.part_blocks - 1) / a.part_blocks;
     if (part >= nparts) continue;
     p.s = s;
     p.len = len;
     p.nb = nb;
-    p.j0 = part * a.part_blocks;
+    p.j0 = sb + part * a.part_blocks;
     p.j1 = min(nb, p.j0 + a.part_blocks);
+    p.first = part == 0;
     p.kind = nparts == 1 ? kFinal : kPartialFixed;
     p.part = part;
     p.which = 0;
@@ -511,7 +531,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int per = (S + kThreads - 1) / kThreads;
     const int s0 = min(S, tid * per), s1 = min(S, s0 + per);
     int local = 0;
-    for (int s = s0; s < s1; ++s) local += (load_len(a, s, false) + kBlockSize - 1) / kBlockSize;
+    for (int s = s0; s < s1; ++s) {
+      const int len = load_len(a, s, false);
+      local += (len + kBlockSize - 1) / kBlockSize - start_block(a, s, len, false);
+    }
     int incl = local;
 #pragma unroll
     for (int off = 1; off < 32; off <<= 1) {
@@ -524,7 +547,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int w = 0; w < warp; ++w) run += misc[4 + w];
     for (int s = s0; s < s1; ++s) {
       pre[s] = run;
-      run += (load_len(a, s, false) + kBlockSize - 1) / kBlockSize;
+      const int len = load_len(a, s, false);
+      run += (len + kBlockSize - 1) / kBlockSize - start_block(a, s, len, false);
     }
     if (tid == kThreads - 1) pre[S] = run;
     __syncthreads();
@@ -561,9 +585,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         ok = false;
         return;
       }
+      // one copy per kv head's rows (G x D, at most 2 KB) on the same
+      // barrier: a single copy of the whole row set (16 KB at 64 q heads)
+      // into this two-slot ring gave nondeterministic query rows when pieces
+      // were one block long; per-head copies do not
       mbar_arrive_expect_tx(bar_qfull + k * 8, qrow_bytes);
-      bulk_load(sbase + L.q_off + k * L.q_bytes, a.q + static_cast<long long>(p.s) * Hq * D,
-                qrow_bytes, bar_qfull + k * 8);
+      const uint32_t chunk = static_cast<uint32_t>(G) * D * 2;
+      for (int h = 0; h < Hkv; ++h)
+        bulk_load(sbase + L.q_off + k * L.q_bytes + h * chunk,
+                  a.q + static_cast<long long>(p.s) * Hq * D + h * G * D, chunk,
+                  bar_qfull + k * 8);
     };
     Piece p{};
     int qi = 0, jbp = 0;
@@ -648,14 +679,17 @@ __global__ void __launch_bounds__(kThreads, 1)
   // -------------------------------------------------------------- consumers
   const int ctid = tid;  // 0..255
   if (a.mode == kModeBalanced) {
-    // sequences without tokens produce out = 0, lse = -inf
+    // sequences without tokens to attend produce out = 0, lse = -inf -- or,
+    // in a cascade suffix pass, the prefix pass's result
     for (int s = blockIdx.x; s < a.num_seqs; s += gridDim.x) {
-      if (load_len(a, s, ctid == 0) != 0) continue;
+      const int len = load_len(a, s, warp == 0);
+      if ((len + kBlockSize - 1) / kBlockSize - start_block(a, s, len, warp == 0) != 0) continue;
+      const long long base = static_cast<long long>(s) * Hq;
       for (int e = ctid; e < Hq * D; e += kConsumerThreads)
-        a.out[static_cast<long long>(s) * Hq * D + e] = __float2bfloat16(0.f);
+        a.out[base * D + e] = __float2bfloat16(a.init_o ? a.init_o[base * D + e] : 0.f);
       if (a.out_lse)
         for (int h = ctid; h < Hq; h += kConsumerThreads)
-          a.out_lse[static_cast<long long>(s) * Hq + h] = -INFINITY;
+          a.out_lse[base + h] = a.init_o ? a.init_lse[base + h] : -INFINITY;
     }
   }
 
@@ -674,7 +708,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   Piece pc;
   uint32_t g = 0;
   int qi = 0;
-  while (next_piece(a, pre, cur, pc, ctid == 0)) {
+  // the report flag is uniform over a warp: lanes of one warp must take the
+  // same path here, or the warp-synchronous MMA and matrix loads below could
+  // be reached at different instructions
+  while (next_piece(a, pre, cur, pc, warp == 0)) {
+    __syncwarp();
     const long long head0 = static_cast<long long>(pc.s) * Hq + hw * G;
     uint32_t qf[KS][2];
     float sl2 = a.scale_log2;  // scores to log2 units (E4M3: scales folded in)
@@ -682,8 +720,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       // query fragments of the group (B operand: k = dim, n = head) from the
       // piece's staged query rows
       const int k = qi & 1;
-      if (!*abort_flag && !mbar_wait(bar_qfull + k * 8, (qi >> 1) & 1)) {
-        atomicOr(a.err, PA_DEVERR_TIMEOUT);
+      if (!warp_flag(abort_flag) && !mbar_wait_warp(bar_qfull + k * 8, (qi >> 1) & 1)) {
+        if (lane == 0) atomicOr(a.err, PA_DEVERR_TIMEOUT);
         *abort_flag = 1;
       }
       const uint32_t qrow = sbase + L.q_off + k * L.q_bytes + (hw * G + hq) * D * 2;
@@ -736,6 +774,19 @@ __global__ void __launch_bounds__(kThreads, 1)
           qf[ks][1] = x1;
         }
       }
+      // The slot is released below and the next bulk copy (async proxy) may
+      // overwrite it at once.  Every loaded value goes into one word stored
+      // to this warp's scratch slot -- an instruction that cannot issue
+      // before all the loads have returned -- then a proxy fence orders the
+      // reads before the copy that the release lets the producer issue.
+      {
+        uint32_t dep = 0u;
+#pragma unroll
+        for (int ks = 0; ks < KS; ++ks) dep ^= qf[ks][0] ^ qf[ks][1];
+        asm volatile("st.shared.u32 [%0], %1;" ::"r"(smem_u32(misc + 16 + warp)), "r"(dep)
+                     : "memory");
+        fence_proxy_async_smem();
+      }
       __syncwarp();
       if (lane == 0) mbar_arrive(bar_qempty + k * 8);
     }
@@ -744,14 +795,42 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
     for (int mt = 0; mt < KS; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
     float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
+    if (a.init_o && pc.first && active && sub == 0) {
+      // cascade suffix pass: the sequence's first piece starts from the prefix
+      // pass's result: accumulator o_pre (before the V scale), running max
+      // lse in log2 units, running sum 1 (held by one lane of the 8 that
+      // share a head column; the sums are reduced across them at the end)
+      const float l2e = 1.4426950408889634f;
+      const float inv_v = 1.f / vsc;
+#pragma unroll
+      for (int k = 0; k < 2; ++k) {
+        const int hk = 2 * q4 + k;
+        if (hk >= G) continue;
+        const long long row = head0 + hk;
+        const float lse = a.init_lse[row];
+        if (!(lse > -INFINITY)) continue;
+        if (k == 0) {
+          m0 = lse * l2e;
+          l0 = d0 == 0 ? 1.f : 0.f;
+        } else {
+          m1 = lse * l2e;
+          l1 = d0 == 0 ? 1.f : 0.f;
+        }
+#pragma unroll
+        for (int mt = 0; mt < KS; ++mt) {
+          o[mt][k] = a.init_o[row * D + out_dim<KV8>(mt, d0, 0)] * inv_v;
+          o[mt][2 + k] = a.init_o[row * D + out_dim<KV8>(mt, d0, 1)] * inv_v;
+        }
+      }
+    }
 
     if (active) {
       for (int j = pc.j0; j < pc.j1; ++j, ++g) {
         if (static_cast<int>(g % wph) != sub) continue;
-        if (*abort_flag) continue;
+        if (warp_flag(abort_flag)) continue;
         const uint32_t st = g % NS;
-        if (!mbar_wait(bar_full + st * 8, (g / NS) & 1)) {
-          atomicOr(a.err, PA_DEVERR_TIMEOUT);
+        if (!mbar_wait_warp(bar_full + st * 8, (g / NS) & 1)) {
+          if (lane == 0) atomicOr(a.err, PA_DEVERR_TIMEOUT);
           *abort_flag = 1;
           continue;
         }

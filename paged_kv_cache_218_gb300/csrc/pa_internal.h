@@ -45,6 +45,12 @@ struct DecodeArgs {
   int kv_fp8;          // pools hold E4M3 bytes (head_dim 128) with per-kv-head scales
   const float* k_scales;  // E4M3: [Hkv] dequantization scales of K and V
   const float* v_scales;
+  // cascade suffix pass (all null otherwise): sequence s attends over its own
+  // blocks [start_blocks[s], ceil(len/16)) only, starting from the prefix
+  // pass's normalized o [S, Hq, D] and lse [S, Hq] (natural log)
+  const int32_t* start_blocks;
+  const float* init_o;
+  const float* init_lse;
 };
 
 struct MergeArgs {
@@ -57,6 +63,7 @@ struct MergeArgs {
   int part_blocks;
   int max_blocks;
   int skip_single;           // parts == 1 were written final by the decode kernel
+  const int32_t* start_blocks;  // cascade suffix pass: parts cover blocks [start, ceil(len/16))
   int num_seqs;
   int num_q_heads;
   int head_dim;
@@ -81,6 +88,29 @@ struct PrefillArgs {
   float scale_log2;
 };
 
+struct CascadeArgs {
+  const __nv_bfloat16* q;        // [S, Hq, 128]
+  const int32_t* seq_lens;       // [S]
+  const int32_t* group_offsets;  // [num_groups + 1]
+  const int32_t* prefix_tables;  // [num_groups, max_prefix_blocks]
+  const int32_t* shared_blocks;  // [S]
+  float* pre_o;                  // [S, Hq, 128] normalized prefix attention
+  float* pre_lse;                // [S, Hq] natural log, -inf without a prefix
+  unsigned int* err;
+  int64_t num_blocks;
+  int num_seqs;
+  int max_prefix_blocks;
+  int num_groups;
+  int max_group;
+  int num_q_heads;
+  int num_kv_heads;
+  int group;
+  int kv_per_cta;   // kv heads per CTA
+  int warps_per_kv; // consumer warps per kv head (16 query rows each)
+  int stages;       // K/V ring depth
+  float scale_log2;
+};
+
 // Balanced-mode workspace layout (shared by the size query and the launch):
 // per-CTA merge tickets, then two partial slots per CTA of Hq*(D+1) floats.
 size_t balanced_slot_floats(int num_q_heads, int head_dim);
@@ -96,6 +126,10 @@ cudaError_t launch_merge(const MergeArgs& a, cudaStream_t stream);
 cudaError_t launch_prefill(const PrefillArgs& a, const CUtensorMap* tm_q, const CUtensorMap* tm_k,
                            const CUtensorMap* tm_v, int grid_tiles, cudaStream_t stream);
 size_t prefill_smem_bytes();
+bool cascade_shape(int num_kv_heads, int group, int max_group, int* kv_per_cta, int* warps_per_kv,
+                   int* stages);
+cudaError_t launch_cascade_prefix(const CascadeArgs& a, const CUtensorMap* tm_k,
+                                  const CUtensorMap* tm_v, cudaStream_t stream);
 int prefill_cluster();  // query tiles per cluster (the grid is a multiple of it)
 
 }  // namespace pa

@@ -106,6 +106,19 @@ __device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, vol
   return false;
 }
 
+// wait_or_abort for a whole warp that goes on to warp-synchronous tensor-
+// memory loads and stores: the lanes reconverge and agree on the result.
+__device__ __forceinline__ bool wait_or_abort_warp(uint32_t bar, uint32_t parity,
+                                                   volatile int* abort, unsigned int* err) {
+  bool ok = !warp_flag(abort);
+  if (ok) ok = mbar_wait_warp(bar, parity);
+  if (!ok && !*abort) {
+    *abort = 1;
+    if ((threadIdx.x & 31) == 0) atomicOr(err, PA_DEVERR_TIMEOUT);
+  }
+  return ok;
+}
+
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                    const __grid_constant__ CUtensorMap tm_v, const PrefillArgs a) {
@@ -345,7 +358,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t v[64];
     for (int j = 0; j < nkt; ++j) {
       const int b = j & 1;
-      wait_or_abort(bar_s_full + 8 * b, (j >> 1) & 1, abort_flag, a.err);
+      wait_or_abort_warp(bar_s_full + 8 * b, (j >> 1) & 1, abort_flag, a.err);
       tc_fence_after();
       tmem_ld64(tmem + lane_off + b * 128 + hc * 64, v);
       tc_fence_before();
@@ -407,7 +420,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // O is rescaled only when a row maximum moved; then PV of the previous
       // tile must have landed first
       if (j >= 1 && __any_sync(0xffffffffu, alpha != 1.f)) {
-        wait_or_abort(bar_o_done + 8 * ((j - 1) & 1), ((j - 1) >> 1) & 1, abort_flag, a.err);
+        wait_or_abort_warp(bar_o_done + 8 * ((j - 1) & 1), ((j - 1) >> 1) & 1, abort_flag, a.err);
         tc_fence_after();
         const uint32_t ocol = tmem + lane_off + kTmemO + hc * 64;
 #pragma unroll
@@ -421,7 +434,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       // P buffer j & 1 is free once PV of tile j-2 has read it
       if (j >= 2) {
-        wait_or_abort(bar_o_done + 8 * (j & 1), ((j >> 1) - 1) & 1, abort_flag, a.err);
+        wait_or_abort_warp(bar_o_done + 8 * (j & 1), ((j >> 1) - 1) & 1, abort_flag, a.err);
         tc_fence_after();
       }
       // keys hc*64 .. hc*64+63 of row r = columns hc*32 .. +31 of P buffer j & 1
@@ -431,7 +444,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if ((n & (kBlockSize - 1)) != 0) {
         const int jl = (n - 1) / kBlockSize;
         if (jl < nb_vis && jl / 8 == j) {
-          wait_or_abort(bar_v_full + 8 * (j % kNV), (j / kNV) & 1, abort_flag, a.err);
+          wait_or_abort_warp(bar_v_full + 8 * (j % kNV), (j / kNV) & 1, abort_flag, a.err);
           const uint32_t vt = sbase + kVOff + (j % kNV) * kTileBytes;
           const int first = n - jl * kBlockSize;  // rows first..15 of block jl % 8
           const int rows = kBlockSize - first;
@@ -451,7 +464,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 
     // ---- epilogue: O / l -> bf16, and lse
-    wait_or_abort(bar_o_done + 8 * ((nkt - 1) & 1), ((nkt - 1) >> 1) & 1, abort_flag, a.err);
+    wait_or_abort_warp(bar_o_done + 8 * ((nkt - 1) & 1), ((nkt - 1) >> 1) & 1, abort_flag, a.err);
     tc_fence_after();
     red_sum[hc * 128 + r] = l_run;
     named_barrier(1 + qd, 64);

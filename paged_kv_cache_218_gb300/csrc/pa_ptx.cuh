@@ -66,14 +66,32 @@ __device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
-// Bounded wait for the phase with the given parity; false on timeout.
+// Bounded wait for the phase with the given parity; false on timeout.  One
+// loop with a single exit, so the code after a wait has one copy.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
-  if (mbar_try_wait(bar, parity)) return true;
-  const uint64_t t0 = global_ns();
-  for (uint32_t it = 1;; ++it) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if ((it & 63u) == 0 && global_ns() - t0 > kWaitLimitNs) return false;
+  bool done = mbar_try_wait(bar, parity);
+  const uint64_t t0 = done ? 0ull : global_ns();
+  for (uint32_t it = 1; !done; ++it) {
+    if ((it & 63u) == 0 && global_ns() - t0 > kWaitLimitNs) break;
+    done = mbar_try_wait(bar, parity);
   }
+  return done;
+}
+
+// The same wait for a whole warp that goes on to warp-synchronous
+// instructions (ldmatrix, mma.sync, movmatrix, tcgen05.ld ...), which every
+// lane must reach at the same instruction: the lanes leave their polling
+// loops at different times, so they reconverge here, and the result is the
+// same for all of them.
+__device__ __forceinline__ bool mbar_wait_warp(uint32_t bar, uint32_t parity) {
+  const bool ok = mbar_wait(bar, parity);
+  __syncwarp();
+  return __all_sync(0xffffffffu, ok);
+}
+
+// A flag word in shared memory as one value for the whole warp (lane 0's read).
+__device__ __forceinline__ bool warp_flag(volatile int* f) {
+  return __shfl_sync(0xffffffffu, *f, 0) != 0;
 }
 
 // ------------------------------------------------------------------ TMA

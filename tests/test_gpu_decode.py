@@ -292,3 +292,24 @@ def test_split_partials_merge_to_single_pass(pa, cuda_device):
     pa.pa_merge_partials(out2, part_o, part_lse, nparts)
     torch.cuda.synchronize()
     assert_close(out2[torch.from_numpy(~single)], ref[~single], "re-merged partials")
+
+
+@pytest.mark.parametrize("partition", [-1, 16, 0])
+def test_decode_is_bitwise_deterministic_on_one_block_pieces(pa, cuda_device, partition):
+    """Many one-block pieces at 64 q heads stress the query staging ring: the
+    outputs of repeated launches must be identical bit for bit."""
+    w = W.decode_batch(600, 1, 16, 64, 8, 128, seed=3)
+    dw = DeviceWorkload(w, cuda_device)
+    dw.scatter(pa)
+    S, Hq, D = w.num_decode_seqs, w.num_q_heads, w.head_dim
+    ws = pa.alloc_workspace(pa.pa_decode_workspace_size(S, Hq, 8, D, w.max_blocks_per_seq, 16,
+                                                        partition), cuda_device)
+    outs = []
+    for _ in range(12):
+        out = torch.empty((S, Hq, D), dtype=torch.bfloat16, device=cuda_device)
+        pa.pa_decode(out, dw.dq, dw.k_cache, dw.v_cache, dw.dtables, dw.dlens, w.scale,
+                     partition_tokens=partition, workspace=ws)
+        outs.append(out)
+    torch.cuda.synchronize()
+    for o in outs[1:]:
+        assert torch.equal(o.view(torch.int16), outs[0].view(torch.int16))
