@@ -367,9 +367,11 @@ def run_gpu(args, rank, world, local_rank):
     e2e = run_e2e(args, w, reps, ws, dev, pa, dist)
     fp8 = measure_fp8_decode(args, w, reps, ws, dev, pa) if (use_graphs and w.head_dim == 128) \
         else None
+    casc = measure_cascade(args, w, reps, dev, pa) if (use_graphs and args.config == "cow_prefix_mix") \
+        else None
     return dict(w=w, elapsed_ms=elapsed_ms, kv_all=kv_all, dec_ms=dec_ms, chunk_ms=chunk_ms,
                 clocks=clocks, e2e=e2e, launches=launches_per_step * K, graphs=use_graphs,
-                fp8=fp8)
+                fp8=fp8, cascade=casc)
 
 
 def measure_fp8_decode(args, w, reps, ws, dev, pa):
@@ -425,6 +427,54 @@ def measure_fp8_decode(args, w, reps, ws, dev, pa):
             "kv_bytes_per_token": 2 * Hkv * D, "tokens_per_s": S / (ms * 1e-3),
             "achieved_gbs": alg / (ms * 1e-3) / 1e9,
             "scales": "per kv head, max |x| / 448"}
+
+
+def measure_cascade(args, w, reps, dev, pa, group=4):
+    """Cascade decode of the copy-on-write mix (each group's shared prefix
+    attended once for its members, then each suffix): two launches per call,
+    timed like the plain decode over back-to-back calls from graphs of R."""
+    import torch
+
+    from paged_kv_cache_218_gb300 import workload as W
+    R = len(reps)
+    P = args.partition_tokens
+    go, pt, sb = W.cascade_groups(w, group)
+    S, Hq, D = w.num_decode_seqs, w.num_q_heads, w.head_dim
+    meta = [torch.from_numpy(x).to(dev) for x in (go, pt, sb)]
+    wss = [pa.alloc_workspace(pa.pa_cascade_workspace_size(S, Hq, w.num_kv_heads, D,
+                                                           w.max_blocks_per_seq, 16, P), dev)
+           for _ in range(R)]
+
+    def call(i):
+        out, q, kc, vc, bt, sl = decode_args(w, reps[i])
+        pa.pa_cascade_decode(out, q, kc, vc, bt, sl, meta[0], group, meta[1], meta[2], w.scale,
+                             partition_tokens=P, workspace=wss[i])
+
+    for i in range(max(3, args.warmup // 4)):
+        call(i % R)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        for i in range(R):
+            call(i)
+    g.replay()
+    torch.cuda.synchronize()
+    n = max(1, min(args.steps, args.kernel_steps) // R)
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(n):
+        g.replay()
+    b.record()
+    torch.cuda.synchronize()
+    ms = a.elapsed_time(b) / (n * R)
+    if pa.pa_device_error_flags() != 0:
+        raise RuntimeError("device error flags set by the cascade decode")
+    logical = kv_bytes_decode(w)
+    unique = W.unique_kv_bytes(w.decode_block_tables, w.decode_seq_lens, w.num_kv_heads, D)
+    return {"launch_ms": ms, "launches_per_call": 2, "groups": int(len(go) - 1),
+            "group_size": group, "shared_prefix_blocks": int(pt.shape[1]),
+            "logical_kv_bytes": logical, "unique_kv_bytes": unique,
+            "unique_gbs": unique / (ms * 1e-3) / 1e9, "logical_gbs": logical / (ms * 1e-3) / 1e9,
+            "tokens_per_s": S / (ms * 1e-3)}
 
 
 def run_e2e(args, w, reps, ws, dev, pa, dist):
@@ -607,7 +657,8 @@ def profile_case(args):
     from paged_kv_cache_218_gb300 import workload as W
     dev = torch.device("cuda", 0)
     torch.cuda.set_device(dev)
-    w = W.sarathi_hybrid() if args.profile_case == "prefill" else W.llama3_8b_layer()
+    w = {"prefill": W.sarathi_hybrid, "cascade": W.cow_mix}.get(args.profile_case,
+                                                                 W.llama3_8b_layer)()
     r = Replica(w, dev)
     pa.pa_reshape_and_cache(r.key, r.value, r.k_cache, r.v_cache, r.slot_mapping)
     S, Hq, D = w.num_decode_seqs, w.num_q_heads, w.head_dim
@@ -618,6 +669,15 @@ def profile_case(args):
             pa.pa_prefill_chunk(r.out_chunk, r.q[:T], r.k_cache, r.v_cache,
                                 r.block_tables[:w.num_chunks], r.cu, r.qs,
                                 r.seq_lens[:w.num_chunks], max_q, w.scale)
+    elif args.profile_case == "cascade":
+        go, pt, sb = W.cascade_groups(w, 4)
+        meta = [torch.from_numpy(x).to(dev) for x in (go, pt, sb)]
+        ws = pa.alloc_workspace(pa.pa_cascade_workspace_size(S, Hq, w.num_kv_heads, D,
+                                                             w.max_blocks_per_seq, 16, 0), dev)
+        out, q, kc, vc, bt, sl = decode_args(w, r)
+        for _ in range(3):
+            pa.pa_cascade_decode(out, q, kc, vc, bt, sl, meta[0], 4, meta[1], meta[2], w.scale,
+                                 partition_tokens=0, workspace=ws)
     else:
         ws = pa.alloc_workspace(pa.pa_decode_workspace_size(S, Hq, w.num_kv_heads, D,
                                                             w.max_blocks_per_seq, 16, 0), dev)
@@ -661,7 +721,8 @@ def main():
                     help="decode-only launches timed for the roofline's kernel duration")
     ap.add_argument("--no-graphs", action="store_true",
                     help="launch every kernel from Python instead of replaying CUDA graphs")
-    ap.add_argument("--profile-case", default=None, choices=["decode", "decode_fp8", "prefill"],
+    ap.add_argument("--profile-case", default=None,
+                    choices=["decode", "decode_fp8", "prefill", "cascade"],
                     help="run three launches of one kernel on a small case (for ncu) and exit")
     args = ap.parse_args()
     if args.profile_case:
@@ -732,6 +793,13 @@ def main():
         "gpu_launches": res["launches"],
         "clocks": res["clocks"],
     }
+    if res.get("cascade") is not None:
+        c = res["cascade"]
+        plain_ms = res["dec_ms"]
+        line["cascade"] = dict(c, peak=hbm, frac_unique=c["unique_gbs"] / hbm,
+                               plain_decode_ms=plain_ms,
+                               plain_unique_gbs=c["unique_kv_bytes"] / (plain_ms * 1e-3) / 1e9,
+                               speedup_vs_plain=plain_ms / c["launch_ms"])
     if res.get("fp8") is not None:
         f = res["fp8"]
         line["fp8_kv"] = dict(f, peak=hbm, frac=f["achieved_gbs"] / hbm,
