@@ -48,6 +48,11 @@ constexpr int kThreads = kConsumerThreads + 32;
 constexpr int kBoxBytes = 16 * 128;  // one TMA box: 16 token rows x 64 bf16
 constexpr int kMaxStages = 16;
 constexpr float kLn2 = 0.6931471805599453f;
+constexpr int kLenCache = 512;  // balanced mode keeps the lengths in shared memory up to this batch
+
+// Shared-memory ints of the balanced mode's per-sequence data: the exclusive
+// prefix of block counts (S + 1) and, for small batches, the lengths (S).
+__host__ __device__ inline int balanced_pre_ints(int S) { return S + 1 + (S <= kLenCache ? S : 0); }
 
 enum PieceKind : int { kFinal = 0, kPartialFixed = 1, kPartialBalanced = 2 };
 
@@ -118,8 +123,8 @@ __device__ __forceinline__ long long cta_of(long long x, long long W, int C) {
   return ((x + 1) * C + W - 1) / W - 1;
 }
 
-__device__ bool next_piece(const DecodeArgs& a, const int* pre, Cursor& c, Piece& p,
-                           bool report) {
+__device__ bool next_piece(const DecodeArgs& a, const int* pre, const int* lens_c, Cursor& c,
+                           Piece& p, bool report) {
   if (a.mode == kModeBalanced) {
     if (c.idx >= c.hi) return false;
     int lo = 0, hi = a.num_seqs - 1;  // largest s with pre[s] <= idx
@@ -136,7 +141,7 @@ __device__ bool next_piece(const DecodeArgs& a, const int* pre, Cursor& c, Piece
     const long long end = c.hi < seg_end ? c.hi : seg_end;
     const int r1 = r0 + static_cast<int>(end - c.idx);
     c.idx = end;
-    p.len = load_len(a, s, false);
+    p.len = lens_c ? lens_c[s] : load_len(a, s, false);
     const int sb = start_block(a, s, p.len, false);
     p.j0 = sb + r0;
     p.j1 = sb + r1;
@@ -502,6 +507,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     misc[0] = 0;  // abort flag
     fence_mbar_init();
   }
+  __syncthreads();  // barriers initialized before any warp uses them
   // Launched as a programmatic dependent of the previous kernel on the stream,
   // the CTA may get here while that kernel still runs.  Until griddep_wait()
   // returns it reads no global memory; it only asks L2 for the lines of this
@@ -525,33 +531,41 @@ __global__ void __launch_bounds__(kThreads, 1)
   griddep_launch_dependents();
 
   Cursor cur{};
+  const int* lens_c = nullptr;
   if (a.mode == kModeBalanced) {
-    // exclusive prefix of block counts over sequences (every thread of the CTA)
+    // exclusive prefix of block counts over sequences, computed by the
+    // producer warp alone (it needs it first); the consumers wait on a named
+    // barrier that the producer passes without waiting
     const int S = a.num_seqs;
-    const int per = (S + kThreads - 1) / kThreads;
-    const int s0 = min(S, tid * per), s1 = min(S, s0 + per);
-    int local = 0;
-    for (int s = s0; s < s1; ++s) {
-      const int len = load_len(a, s, false);
-      local += (len + kBlockSize - 1) / kBlockSize - start_block(a, s, len, false);
-    }
-    int incl = local;
+    int* lens_w = S <= kLenCache ? pre + S + 1 : nullptr;
+    lens_c = lens_w;
+    if (warp == kConsumerWarps) {
+      const int per = (S + 31) / 32;
+      const int s0 = min(S, lane * per), s1 = min(S, s0 + per);
+      int local = 0;
+      for (int s = s0; s < s1; ++s) {
+        const int len = load_len(a, s, true);
+        if (lens_w) lens_w[s] = len;
+        local += (len + kBlockSize - 1) / kBlockSize - start_block(a, s, len, true);
+      }
+      int incl = local;
 #pragma unroll
-    for (int off = 1; off < 32; off <<= 1) {
-      const int v = __shfl_up_sync(0xffffffffu, incl, off);
-      if (lane >= off) incl += v;
+      for (int off = 1; off < 32; off <<= 1) {
+        const int v = __shfl_up_sync(0xffffffffu, incl, off);
+        if (lane >= off) incl += v;
+      }
+      int run = incl - local;
+      for (int s = s0; s < s1; ++s) {
+        pre[s] = run;
+        const int len = lens_w ? lens_w[s] : load_len(a, s, false);
+        run += (len + kBlockSize - 1) / kBlockSize - start_block(a, s, len, false);
+      }
+      if (lane == 31) pre[S] = incl;
+      __syncwarp();
+      asm volatile("bar.arrive 2, %0;" ::"n"(kThreads) : "memory");
+    } else {
+      asm volatile("bar.sync 2, %0;" ::"n"(kThreads) : "memory");
     }
-    if (lane == 31) misc[4 + warp] = incl;
-    __syncthreads();
-    int run = incl - local;
-    for (int w = 0; w < warp; ++w) run += misc[4 + w];
-    for (int s = s0; s < s1; ++s) {
-      pre[s] = run;
-      const int len = load_len(a, s, false);
-      run += (len + kBlockSize - 1) / kBlockSize - start_block(a, s, len, false);
-    }
-    if (tid == kThreads - 1) pre[S] = run;
-    __syncthreads();
     cur.W = pre[S];
     cur.C = static_cast<int>(cur.W < gridDim.x ? cur.W : gridDim.x);
     if (static_cast<int>(blockIdx.x) < cur.C) {
@@ -564,7 +578,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else {
     cur.u = blockIdx.x;
     cur.U = static_cast<long long>(a.num_seqs) * a.max_parts;
-    __syncthreads();
   }
 
   if (warp == kConsumerWarps) {
@@ -598,7 +611,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     };
     Piece p{};
     int qi = 0, jbp = 0;
-    bool have_p = next_piece(a, pre, cur, p, false);
+    bool have_p = next_piece(a, pre, lens_c, cur, p, false);
     if (have_p) {
       stage_q(p, qi++);
       jbp = p.j0;
@@ -613,7 +626,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           jbp += n;
           return true;
         }
-        have_p = next_piece(a, pre, cur, p, false);
+        have_p = next_piece(a, pre, lens_c, cur, p, false);
         if (!have_p) return false;
         stage_q(p, qi++);
         jbp = p.j0;
@@ -626,10 +639,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t g = 0;
     ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
     while (have && ok) {
-      int s2, jb2, n2;
-      const bool have2 = next_chunk2(s2, jb2, n2);
-      const int ids2 = have2 ? load_ids(a, s2, jb2, n2, lane) : 0;
-      ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+      // the next chunk (its table row, and the queries of a new piece) is
+      // prepared once the current chunk's first ring's worth of blocks is
+      // issued, so the first loads of a launch go out without waiting on it
+      int s2 = 0, jb2 = 0, n2 = 0, ids2 = 0;
+      bool have2 = false, got2 = false;
       for (int i = 0; i < n && ok; ++i, ++g) {
         const int blk = __shfl_sync(0xffffffffu, ids, i);
         const uint32_t st = g % NS;
@@ -660,7 +674,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           }
         }
+        if (!got2 && (i + 1 == n || i + 1 == NS)) {
+          have2 = next_chunk2(s2, jb2, n2);
+          ids2 = have2 ? load_ids(a, s2, jb2, n2, lane) : 0;
+          got2 = true;
+          ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+        }
       }
+      if (!got2) break;  // stopped early (a failed wait): nothing more is issued
       s = s2;
       jb = jb2;
       n = n2;
@@ -669,7 +690,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     // queries of pieces without blocks (empty sequences) still get staged
     while (ok && have_p) {
-      have_p = next_piece(a, pre, cur, p, false);
+      have_p = next_piece(a, pre, lens_c, cur, p, false);
       if (have_p) stage_q(p, qi++);
     }
     if (!ok) *reinterpret_cast<volatile int*>(misc) = 1;
@@ -711,7 +732,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   // the report flag is uniform over a warp: lanes of one warp must take the
   // same path here, or the warp-synchronous MMA and matrix loads below could
   // be reached at different instructions
-  while (next_piece(a, pre, cur, pc, warp == 0)) {
+  while (next_piece(a, pre, lens_c, cur, pc, warp == 0)) {
     __syncwarp();
     const long long head0 = static_cast<long long>(pc.s) * Hq + hw * G;
     uint32_t qf[KS][2];
@@ -1066,7 +1087,7 @@ bool decode_supported(int head_dim, int num_kv_heads, int num_q_heads, int mode,
                       bool kv_fp8) {
   if (num_kv_heads > kConsumerWarps) return false;
   if (kv_fp8 && head_dim != 128) return false;
-  const int pre = mode == kModeBalanced ? num_seqs + 1 : 0;
+  const int pre = mode == kModeBalanced ? balanced_pre_ints(num_seqs) : 0;
   const int wph = warps_per_head(num_kv_heads);
   return make_layout(head_dim, num_kv_heads, num_q_heads, wph, 2, pre, kv_fp8 ? 1 : 2).total <=
          227 * 1024 - 1024;
@@ -1074,7 +1095,7 @@ bool decode_supported(int head_dim, int num_kv_heads, int num_q_heads, int mode,
 
 cudaError_t launch_decode(DecodeArgs a, const CUtensorMap* tm_k, const CUtensorMap* tm_v,
                           int head_dim, int grid, cudaStream_t stream) {
-  const int pre = a.mode == kModeBalanced ? a.num_seqs + 1 : 0;
+  const int pre = a.mode == kModeBalanced ? balanced_pre_ints(a.num_seqs) : 0;
   const int elem = a.kv_fp8 ? 1 : 2;
   a.warps_per_head = warps_per_head(a.num_kv_heads);
   a.stages = pick_stages(head_dim, a.num_kv_heads, a.num_q_heads, pre, elem);
