@@ -64,8 +64,10 @@ struct Piece {
 struct Cursor {
   long long u, U;         // fixed / single-pass unit walk
   long long idx, lo, hi;  // balanced block range [lo, hi)
+  long long mid, end;     // balanced: walk [mid, hi) first, then [lo, mid)
   long long W;            // balanced: total blocks
   int C;                  // balanced: CTAs that own a non-empty range
+  int phase;              // balanced: 0 while walking [mid, hi)
 };
 
 // Shared-memory carve-up (byte offsets from a 1024-aligned base).
@@ -123,22 +125,33 @@ __device__ __forceinline__ long long cta_of(long long x, long long W, int C) {
   return ((x + 1) * C + W - 1) / W - 1;
 }
 
+// the sequence holding global block x: the largest s with pre[s] <= x
+__device__ __forceinline__ int seq_of(const int* pre, int S, long long x) {
+  int lo = 0, hi = S - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (pre[mid] <= x) lo = mid; else hi = mid - 1;
+  }
+  return lo;
+}
+
 __device__ bool next_piece(const DecodeArgs& a, const int* pre, const int* lens_c, Cursor& c,
                            Piece& p, bool report) {
   if (a.mode == kModeBalanced) {
-    if (c.idx >= c.hi) return false;
-    int lo = 0, hi = a.num_seqs - 1;  // largest s with pre[s] <= idx
-    while (lo < hi) {
-      const int mid = (lo + hi + 1) >> 1;
-      if (pre[mid] <= c.idx) lo = mid; else hi = mid - 1;
+    if (c.idx >= c.end) {
+      if (c.phase != 0) return false;
+      c.phase = 1;
+      c.idx = c.lo;
+      c.end = c.mid;
+      if (c.idx >= c.end) return false;
     }
-    const int s = lo;
+    const int s = seq_of(pre, a.num_seqs, c.idx);
     p.s = s;
     p.nb = pre[s + 1] - pre[s];
     p.seg_start = pre[s];
     const int r0 = static_cast<int>(c.idx - p.seg_start);
     const long long seg_end = p.seg_start + p.nb;
-    const long long end = c.hi < seg_end ? c.hi : seg_end;
+    const long long end = c.end < seg_end ? c.end : seg_end;
     const int r1 = r0 + static_cast<int>(end - c.idx);
     c.idx = end;
     p.len = lens_c ? lens_c[s] : load_len(a, s, false);
@@ -390,10 +403,11 @@ __device__ __forceinline__ int out_dim(int mt, int g, int half) {
 // groups of the output and keeps, per group, the running maximum M, the sum
 // S = sum_k exp(lse_k - M) and the weighted sum of the pieces' outputs.  The
 // pieces are read kKB at a time with all their loads issued together, so a
-// merge of up to kKB pieces costs about one L2 round trip.  Not inlined: it
-// runs at most twice per CTA and gets its registers apart from the main loop.
+// merge of up to kKB pieces costs about one L2 round trip.  Inlined: it runs
+// inside the piece loop, where a call would save the loop's live registers to
+// the stack around it.
 template <int D>
-__device__ __noinline__ void merge_pieces(const DecodeArgs& a, int s, long long c_first,
+__device__ __forceinline__ void merge_pieces(const DecodeArgs& a, int s, long long c_first,
                                              int npieces, int ctid) {
   const int Hq = a.num_q_heads;
   constexpr int kNI = 4;  // float4 groups per thread per batch
@@ -574,7 +588,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else {
       cur.lo = cur.hi = 0;
     }
-    cur.idx = cur.lo;
+    // When the range's last sequence runs on into the next CTA's range, that
+    // piece is walked first ([mid, hi), then [lo, mid)): the range's first
+    // piece is also the first of [lo, mid), so both partial pieces of a
+    // sequence split between neighbouring CTAs finish early in both, and its
+    // merge happens while other blocks still stream, not at the launch's end.
+    cur.mid = cur.lo;
+    if (cur.hi > cur.lo) {
+      const int sl = seq_of(pre, S, cur.hi - 1);
+      if (pre[sl + 1] > cur.hi && pre[sl] > cur.lo) cur.mid = pre[sl];
+    }
+    cur.phase = cur.mid > cur.lo ? 0 : 1;
+    cur.idx = cur.phase == 0 ? cur.mid : cur.lo;
+    cur.end = cur.hi;
   } else {
     cur.u = blockIdx.x;
     cur.U = static_cast<long long>(a.num_seqs) * a.max_parts;
@@ -722,10 +748,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int d0 = lane >> 2;
   const int hq = lane >> 2;
   volatile int* abort_flag = misc;
-  // balanced partial pieces (at most the CTA's first and last) are published
-  // as they finish; their tickets and merges wait until the CTA is done
-  long long def_cf[2] = {0, 0};
-  int def_np[2] = {0, 0}, def_s[2] = {0, 0}, def_tk[2] = {0, 0}, ndef = 0;
   Piece pc;
   uint32_t g = 0;
   int qi = 0;
@@ -1024,33 +1046,18 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (hb < G) slot[Hq * D + hgb] = lseb;
         }
       }
-      // take the sequence's ticket now (release of the slot stores above);
-      // the result is read after the CTA's last piece, so a first piece does
-      // not hold up the stream, and a merge is left to the end
+      // take the sequence's ticket (release of the slot stores above); the
+      // last of its pieces to draw one merges them all, here and now: the
+      // partial pieces are walked first, so this happens while the producer
+      // keeps the ring full and other CTAs use the bandwidth
       const long long cf = cta_of(pc.seg_start, cur.W, cur.C);
+      const int np = static_cast<int>(cta_of(pc.seg_start + pc.nb - 1, cur.W, cur.C) - cf + 1);
       named_barrier(1, kConsumerThreads);
-      int tk = 0;
-      if (ctid == 0) tk = atom_add_acq_rel_gpu(a.counters + cf, 1);
-      if (ndef < 2) {
-        def_cf[ndef] = cf;
-        def_np[ndef] = static_cast<int>(cta_of(pc.seg_start + pc.nb - 1, cur.W, cur.C) - cf + 1);
-        def_s[ndef] = pc.s;
-        def_tk[ndef] = tk;
-        ++ndef;
-      }
-    }
-  }
-
-  // ---- the last piece of a sequence to draw its ticket merges all of them
-  if (a.mode == kModeBalanced && ndef > 0) {
-    if (ctid == 0)
-      for (int k = 0; k < ndef; ++k) misc[1 + k] = def_tk[k];
-    named_barrier(1, kConsumerThreads);
-    for (int k = 0; k < ndef; ++k) {
-      if (misc[1 + k] == def_np[k] - 1) {
-        merge_pieces<D>(a, def_s[k], def_cf[k], def_np[k], ctid);
-        if (ctid == 0) a.counters[def_cf[k]] = 0;
-        named_barrier(1, kConsumerThreads);
+      if (ctid == 0) misc[1] = atom_add_acq_rel_gpu(a.counters + cf, 1);
+      named_barrier(1, kConsumerThreads);
+      if (misc[1] == np - 1) {
+        merge_pieces<D>(a, pc.s, cf, np, ctid);
+        if (ctid == 0) a.counters[cf] = 0;
       }
     }
   }
