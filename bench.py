@@ -181,6 +181,7 @@ class Replica:
         self.slot_mapping = torch.from_numpy(w.slot_mapping).to(dev)
         S, Hq, D = w.num_decode_seqs, w.num_q_heads, w.head_dim
         self.out = torch.empty((S, Hq, D), dtype=torch.bfloat16, device=dev)
+        self.cow_pairs = torch.from_numpy(w.cow_pairs).to(dev) if len(w.cow_pairs) else None
         C = w.num_chunks
         if C:
             T = int(w.cu_q_lens[C])
@@ -242,13 +243,28 @@ def run_gpu(args, rank, world, local_rank):
     T = int(w.cu_q_lens[w.num_chunks]) if hybrid else 0
     main = torch.cuda.current_stream()
     s_chunk = torch.cuda.Stream(device=dev) if hybrid else None
-    launches_per_step = 2 + (1 if P > 0 else 0) + (1 if hybrid else 0)
+    hws = [pa.alloc_workspace(pa.pa_hybrid_workspace_size(S, Hq, w.num_kv_heads, D,
+                                                          w.max_blocks_per_seq), dev)
+           for _ in range(R)] if hybrid else None
+    cow = len(w.cow_pairs) > 0
+    launches_per_step = 2 + (1 if P > 0 else 0) + (1 if hybrid else 0) + (1 if cow else 0)
 
     def step(i, ev=None, cev=None):
         r = reps[i % R]
         cur = torch.cuda.current_stream()
+        if cow:  # private copies of shared blocks about to be written (copy on write)
+            pa.pa_copy_blocks(r.k_cache, r.v_cache, r.cow_pairs)
         pa.pa_reshape_and_cache(r.key, r.value, r.k_cache, r.v_cache, r.slot_mapping)
-        if hybrid:
+        if hybrid and ev is None:
+            # the hybrid batch in one call: the chunk's tiles co-scheduled
+            # beside the decode on the SMs it leaves free
+            s0, q0, S_ = w.decode_seq0, w.q_decode_row0, w.num_decode_seqs
+            pa.pa_hybrid_attention(r.out_chunk, r.q[:T], r.block_tables[:w.num_chunks], r.cu,
+                                   r.qs, r.seq_lens[:w.num_chunks], max_q, r.out,
+                                   r.q[q0:q0 + S_], r.block_tables[s0:], r.seq_lens[s0:],
+                                   r.k_cache, r.v_cache, w.scale, hws[i % R])
+            return
+        if hybrid:  # timed kernel by kernel (no graphs): chunk and decode on two streams
             s_chunk.wait_stream(cur)
             if cev is not None:
                 cev[0].record(s_chunk)
@@ -278,8 +294,8 @@ def run_gpu(args, rank, world, local_rank):
         raise RuntimeError("device error flags set during warm-up")
 
     # Graph replay: one CUDA graph per round of R steps (every replica's
-    # scatter, then its decode; the hybrid step forks the prefill chunk onto a
-    # second stream), each kernel a programmatic dependent of the one before,
+    # scatter, then its decode; the hybrid step's call co-schedules the prefill
+    # chunk beside the decode), each kernel a programmatic dependent of the one before,
     # so consecutive kernels overlap launch and prologue with the previous
     # one's drain.  Single-step graphs cover a remainder of K mod R steps.
     use_graphs = not args.no_graphs
@@ -364,7 +380,7 @@ def run_gpu(args, rank, world, local_rank):
     if flags:
         raise RuntimeError(f"device error flags {flags} after the timed region")
 
-    e2e = run_e2e(args, w, reps, ws, dev, pa, dist)
+    e2e = run_e2e(args, w, reps, ws, dev, pa, dist, s_chunk, max_q, T, hws)
     fp8 = measure_fp8_decode(args, w, reps, ws, dev, pa) if (use_graphs and w.head_dim == 128) \
         else None
     casc = measure_cascade(args, w, reps, dev, pa) if (use_graphs and args.config == "cow_prefix_mix") \
@@ -477,46 +493,148 @@ def measure_cascade(args, w, reps, dev, pa, group=4):
             "tokens_per_s": S / (ms * 1e-3)}
 
 
-def run_e2e(args, w, reps, ws, dev, pa, dist):
-    """Same metric through the public API with host buffers: every step copies
-    its inputs (queries, new K/V, slots, block tables, lengths) from pinned
-    host memory, runs scatter + decode, and reads the output back."""
+def run_e2e(args, w, reps, ws, dev, pa, dist, s_chunk, max_q, T, hws):
+    """Same metric through the public API with host buffers, run the way a
+    serving loop runs it.  Every step uploads its inputs (queries, new K/V,
+    slots, copy-on-write pairs, block tables, lengths; the chunk's metadata in
+    the hybrid batch) from one pinned host buffer in one copy, runs the step's
+    kernels on views of the uploaded buffer, and reads its outputs back into
+    pinned host memory.  Three streams pipeline the steps: uploads run ahead of
+    the kernels, read-backs follow them.  With graphs (the default) one CUDA
+    graph holds a round of R steps, one per replica, and rounds replay back to
+    back; without, the steps are issued one by one and a replica's buffers are
+    reused only after the step that last used them has finished its kernels
+    (for the upload) and its read-back (for the outputs)."""
     import torch
 
+    R = len(reps)
     K = max(args.warmup + 1, min(args.steps, args.e2e_steps))
-    r = reps[0]
-    s0, q0, S = w.decode_seq0, w.q_decode_row0, w.num_decode_seqs
-    host = {n: getattr(r, n).cpu().pin_memory() for n in
-            ("q", "key", "value", "slot_mapping", "block_tables", "seq_lens")}
-    out_h = torch.empty(r.out.shape, dtype=r.out.dtype).pin_memory()
-    h2d = sum(t.numel() * t.element_size() for t in host.values())
-    d2h = out_h.numel() * out_h.element_size()
+    if not args.no_graphs:
+        K = (K + R - 1) // R * R
+    hybrid = w.num_chunks > 0
+    s0, q0, S, C = w.decode_seq0, w.q_decode_row0, w.num_decode_seqs, w.num_chunks
     P = args.partition_tokens
-    main = torch.cuda.current_stream()
+    names = ["q", "key", "value", "slot_mapping", "block_tables", "seq_lens"]
+    names += ["cow_pairs"] if reps[0].cow_pairs is not None else []
+    names += ["cu", "qs"] if hybrid else []
+    layout, total = {}, 0
+    for n in names:
+        t = getattr(reps[0], n)
+        layout[n] = (total, t.dtype, tuple(t.shape), t.numel() * t.element_size())
+        total += (layout[n][3] + 255) // 256 * 256
+    host = torch.zeros(total, dtype=torch.uint8).pin_memory()
+    for n, (o, _, _, nb) in layout.items():
+        host[o:o + nb].copy_(getattr(reps[0], n).cpu().contiguous().view(-1).view(torch.uint8))
+    arenas = [torch.empty(total, dtype=torch.uint8, device=dev) for _ in range(R)]
+    views = [{n: ar[o:o + nb].view(dt).view(shape) for n, (o, dt, shape, nb) in layout.items()}
+             for ar in arenas]
+    results = [[r.out] + ([r.out_chunk] if hybrid else []) for r in reps]
+    host_out = [[torch.empty(x.shape, dtype=x.dtype).pin_memory() for x in res] for res in results]
+    d2h = sum(x.numel() * x.element_size() for x in results[0])
 
-    def step(i):
-        rr = reps[i % len(reps)]
-        for n, t in host.items():
-            getattr(rr, n).copy_(t, non_blocking=True)
-        pa.pa_reshape_and_cache(rr.key, rr.value, rr.k_cache, rr.v_cache, rr.slot_mapping)
-        pa.pa_decode(*decode_args(w, rr), w.scale, partition_tokens=P, workspace=ws[i % len(reps)])
-        out_h.copy_(rr.out, non_blocking=True)
+    comp = torch.cuda.current_stream()
+    s_up, s_dn = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
+    ev_up = [torch.cuda.Event() for _ in range(R)]
+    ev_k = [torch.cuda.Event() for _ in range(R)]
+    ev_dn = [torch.cuda.Event() for _ in range(R)]
+    used = [False] * R
 
-    for i in range(args.warmup):
-        step(i)
+    def kernels(j):  # on the current stream
+        r, v = reps[j], views[j]
+        comp = torch.cuda.current_stream()
+        if "cow_pairs" in v:
+            pa.pa_copy_blocks(r.k_cache, r.v_cache, v["cow_pairs"])
+        pa.pa_reshape_and_cache(v["key"], v["value"], r.k_cache, r.v_cache, v["slot_mapping"])
+        if hybrid and not args.no_graphs:
+            pa.pa_hybrid_attention(r.out_chunk, v["q"][:T], v["block_tables"][:C], v["cu"],
+                                   v["qs"], v["seq_lens"][:C], max_q, r.out, v["q"][q0:q0 + S],
+                                   v["block_tables"][s0:], v["seq_lens"][s0:], r.k_cache,
+                                   r.v_cache, w.scale, hws[j])
+            return
+        if hybrid:
+            s_chunk.wait_stream(comp)
+            pa.pa_prefill_chunk(r.out_chunk, v["q"][:T], r.k_cache, r.v_cache,
+                                v["block_tables"][:C], v["cu"], v["qs"], v["seq_lens"][:C],
+                                max_q, w.scale, stream=s_chunk)
+        pa.pa_decode(r.out, v["q"][q0:q0 + S], r.k_cache, r.v_cache, v["block_tables"][s0:],
+                     v["seq_lens"][s0:], w.scale, partition_tokens=P, workspace=ws[j])
+        if hybrid:
+            comp.wait_stream(s_chunk)
+
+    def one(i):
+        j = i % R
+        if used[j]:
+            s_up.wait_event(ev_k[j])
+        with torch.cuda.stream(s_up):
+            arenas[j].copy_(host, non_blocking=True)
+        ev_up[j].record(s_up)
+        comp.wait_event(ev_up[j])
+        if used[j]:
+            comp.wait_event(ev_dn[j])
+        kernels(j)
+        ev_k[j].record(comp)
+        s_dn.wait_event(ev_k[j])
+        with torch.cuda.stream(s_dn):
+            for dst, src in zip(host_out[j], results[j]):
+                dst.copy_(src, non_blocking=True)
+        ev_dn[j].record(s_dn)
+        used[j] = True
+
+    def round_body():  # R pipelined steps, captured into one graph
+        cap = torch.cuda.current_stream()
+        s_up.wait_stream(cap)
+        s_dn.wait_stream(cap)
+        for j in range(R):
+            with torch.cuda.stream(s_up):
+                arenas[j].copy_(host, non_blocking=True)
+            ev_up[j].record(s_up)
+            cap.wait_event(ev_up[j])
+            kernels(j)
+            ev_k[j].record(cap)
+            s_dn.wait_event(ev_k[j])
+            with torch.cuda.stream(s_dn):
+                for dst, src in zip(host_out[j], results[j]):
+                    dst.copy_(src, non_blocking=True)
+        cap.wait_stream(s_up)
+        cap.wait_stream(s_dn)
+
+    g = None
+    if not args.no_graphs:
+        for i in range(args.warmup):
+            one(i)
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            round_body()
+        for _ in range(max(1, args.warmup // R)):
+            g.replay()
+    else:
+        for i in range(args.warmup):
+            one(i)
     torch.cuda.synchronize()
     a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     if dist:
         import torch.distributed as tdist
         tdist.barrier()
     torch.cuda.synchronize()
-    a.record(main)
-    for i in range(K):
-        step(i)
-    b.record(main)
+    a.record(comp)
+    if g is not None:
+        for _ in range(K // R):
+            g.replay()
+    else:
+        s_up.wait_stream(comp)
+        for i in range(K):
+            one(args.warmup + i)
+        comp.wait_stream(s_dn)
+    b.record(comp)
     torch.cuda.synchronize()
+    if pa.pa_device_error_flags() != 0:
+        raise RuntimeError("device error flags set in the end-to-end run")
     ms, kv_all = reduce_over_ranks(a.elapsed_time(b), kv_bytes_decode(w) * K, dev)
-    return dict(ms=ms, steps=K, h2d=h2d, d2h=d2h, kv_all=kv_all)
+    return dict(ms=ms, steps=K, h2d=total, d2h=d2h, kv_all=kv_all,
+                pipeline=(f"one CUDA graph per round of {R} steps; " if g is not None else "")
+                + "upload (one copy from pinned host memory), kernels and read-back on three "
+                  "streams, uploads running ahead of the kernels and read-backs following them")
 
 
 def run_oracle(w, min_seconds):
@@ -773,8 +891,10 @@ def main():
                          f"({args.replicas * 2 * w.k_cache.nbytes / 1e9:.2f} GB) >> 129 MB L2",
                    "parallelism": f"replicas x{world}",
                    "launch": (f"CUDA graph per round of {args.replicas} steps (scatter, "
-                              + ("prefill chunk on a second stream, " if w.num_chunks else "")
-                              + "decode; programmatic dependent launches)") if res["graphs"]
+                              + ("then pa_hybrid_attention: the decode on the SMs the prefill "
+                                 "chunk leaves free, the chunk beside it; "
+                                 if w.num_chunks else "decode; ")
+                              + "programmatic dependent launches)") if res["graphs"]
                              else "eager launches from Python"},
         "tokens_per_s": w.num_decode_seqs * world * K / (res["elapsed_ms"] * 1e-3),
         "pct_of_nominal_8tbps": 100.0 * value / world / NOMINAL_HBM_GBS,
@@ -789,7 +909,8 @@ def main():
                                       else "CUDA events around each decode launch in the timed region"},
         "e2e": {"value": e["kv_all"] / (e["ms"] * 1e-3) / 1e9, "unit": "GB/s",
                 "h2d_bytes_per_step": e["h2d"], "d2h_bytes_per_step": e["d2h"],
-                "steps": e["steps"], "ms_per_step": e["ms"] / e["steps"]},
+                "steps": e["steps"], "ms_per_step": e["ms"] / e["steps"],
+                "pipeline": e["pipeline"]},
         "gpu_launches": res["launches"],
         "clocks": res["clocks"],
     }
@@ -816,6 +937,14 @@ def main():
                                             f"{args.replicas}); time / launches") if res["graphs"]
                                            else "CUDA events around each chunk launch while "
                                                 "the decode runs beside it"}
+        if res["graphs"]:
+            line["hybrid_step"] = {
+                "step_ms": step_ms, "decode_alone_ms": res["dec_ms"],
+                "chunk_alone_ms": res["chunk_ms"],
+                "chunk_hidden_frac": max(0.0, min(1.0, (res["dec_ms"] + res["chunk_ms"] - step_ms)
+                                                  / res["chunk_ms"])),
+                "how": "pa_hybrid_attention co-schedules the chunk's query tiles on the SMs the "
+                       "decode leaves free; step = scatter + that call"}
     if rank == 0:
         line["cpu_baseline"] = cpu_baseline_obj(w, args.cpu_seconds)
         line["host_block_manager"] = block_manager_timing()

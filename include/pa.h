@@ -276,6 +276,48 @@ int pa_prefill_chunk(void *out, const void *q, const void *k_cache, const void *
                      int64_t num_blocks, float scale, float *out_lse, void *stream);
 
 /*
+ * Bytes of workspace pa_hybrid_attention needs (a balanced decode's workspace
+ * plus 256 bytes); 0 on invalid sizes.
+ */
+size_t pa_hybrid_workspace_size(int num_decode_seqs, int num_q_heads, int num_kv_heads,
+                                int head_dim, int max_blocks_per_seq, int block_size);
+
+/*
+ * One Sarathi hybrid batch ("03 - Engines Papers", section 3 Sarathi /
+ * Sarathi-Serve: a step carries prefill chunks next to decodes under one
+ * token budget) in one call, after pa_reshape_and_cache of all the step's
+ * new tokens: the prefill chunks of pa_prefill_chunk (chunk arguments, same
+ * meaning and layouts) and the balanced decode of pa_decode with
+ * partition_tokens = 0 (decode arguments).  Both read the same pools.
+ *
+ * Co-scheduled on one stream: the decode runs on num_sms - chunk_sms
+ * persistent CTAs, and the chunk's query tiles start at once on the SMs it
+ * leaves free, so the chunk's tensor-core work runs under the decode's HBM
+ * streaming instead of after it.  chunk_sms = 0 picks about a fifth of the
+ * SMs; values are clamped to [1, num_sms - 1].  The chunk reads nothing the
+ * decode writes; the call's last kernel to finish waits for both, so work
+ * queued after the call on the stream sees both results.  With no chunk (or
+ * no decode) the call is pa_decode (or pa_prefill_chunk) alone.
+ *   workspace  device, pa_hybrid_workspace_size bytes, 256-byte aligned,
+ *              zero-filled before its first use (calls leave it zeroed);
+ *              one call in flight per workspace.
+ * Errors as pa_decode and pa_prefill_chunk; every argument is checked before
+ * anything is launched, except device errors, which surface at the caller's
+ * synchronization (pa_device_error_flags).
+ */
+int pa_hybrid_attention(void *out_chunk, const void *q_chunk, const int32_t *chunk_block_tables,
+                        int chunk_max_blocks, const int32_t *cu_q_lens,
+                        const int32_t *q_start_pos, const int32_t *chunk_seq_lens,
+                        int num_chunks, int total_q_tokens, int max_q_len, float *chunk_lse,
+                        void *out_decode, const void *q_decode,
+                        const int32_t *decode_block_tables, int decode_max_blocks,
+                        const int32_t *decode_seq_lens, int num_decode_seqs, float *decode_lse,
+                        const void *k_cache, const void *v_cache, int num_q_heads,
+                        int num_kv_heads, int head_dim, int block_size, int64_t num_blocks,
+                        float scale, int chunk_sms, void *workspace, size_t workspace_bytes,
+                        void *stream);
+
+/*
  * Size of the static device scratch behind pa_decode_noalloc (8 MiB).
  */
 #define PA_NOALLOC_SCRATCH_BYTES (8u << 20)

@@ -60,6 +60,10 @@ _SIGS = {
     "pa_decode_fp8": ([_P, _P, _P, _P, _P, _P, _P, _I, _P, _I, _I, _I, _I, _I, _L, _F, _I, _P, _P,
                        _S, _P], _I),
     "pa_device_error_flags": ([ctypes.POINTER(ctypes.c_uint), _I], _I),
+    "pa_hybrid_workspace_size": ([_I, _I, _I, _I, _I, _I], _S),
+    "pa_hybrid_attention": ([_P, _P, _P, _I, _P, _P, _P, _I, _I, _I, _P,
+                             _P, _P, _P, _I, _P, _I, _P,
+                             _P, _P, _I, _I, _I, _I, _L, _F, _I, _P, _S, _P], _I),
 }
 for _name, (_args, _res) in _SIGS.items():
     _fn = getattr(_lib, _name)
@@ -311,6 +315,46 @@ def pa_prefill_chunk(out, q, k_cache, v_cache, block_tables, cu_q_lens, q_start_
         _ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables),
         block_tables.shape[1], _ptr(cu_q_lens), _ptr(q_start_pos), _ptr(seq_lens), C, T,
         int(max_q_len), Hq, Hkv, D, bs, nb, float(scale), _ptr(out_lse), _stream(stream)))
+
+
+def pa_hybrid_workspace_size(num_decode_seqs, num_q_heads, num_kv_heads, head_dim,
+                             max_blocks_per_seq, block_size=16) -> int:
+    return int(_lib.pa_hybrid_workspace_size(num_decode_seqs, num_q_heads, num_kv_heads, head_dim,
+                                             max_blocks_per_seq, block_size))
+
+
+def pa_hybrid_attention(out_chunk, q_chunk, chunk_block_tables, cu_q_lens, q_start_pos,
+                        chunk_seq_lens, max_q_len, out_decode, q_decode, decode_block_tables,
+                        decode_seq_lens, k_cache, v_cache, scale, workspace, chunk_sms=0,
+                        chunk_lse=None, decode_lse=None, stream=None) -> None:
+    """Prefill chunks and balanced decodes of one hybrid batch, co-scheduled."""
+    _need(out_chunk, "out_chunk", torch.bfloat16, 3)
+    _need(q_chunk, "q_chunk", torch.bfloat16, 3)
+    _need(chunk_block_tables, "chunk_block_tables", torch.int32, 2)
+    _need(cu_q_lens, "cu_q_lens", torch.int32, 1)
+    _need(q_start_pos, "q_start_pos", torch.int32, 1)
+    _need(chunk_seq_lens, "chunk_seq_lens", torch.int32, 1)
+    _need(out_decode, "out_decode", torch.bfloat16, 3)
+    _need(q_decode, "q_decode", torch.bfloat16, 3)
+    _need(decode_block_tables, "decode_block_tables", torch.int32, 2)
+    _need(decode_seq_lens, "decode_seq_lens", torch.int32, 1)
+    _need(k_cache, "k_cache", torch.bfloat16, 4)
+    _need(v_cache, "v_cache", torch.bfloat16, 4)
+    _need(workspace, "workspace", torch.uint8, 1)
+    if chunk_lse is not None:
+        _need(chunk_lse, "chunk_lse", torch.float32, 2)
+    if decode_lse is not None:
+        _need(decode_lse, "decode_lse", torch.float32, 2)
+    T, Hq, D = q_chunk.shape
+    nb, bs, Hkv, _ = k_cache.shape
+    _check("pa_hybrid_attention", _lib.pa_hybrid_attention(
+        _ptr(out_chunk), _ptr(q_chunk), _ptr(chunk_block_tables), chunk_block_tables.shape[1],
+        _ptr(cu_q_lens), _ptr(q_start_pos), _ptr(chunk_seq_lens), q_start_pos.shape[0], T,
+        int(max_q_len), _ptr(chunk_lse),
+        _ptr(out_decode), _ptr(q_decode), _ptr(decode_block_tables), decode_block_tables.shape[1],
+        _ptr(decode_seq_lens), q_decode.shape[0], _ptr(decode_lse),
+        _ptr(k_cache), _ptr(v_cache), Hq, Hkv, D, bs, nb, float(scale), int(chunk_sms),
+        _ptr(workspace), workspace.numel(), _stream(stream)))
 
 
 def _host_ptr(a):

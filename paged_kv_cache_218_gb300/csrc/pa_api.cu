@@ -504,7 +504,8 @@ size_t pa_decode_workspace_size(int num_seqs, int num_q_heads, int num_kv_heads,
     cudaGetLastError();
     num_sms = 1024;  // no device visible: an upper bound
   }
-  return balanced_workspace_bytes(decode_grid(num_sms, kModeBalanced), num_q_heads, head_dim);
+  // sized for the largest grid a launch may use: one CTA per SM
+  return balanced_workspace_bytes(num_sms, num_q_heads, head_dim);
 }
 
 // pa_decode and pa_decode_fp8: the same launch; kv_fp8 selects E4M3 pools.
@@ -515,7 +516,8 @@ static int decode_impl(void* out, const void* q, const void* k_cache, const void
                        int num_kv_heads, int head_dim, int block_size, int64_t num_blocks,
                        float scale, int partition_tokens, float* out_lse, void* workspace,
                        size_t workspace_bytes, void* stream, const int32_t* start_blocks = nullptr,
-                       const float* init_o = nullptr, const float* init_lse = nullptr) {
+                       const float* init_o = nullptr, const float* init_lse = nullptr,
+                       int grid_override = 0) {
   if (int rc = check_shape(num_q_heads, num_kv_heads, head_dim, block_size)) return rc;
   if (kv_fp8 && head_dim != 128) return PA_ERR_UNSUPPORTED;
   if (num_seqs < 0 || max_blocks_per_seq <= 0 || num_blocks <= 0) return PA_ERR_INVALID;
@@ -557,7 +559,8 @@ static int decode_impl(void* out, const void* q, const void* k_cache, const void
   a.start_blocks = start_blocks;
   a.init_o = init_o;
   a.init_lse = init_lse;
-  int grid = decode_grid(d->num_sms, mode);
+  int grid = decode_grid(d->num_sms, mode, a.group, kv_fp8);
+  if (grid_override > 0) grid = grid_override < d->num_sms ? grid_override : d->num_sms;
   if (mode == kModeSinglePass) {
     a.part_blocks = max_blocks_per_seq;
     a.max_parts = 1;
@@ -731,8 +734,7 @@ int pa_decode_noalloc(void* out, const void* q, const void* k_cache, const void*
   if (num_seqs == 0) return PA_OK;
   DeviceInfo* d;
   if (int rc = current_device_info(&d)) return rc;
-  const size_t need = balanced_workspace_bytes(decode_grid(d->num_sms, kModeBalanced),
-                                               num_q_heads, head_dim);
+  const size_t need = balanced_workspace_bytes(d->num_sms, num_q_heads, head_dim);
   if (need > PA_NOALLOC_SCRATCH_BYTES) return PA_ERR_SCRATCH_LIMIT;
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return PA_ERR_CUDA;
@@ -749,8 +751,7 @@ int pa_decode_noalloc(void* out, const void* q, const void* k_cache, const void*
   }
   // the merge tickets must start at zero (the kernel leaves them zeroed, but a
   // call cut short by an error may not)
-  const size_t tickets = (static_cast<size_t>(decode_grid(d->num_sms, kModeBalanced)) * 4 + 255) /
-                         256 * 256;
+  const size_t tickets = (static_cast<size_t>(d->num_sms) * 4 + 255) / 256 * 256;
   if (cudaMemsetAsync(scratch, 0, tickets, static_cast<cudaStream_t>(stream)) != cudaSuccess)
     return PA_ERR_CUDA;
   return pa_decode(out, q, k_cache, v_cache, block_tables, max_blocks_per_seq, seq_lens, num_seqs,
@@ -784,12 +785,14 @@ int pa_merge_partials(void* out, float* out_lse, const float* part_out, const fl
   return launch_merge(m, static_cast<cudaStream_t>(stream)) == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
 
-int pa_prefill_chunk(void* out, const void* q, const void* k_cache, const void* v_cache,
-                     const int32_t* block_tables, int max_blocks_per_seq,
-                     const int32_t* cu_q_lens, const int32_t* q_start_pos,
-                     const int32_t* seq_lens, int num_chunks, int total_q_tokens, int max_q_len,
-                     int num_q_heads, int num_kv_heads, int head_dim, int block_size,
-                     int64_t num_blocks, float scale, float* out_lse, void* stream) {
+// Argument checks of a prefill-chunk call (PA_OK: launch it; done: nothing to do).
+static int prefill_check(const void* out, const void* q, const void* k_cache, const void* v_cache,
+                         const int32_t* block_tables, int max_blocks_per_seq,
+                         const int32_t* cu_q_lens, const int32_t* q_start_pos,
+                         const int32_t* seq_lens, int num_chunks, int total_q_tokens,
+                         int max_q_len, int num_q_heads, int num_kv_heads, int head_dim,
+                         int block_size, int64_t num_blocks, float scale, bool* done) {
+  *done = false;
   if (int rc = check_shape(num_q_heads, num_kv_heads, head_dim, block_size)) return rc;
   if (head_dim != 128) return PA_ERR_UNSUPPORTED;
   const int group = num_q_heads / num_kv_heads;
@@ -799,14 +802,41 @@ int pa_prefill_chunk(void* out, const void* q, const void* k_cache, const void* 
     return PA_ERR_INVALID;
   if (num_blocks * kBlockSize > (int64_t)INT32_MAX) return PA_ERR_UNSUPPORTED;
   if (!(scale > 0.f) || !isfinite(scale)) return PA_ERR_INVALID;
-  if (num_chunks == 0 || total_q_tokens == 0 || max_q_len == 0) return PA_OK;
+  if (num_chunks == 0 || total_q_tokens == 0 || max_q_len == 0) {
+    *done = true;
+    return PA_OK;
+  }
   if (!out || !q || !k_cache || !v_cache || !block_tables || !cu_q_lens || !q_start_pos ||
       !seq_lens)
     return PA_ERR_INVALID;
   if (!aligned(out, 16) || !aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16))
     return PA_ERR_INVALID;
+  const int tokens_per_tile = 128 / group;
+  const int64_t tiles = static_cast<int64_t>((max_q_len + tokens_per_tile - 1) / tokens_per_tile +
+                                             kMaxCluster) * num_chunks * num_kv_heads;
+  if (tiles > INT32_MAX) return PA_ERR_UNSUPPORTED;
+  return PA_OK;
+}
+
+// The chunk launch of pa_prefill_chunk; done_ctr non-null: co-scheduled
+// behind the decode just launched on the same stream (pa_hybrid_attention).
+static int prefill_impl(void* out, const void* q, const void* k_cache, const void* v_cache,
+                        const int32_t* block_tables, int max_blocks_per_seq,
+                        const int32_t* cu_q_lens, const int32_t* q_start_pos,
+                        const int32_t* seq_lens, int num_chunks, int total_q_tokens, int max_q_len,
+                        int num_q_heads, int num_kv_heads, int head_dim, int block_size,
+                        int64_t num_blocks, float scale, float* out_lse, void* stream,
+                        unsigned int* done_ctr) {
+  bool done = false;
+  if (int rc = prefill_check(out, q, k_cache, v_cache, block_tables, max_blocks_per_seq,
+                             cu_q_lens, q_start_pos, seq_lens, num_chunks, total_q_tokens,
+                             max_q_len, num_q_heads, num_kv_heads, head_dim, block_size,
+                             num_blocks, scale, &done))
+    return rc;
+  if (done) return PA_OK;
   DeviceInfo* d;
   if (int rc = current_device_info(&d)) return rc;
+  const int group = num_q_heads / num_kv_heads;
   PrefillArgs a{};
   a.out = static_cast<__nv_bfloat16*>(out);
   a.block_tables = block_tables;
@@ -821,9 +851,11 @@ int pa_prefill_chunk(void* out, const void* q, const void* k_cache, const void* 
   a.num_q_heads = num_q_heads;
   a.num_kv_heads = num_kv_heads;
   a.group = group;
+  a.after_decode = done_ctr ? 1 : 0;
+  a.done_ctr = done_ctr;
   const int tokens_per_tile = 128 / group;
   a.tiles_per_chunk = (max_q_len + tokens_per_tile - 1) / tokens_per_tile;
-  const int cl = prefill_cluster();
+  const int cl = prefill_cluster(done_ctr != nullptr);
   a.tiles_per_chunk = (a.tiles_per_chunk + cl - 1) / cl * cl;
   a.scale_log2 = scale * 1.4426950408889634f;
   CUtensorMap tm_q, tm_k, tm_v;
@@ -832,11 +864,85 @@ int pa_prefill_chunk(void* out, const void* q, const void* k_cache, const void* 
       encode_pool_map(&tm_v, v_cache, num_blocks, num_kv_heads, head_dim, kBlockSize))
     return PA_ERR_CUDA;
   const int64_t tiles = static_cast<int64_t>(a.tiles_per_chunk) * num_chunks * num_kv_heads;
-  if (tiles > INT32_MAX) return PA_ERR_UNSUPPORTED;
   return launch_prefill(a, &tm_q, &tm_k, &tm_v, static_cast<int>(tiles),
                         static_cast<cudaStream_t>(stream)) == cudaSuccess
              ? PA_OK
              : PA_ERR_CUDA;
+}
+
+int pa_prefill_chunk(void* out, const void* q, const void* k_cache, const void* v_cache,
+                     const int32_t* block_tables, int max_blocks_per_seq,
+                     const int32_t* cu_q_lens, const int32_t* q_start_pos,
+                     const int32_t* seq_lens, int num_chunks, int total_q_tokens, int max_q_len,
+                     int num_q_heads, int num_kv_heads, int head_dim, int block_size,
+                     int64_t num_blocks, float scale, float* out_lse, void* stream) {
+  return prefill_impl(out, q, k_cache, v_cache, block_tables, max_blocks_per_seq, cu_q_lens,
+                      q_start_pos, seq_lens, num_chunks, total_q_tokens, max_q_len, num_q_heads,
+                      num_kv_heads, head_dim, block_size, num_blocks, scale, out_lse, stream,
+                      nullptr);
+}
+
+size_t pa_hybrid_workspace_size(int num_decode_seqs, int num_q_heads, int num_kv_heads,
+                                int head_dim, int max_blocks_per_seq, int block_size) {
+  const size_t dec = pa_decode_workspace_size(num_decode_seqs, num_q_heads, num_kv_heads, head_dim,
+                                              max_blocks_per_seq, block_size, 0);
+  return dec == 0 ? 0 : 256 + dec;
+}
+
+int pa_hybrid_attention(void* out_chunk, const void* q_chunk, const int32_t* chunk_block_tables,
+                        int chunk_max_blocks, const int32_t* cu_q_lens,
+                        const int32_t* q_start_pos, const int32_t* chunk_seq_lens,
+                        int num_chunks, int total_q_tokens, int max_q_len, float* chunk_lse,
+                        void* out_decode, const void* q_decode,
+                        const int32_t* decode_block_tables, int decode_max_blocks,
+                        const int32_t* decode_seq_lens, int num_decode_seqs, float* decode_lse,
+                        const void* k_cache, const void* v_cache, int num_q_heads,
+                        int num_kv_heads, int head_dim, int block_size, int64_t num_blocks,
+                        float scale, int chunk_sms, void* workspace, size_t workspace_bytes,
+                        void* stream) {
+  bool no_chunk = false;
+  if (int rc = prefill_check(out_chunk, q_chunk, k_cache, v_cache, chunk_block_tables,
+                             chunk_max_blocks, cu_q_lens, q_start_pos, chunk_seq_lens, num_chunks,
+                             total_q_tokens, max_q_len, num_q_heads, num_kv_heads, head_dim,
+                             block_size, num_blocks, scale, &no_chunk))
+    return rc;
+  if (num_decode_seqs < 0 || chunk_sms < 0) return PA_ERR_INVALID;
+  if (num_decode_seqs == 0)
+    return no_chunk ? PA_OK
+                    : prefill_impl(out_chunk, q_chunk, k_cache, v_cache, chunk_block_tables,
+                                   chunk_max_blocks, cu_q_lens, q_start_pos, chunk_seq_lens,
+                                   num_chunks, total_q_tokens, max_q_len, num_q_heads,
+                                   num_kv_heads, head_dim, block_size, num_blocks, scale,
+                                   chunk_lse, stream, nullptr);
+  const size_t need = pa_hybrid_workspace_size(num_decode_seqs, num_q_heads, num_kv_heads,
+                                               head_dim, decode_max_blocks, block_size);
+  if (need == 0) return PA_ERR_INVALID;
+  if (!workspace || workspace_bytes < need || !aligned(workspace, 256)) return PA_ERR_WORKSPACE;
+  void* dec_ws = static_cast<char*>(workspace) + 256;
+  const size_t dec_bytes = workspace_bytes - 256;
+  if (no_chunk)
+    return decode_impl(out_decode, q_decode, k_cache, v_cache, nullptr, nullptr, false,
+                       decode_block_tables, decode_max_blocks, decode_seq_lens, num_decode_seqs,
+                       num_q_heads, num_kv_heads, head_dim, block_size, num_blocks, scale, 0,
+                       decode_lse, dec_ws, dec_bytes, stream);
+  DeviceInfo* d;
+  if (int rc = current_device_info(&d)) return rc;
+  if (d->num_sms < 2) return PA_ERR_UNSUPPORTED;
+  // SMs left to the chunk: by default about a fifth (32 of 152), which on the
+  // Sarathi batch of a 512-query chunk next to 128 decodes hides the chunk's
+  // tensor work under the decode's HBM streaming
+  int cs = chunk_sms > 0 ? chunk_sms : (d->num_sms * 21 + 50) / 100;
+  cs = cs < 1 ? 1 : (cs > d->num_sms - 1 ? d->num_sms - 1 : cs);
+  if (int rc = decode_impl(out_decode, q_decode, k_cache, v_cache, nullptr, nullptr, false,
+                           decode_block_tables, decode_max_blocks, decode_seq_lens,
+                           num_decode_seqs, num_q_heads, num_kv_heads, head_dim, block_size,
+                           num_blocks, scale, 0, decode_lse, dec_ws, dec_bytes, stream, nullptr,
+                           nullptr, nullptr, d->num_sms - cs))
+    return rc;
+  return prefill_impl(out_chunk, q_chunk, k_cache, v_cache, chunk_block_tables, chunk_max_blocks,
+                      cu_q_lens, q_start_pos, chunk_seq_lens, num_chunks, total_q_tokens,
+                      max_q_len, num_q_heads, num_kv_heads, head_dim, block_size, num_blocks,
+                      scale, chunk_lse, stream, static_cast<unsigned int*>(workspace));
 }
 
 int pa_validate_metadata(const int32_t* block_tables, int max_blocks_per_seq,

@@ -12,6 +12,7 @@ namespace pa {
 constexpr int kBlockSize = 16;
 constexpr int kMaxGroup = 8;            // q heads per kv head handled by one MMA column tile
 constexpr int kMaxSeqsBalanced = 16000; // per-CTA prefix of block counts lives in shared memory
+constexpr int kMaxCluster = 4;          // prefill: most query tiles per cluster
 
 enum DecodeMode : int {
   kModeSinglePass = 0,  // one work item per (sequence, kv head)
@@ -86,6 +87,8 @@ struct PrefillArgs {
   int group;
   int tiles_per_chunk;  // M tiles of 128 rows per (chunk, kv head)
   float scale_log2;
+  int after_decode;          // co-scheduled behind a decode on the same stream
+  unsigned int* done_ctr;    // after_decode: CTAs finished (self-resetting)
 };
 
 struct CascadeArgs {
@@ -119,7 +122,7 @@ size_t balanced_workspace_bytes(int grid, int num_q_heads, int head_dim);
 // Kernel launchers (return cudaError_t of the launch).
 cudaError_t launch_decode(DecodeArgs a, const CUtensorMap* tm_k, const CUtensorMap* tm_v,
                           int head_dim, int grid, cudaStream_t stream);
-int decode_grid(int num_sms, int mode);
+int decode_grid(int num_sms, int mode, int group, bool kv_fp8);  // CTAs of a decode launch
 bool decode_supported(int head_dim, int num_kv_heads, int num_q_heads, int mode, int num_seqs,
                       bool kv_fp8);
 cudaError_t launch_merge(const MergeArgs& a, cudaStream_t stream);
@@ -130,6 +133,6 @@ bool cascade_shape(int num_kv_heads, int group, int max_group, int* kv_per_cta, 
                    int* stages);
 cudaError_t launch_cascade_prefix(const CascadeArgs& a, const CUtensorMap* tm_k,
                                   const CUtensorMap* tm_v, cudaStream_t stream);
-int prefill_cluster();  // query tiles per cluster (the grid is a multiple of it)
+int prefill_cluster(bool co_scheduled);  // query tiles per cluster (the grid is a multiple of it)
 
 }  // namespace pa

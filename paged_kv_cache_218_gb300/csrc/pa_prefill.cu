@@ -48,7 +48,8 @@
 namespace pa {
 namespace {
 
-constexpr int kCluster = 4;   // query tiles of one kv head sharing every K/V tile load
+constexpr int kClusterAlone = 4;  // query tiles of one kv head sharing every K/V tile load
+static_assert(kClusterAlone <= kMaxCluster, "tile counts are bounded with kMaxCluster");
 constexpr int kSoftmaxWarps = 8;
 constexpr int kMmaWarp = 8;
 constexpr int kLoadWarp = 9;
@@ -119,6 +120,24 @@ __device__ __forceinline__ bool wait_or_abort_warp(uint32_t bar, uint32_t parity
   return ok;
 }
 
+// Co-scheduled next to a decode (PrefillArgs::after_decode) the chunk is a
+// programmatic dependent of that decode, whose result it does not read: its
+// CTAs start as soon as the decode's have started and take the SMs the decode
+// leaves free.  Its K/V were scattered by the kernel before the decode, which
+// has completed by then.  To keep the stream's order for the kernels after
+// it, the last CTA of the chunk to finish waits for the decode before it
+// exits (the others exit at once and free their SMs).
+__device__ __forceinline__ void chunk_exit(const PrefillArgs& a, int tid) {
+  if (!a.after_decode || tid != 0) return;
+  if (atomicAdd(a.done_ctr, 1u) == gridDim.x - 1) {
+    *a.done_ctr = 0;  // for the next call
+    griddep_wait();
+  }
+}
+
+// kCluster query tiles (4 alone, 1 when co-scheduled: a cluster needs that
+// many free SMs of one GPC at once) share each K/V tile load by multicast.
+template <int kCluster>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                    const __grid_constant__ CUtensorMap tm_v, const PrefillArgs a) {
@@ -154,8 +173,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   constexpr uint16_t kMask = (1u << kCluster) - 1;
 
   // launched as a programmatic dependent of the previous kernel (the scatter
-  // of this step's K/V): nothing before this line touches global memory
-  griddep_wait();
+  // of this step's K/V): nothing before this line touches global memory --
+  // unless co-scheduled behind a decode (see chunk_exit)
+  if (!a.after_decode) griddep_wait();
   // the next kernel on the stream may start launching; it waits for this grid
   griddep_launch_dependents();
 
@@ -165,11 +185,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int qlen = q1 - q0;
   if (qlen < 0 || p0 < 0 || p0 + qlen > n || n > a.max_blocks * kBlockSize) {
     if (tid == 0 && m == 0 && kvh == 0) atomicOr(a.err, PA_DEVERR_CHUNK);
+    chunk_exit(a, tid);
     return;
   }
   const int t0 = m * tpt;
   const int tc0 = mg * kCluster * tpt;  // first query token of the cluster
-  if (tc0 >= qlen) return;              // the whole cluster is past the chunk
+  if (tc0 >= qlen) {  // the whole cluster is past the chunk
+    chunk_exit(a, tid);
+    return;
+  }
   const int tv = qlen - t0 < tpt ? qlen - t0 : tpt;  // valid tokens here (<= 0: none)
   // keys [0, kmax) are visible to some row of the cluster; every member walks
   // the same tiles (its own rows mask what they may not see)
@@ -495,16 +519,20 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_before();
   cluster_sync();  // no member leaves while a partner may still write to it
   if (warp == 0) tmem_dealloc(tmem, kTmemCols);
+  chunk_exit(a, tid);
 }
 
 }  // namespace
 
 size_t prefill_smem_bytes() { return kSmemBytes + 1024; }
 
-int prefill_cluster() { return kCluster; }
+int prefill_cluster(bool co_scheduled) { return co_scheduled ? 1 : kClusterAlone; }
 
-cudaError_t launch_prefill(const PrefillArgs& a, const CUtensorMap* tm_q, const CUtensorMap* tm_k,
-                           const CUtensorMap* tm_v, int grid_tiles, cudaStream_t stream) {
+namespace {
+template <int kCluster>
+cudaError_t launch_prefill_as(const PrefillArgs& a, const CUtensorMap* tm_q,
+                              const CUtensorMap* tm_k, const CUtensorMap* tm_v, int grid_tiles,
+                              cudaStream_t stream) {
   const size_t smem = prefill_smem_bytes();
   // raise the kernel's dynamic shared-memory limit once per device
   static std::mutex mu;
@@ -516,15 +544,15 @@ cudaError_t launch_prefill(const PrefillArgs& a, const CUtensorMap* tm_q, const 
   {
     std::lock_guard<std::mutex> lock(mu);
     if (!set_for[dev]) {
-      e = cudaFuncSetAttribute(prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               static_cast<int>(smem));
+      e = cudaFuncSetAttribute(prefill_kernel<kCluster>,
+                               cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
       if (e != cudaSuccess) return e;
       set_for[dev] = true;
     }
   }
   // programmatic dependent launch: the CTAs may start while the previous
   // kernel on the stream finishes; they touch no global memory before
-  // griddepcontrol.wait
+  // griddepcontrol.wait (co-scheduled: see chunk_exit)
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid_tiles);
   cfg.blockDim = dim3(kThreads);
@@ -539,9 +567,16 @@ cudaError_t launch_prefill(const PrefillArgs& a, const CUtensorMap* tm_q, const 
   attr[1].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 2;
-  e = cudaLaunchKernelEx(&cfg, prefill_kernel, *tm_q, *tm_k, *tm_v, a);
+  e = cudaLaunchKernelEx(&cfg, prefill_kernel<kCluster>, *tm_q, *tm_k, *tm_v, a);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
+}
+}  // namespace
+
+cudaError_t launch_prefill(const PrefillArgs& a, const CUtensorMap* tm_q, const CUtensorMap* tm_k,
+                           const CUtensorMap* tm_v, int grid_tiles, cudaStream_t stream) {
+  return a.after_decode ? launch_prefill_as<1>(a, tm_q, tm_k, tm_v, grid_tiles, stream)
+                        : launch_prefill_as<kClusterAlone>(a, tm_q, tm_k, tm_v, grid_tiles, stream);
 }
 
 }  // namespace pa

@@ -161,3 +161,112 @@ def test_prefill_rejects_unsupported_shapes(pa, cuda_device):
     with pytest.raises(pa.PAError) as e:
         _prefill(pa, dw)
     assert e.value.status == pa.PA_ERR_UNSUPPORTED
+
+
+def _hybrid_call(pa, dw, ws, chunk_sms=0, with_lse=True):
+    w = dw.w
+    dev = dw.q.device
+    C = w.num_chunks
+    T = int(w.cu_q_lens[C])
+    S, Hq, D = w.num_decode_seqs, w.num_q_heads, w.head_dim
+    out_c = torch.full((T, Hq, D), float("nan"), dtype=torch.bfloat16, device=dev)
+    out_d = torch.full((S, Hq, D), float("nan"), dtype=torch.bfloat16, device=dev)
+    lse_c = torch.full((T, Hq), float("nan"), dtype=torch.float32, device=dev) if with_lse else None
+    lse_d = torch.full((S, Hq), float("nan"), dtype=torch.float32, device=dev) if with_lse else None
+    pa.pa_hybrid_attention(out_c, dw.q[:T], dw.block_tables[:C],
+                           torch.from_numpy(w.cu_q_lens).to(dev),
+                           torch.from_numpy(w.q_start_pos).to(dev), dw.seq_lens[:C],
+                           int(np.max(np.diff(w.cu_q_lens))), out_d, dw.dq, dw.dtables, dw.dlens,
+                           dw.k_cache, dw.v_cache, w.scale, ws, chunk_sms=chunk_sms,
+                           chunk_lse=lse_c, decode_lse=lse_d)
+    return out_c, out_d, lse_c, lse_d
+
+
+def _hybrid_ws(pa, w, dev):
+    return pa.alloc_workspace(pa.pa_hybrid_workspace_size(
+        w.num_decode_seqs, w.num_q_heads, w.num_kv_heads, w.head_dim, w.max_blocks_per_seq), dev)
+
+
+@pytest.mark.parametrize("chunk_sms", [0, 1, 8, 32, 64, 151, 1000])
+def test_sarathi_hybrid_co_scheduled_matches_oracle(pa, cuda_device, chunk_sms):
+    """pa_hybrid_attention: the decode on the SMs the chunk does not take,
+    the chunk's tiles beside it; both match the oracle, and the chunk is bit
+    for bit the output of pa_prefill_chunk (the same tiles, one per CTA
+    instead of four per cluster)."""
+    w, ref_c, ref_c_lse, ref_d = _hybrid()
+    dw = DeviceWorkload(w, cuda_device)
+    dw.scatter(pa)
+    ws = _hybrid_ws(pa, w, cuda_device)
+    out_c, out_d, lse_c, lse_d = _hybrid_call(pa, dw, ws, chunk_sms)
+    alone, alone_lse = _prefill(pa, dw)
+    torch.cuda.synchronize()
+    assert_close(out_c, ref_c, f"co-scheduled chunk, chunk_sms {chunk_sms}")
+    assert_close(lse_c.cpu().numpy(), ref_c_lse, "co-scheduled chunk lse")
+    assert_close(out_d, ref_d, f"co-scheduled decode, chunk_sms {chunk_sms}")
+    assert torch.isfinite(lse_d).all()
+    assert torch.equal(out_c.view(torch.int16), alone.view(torch.int16))
+    assert torch.equal(lse_c, alone_lse)
+    assert pa.pa_device_error_flags() == 0
+
+
+def test_sarathi_hybrid_co_scheduled_repeats_and_leaves_workspace_zeroed(pa, cuda_device):
+    """Ten calls in a row on one workspace (the chunk's finish counter and the
+    decode's tickets reset themselves); every call gives the same bits."""
+    w, _, _, ref_d = _hybrid()
+    dw = DeviceWorkload(w, cuda_device)
+    dw.scatter(pa)
+    ws = _hybrid_ws(pa, w, cuda_device)
+    outs = [_hybrid_call(pa, dw, ws, 32, with_lse=False)[:2] for _ in range(10)]
+    torch.cuda.synchronize()
+    for c, d in outs[1:]:
+        assert torch.equal(c.view(torch.int16), outs[0][0].view(torch.int16))
+        assert torch.equal(d.view(torch.int16), outs[0][1].view(torch.int16))
+    assert_close(outs[-1][1], ref_d, "repeated co-scheduled decode")
+    assert int(ws[:256].count_nonzero()) == 0
+    assert pa.pa_device_error_flags() == 0
+
+
+def test_hybrid_without_chunks_or_decodes(pa, cuda_device):
+    """With no decode the call is the chunk alone; with no chunk, the decode
+    alone; both still match the oracle."""
+    w, ref_c, _, ref_d = _hybrid()
+    dw = DeviceWorkload(w, cuda_device)
+    dw.scatter(pa)
+    dev = cuda_device
+    ws = _hybrid_ws(pa, w, dev)
+    C = w.num_chunks
+    T = int(w.cu_q_lens[C])
+    S, Hq, D = w.num_decode_seqs, w.num_q_heads, w.head_dim
+    # no decodes
+    out_c = torch.empty((T, Hq, D), dtype=torch.bfloat16, device=dev)
+    none_d = torch.empty((0, Hq, D), dtype=torch.bfloat16, device=dev)
+    pa.pa_hybrid_attention(out_c, dw.q[:T], dw.block_tables[:C],
+                           torch.from_numpy(w.cu_q_lens).to(dev),
+                           torch.from_numpy(w.q_start_pos).to(dev), dw.seq_lens[:C],
+                           int(np.max(np.diff(w.cu_q_lens))), none_d, none_d,
+                           dw.dtables[:0], dw.dlens[:0], dw.k_cache, dw.v_cache, w.scale, ws)
+    # no chunks
+    out_d = torch.empty((S, Hq, D), dtype=torch.bfloat16, device=dev)
+    none_c = torch.empty((0, Hq, D), dtype=torch.bfloat16, device=dev)
+    zero = torch.zeros(1, dtype=torch.int32, device=dev)
+    pa.pa_hybrid_attention(none_c, none_c, dw.block_tables[:1], zero, zero[:0], zero[:0], 0,
+                           out_d, dw.dq, dw.dtables, dw.dlens, dw.k_cache, dw.v_cache, w.scale, ws)
+    torch.cuda.synchronize()
+    assert_close(out_c, ref_c, "hybrid call, chunk only")
+    assert_close(out_d, ref_d, "hybrid call, decode only")
+    assert pa.pa_device_error_flags() == 0
+
+
+def test_hybrid_rejects_bad_arguments_before_launching(pa, cuda_device):
+    w, _, _, _ = _hybrid()
+    dw = DeviceWorkload(w, cuda_device)
+    ws = _hybrid_ws(pa, w, cuda_device)
+    small = ws[:256]
+    with pytest.raises(pa.PAError) as e:
+        _hybrid_call(pa, dw, small)
+    assert e.value.status == pa.PA_ERR_WORKSPACE
+    with pytest.raises(pa.PAError) as e:
+        _hybrid_call(pa, dw, ws, chunk_sms=-1)
+    assert e.value.status == pa.PA_ERR_INVALID
+    torch.cuda.synchronize()
+    assert pa.pa_device_error_flags() == 0
