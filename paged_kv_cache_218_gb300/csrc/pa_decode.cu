@@ -98,7 +98,7 @@ __host__ __device__ inline Layout make_layout(int D, int Hkv, int Hq, int wph, i
 }
 
 __device__ __forceinline__ int load_len(const DecodeArgs& a, int s, bool report) {
-  int len = a.seq_lens[s];
+  int len = __ldcg(a.seq_lens + s);
   const int cap = a.max_blocks * kBlockSize;
   if (len < 0 || len > cap) {
     if (report) atomicOr(a.err, PA_DEVERR_SEQ_LEN);
@@ -111,7 +111,7 @@ __device__ __forceinline__ int load_len(const DecodeArgs& a, int s, bool report)
 // pass's start block (clamped to [0, ceil(len/16)]).
 __device__ __forceinline__ int start_block(const DecodeArgs& a, int s, int len, bool report) {
   if (!a.start_blocks) return 0;
-  int sb = a.start_blocks[s];
+  int sb = __ldcg(a.start_blocks + s);
   const int nb = (len + kBlockSize - 1) / kBlockSize;
   if (sb < 0) {
     if (report) atomicOr(a.err, PA_DEVERR_GROUP);
@@ -190,16 +190,26 @@ __device__ bool next_piece(const DecodeArgs& a, const int* pre, const int* lens_
   return false;
 }
 
-__device__ __forceinline__ int load_ids(const DecodeArgs& a, int s, int jb, int n, int lane) {
-  int id = 0;
-  if (lane < n) {
-    id = a.block_tables[static_cast<long long>(s) * a.max_blocks + jb + lane];
-    if (id < 0 || id >= a.num_blocks) {
-      atomicOr(a.err, PA_DEVERR_BLOCK_ID);
-      id = -1;  // the TMA box then lies outside the pool and reads zeros
-    }
+// Block ids jb .. jb+n-1 of sequence s, one per lane (read from L2: lengths
+// and tables are metadata a CTA may also read before its grid-dependency
+// wait, and a line cached in L1 then could be stale).  load_id_raw issues the
+// read; check_id flags a bad id and turns it into -1 (the TMA box then lies
+// outside the pool and reads zeros).
+__device__ __forceinline__ int load_id_raw(const DecodeArgs& a, int s, int jb, int n, int lane) {
+  return lane < n ? __ldcg(a.block_tables + static_cast<long long>(s) * a.max_blocks + jb + lane)
+                  : 0;
+}
+
+__device__ __forceinline__ int check_id(const DecodeArgs& a, int id, int n, int lane) {
+  if (lane < n && (id < 0 || id >= a.num_blocks)) {
+    atomicOr(a.err, PA_DEVERR_BLOCK_ID);
+    id = -1;
   }
   return id;
+}
+
+__device__ __forceinline__ int load_ids(const DecodeArgs& a, int s, int jb, int n, int lane) {
+  return check_id(a, load_id_raw(a, s, jb, n, lane), n, lane);
 }
 
 // Address of the 16-byte chunk `chunk` (8 bf16) of token row `tok` in one
@@ -539,47 +549,46 @@ __global__ void __launch_bounds__(kThreads, 1)
     warm(a.block_tables, static_cast<long long>(a.num_seqs) * a.max_blocks * 4);
     warm(a.q, static_cast<long long>(a.num_seqs) * Hq * D * 2);
   }
-  griddep_wait();
-  // The next kernel on the stream may start launching now: its CTAs take SMs
-  // as these exit, and it waits for this grid before it reads memory.
-  griddep_launch_dependents();
-
-  Cursor cur{};
-  const int* lens_c = nullptr;
-  if (a.mode == kModeBalanced) {
-    // exclusive prefix of block counts over sequences, computed by the
-    // producer warp alone (it needs it first); the consumers wait on a named
-    // barrier that the producer passes without waiting
-    const int S = a.num_seqs;
-    int* lens_w = S <= kLenCache ? pre + S + 1 : nullptr;
-    lens_c = lens_w;
-    if (warp == kConsumerWarps) {
-      const int per = (S + 31) / 32;
-      const int s0 = min(S, lane * per), s1 = min(S, s0 + per);
-      int local = 0;
-      for (int s = s0; s < s1; ++s) {
-        const int len = load_len(a, s, true);
-        if (lens_w) lens_w[s] = len;
-        local += (len + kBlockSize - 1) / kBlockSize - start_block(a, s, len, true);
-      }
-      int incl = local;
-#pragma unroll
-      for (int off = 1; off < 32; off <<= 1) {
-        const int v = __shfl_up_sync(0xffffffffu, incl, off);
-        if (lane >= off) incl += v;
-      }
-      int run = incl - local;
-      for (int s = s0; s < s1; ++s) {
-        pre[s] = run;
-        const int len = lens_w ? lens_w[s] : load_len(a, s, false);
-        run += (len + kBlockSize - 1) / kBlockSize - start_block(a, s, len, false);
-      }
-      if (lane == 31) pre[S] = incl;
-      __syncwarp();
-      asm volatile("bar.arrive 2, %0;" ::"n"(kThreads) : "memory");
-    } else {
-      asm volatile("bar.sync 2, %0;" ::"n"(kThreads) : "memory");
+  // ---- balanced mode: the plan (exclusive prefix of block counts over
+  // sequences, the CTA's range, its first piece and chunk), made by the
+  // producer warp.  For batches whose lengths fit in shared memory it is made
+  // before the grid-dependency wait, from lengths that the previous kernel
+  // could still be writing: after the wait the producer reads the first
+  // chunk's table row and, at the same time, the lengths and start blocks
+  // once more; the plan stands if they read the same, and is made again if
+  // not.  The first loads of the launch thus wait on one L2 round trip after
+  // the previous kernel, not on three.
+  const int S = a.num_seqs;
+  int* lens_w = (a.mode == kModeBalanced && S <= kLenCache) ? pre + S + 1 : nullptr;
+  const int* lens_c = lens_w;
+  const int per = (S + 31) / 32;
+  const int sl0 = min(S, lane * per), sl1 = min(S, sl0 + per);
+  // prefix over the sequences (producer warp; lane takes [sl0, sl1))
+  auto prefix = [&](bool report) {
+    int local = 0;
+    for (int s = sl0; s < sl1; ++s) {
+      const int len = load_len(a, s, report);
+      if (lens_w) lens_w[s] = len;
+      local += (len + kBlockSize - 1) / kBlockSize - start_block(a, s, len, report);
     }
+    int incl = local;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int v = __shfl_up_sync(0xffffffffu, incl, off);
+      if (lane >= off) incl += v;
+    }
+    int run = incl - local;
+    for (int s = sl0; s < sl1; ++s) {
+      pre[s] = run;
+      const int len = lens_w ? lens_w[s] : load_len(a, s, false);
+      run += (len + kBlockSize - 1) / kBlockSize - start_block(a, s, len, false);
+    }
+    if (lane == 31) pre[S] = incl;
+    __syncwarp();
+  };
+  Cursor cur{};
+  auto init_cursor = [&]() {
+    cur = Cursor{};
     cur.W = pre[S];
     cur.C = static_cast<int>(cur.W < gridDim.x ? cur.W : gridDim.x);
     if (static_cast<int>(blockIdx.x) < cur.C) {
@@ -601,6 +610,60 @@ __global__ void __launch_bounds__(kThreads, 1)
     cur.phase = cur.mid > cur.lo ? 0 : 1;
     cur.idx = cur.phase == 0 ? cur.mid : cur.lo;
     cur.end = cur.hi;
+  };
+  // the producer's walk: piece p, next block jbp of it, the first chunk
+  Piece p{};
+  int jbp = 0, c_s = 0, c_jb = 0, c_n = 0;
+  bool have_p = false, have_c = false;
+  auto first_chunk = [&]() {
+    have_p = next_piece(a, pre, lens_c, cur, p, false);
+    jbp = have_p ? p.j0 : 0;
+    have_c = have_p && jbp < p.j1;  // a balanced piece holds at least one block
+    if (have_c) {
+      c_s = p.s;
+      c_jb = jbp;
+      c_n = min(32, p.j1 - jbp);
+      jbp += c_n;
+    }
+  };
+  if (warp == kConsumerWarps && lens_w) {
+    prefix(false);
+    init_cursor();
+    first_chunk();
+  }
+
+  griddep_wait();
+  // The next kernel on the stream may start launching now: its CTAs take SMs
+  // as these exit, and it waits for this grid before it reads memory.
+  griddep_launch_dependents();
+
+  int ids_raw = 0;
+  if (a.mode == kModeBalanced) {
+    // the consumers wait on a named barrier that the producer passes without
+    // waiting
+    if (warp == kConsumerWarps) {
+      bool same = false;
+      if (lens_w) {
+        ids_raw = have_c ? load_id_raw(a, c_s, c_jb, c_n, lane) : 0;
+        same = true;
+        for (int s = sl0; s < sl1; ++s) {
+          const int len = load_len(a, s, true);
+          const int nb = (len + kBlockSize - 1) / kBlockSize - start_block(a, s, len, true);
+          same = same && len == lens_w[s] && nb == pre[s + 1] - pre[s];
+        }
+        same = __all_sync(0xffffffffu, same);
+      }
+      if (!same) {
+        prefix(true);
+        init_cursor();
+        first_chunk();
+        ids_raw = have_c ? load_id_raw(a, c_s, c_jb, c_n, lane) : 0;
+      }
+      asm volatile("bar.arrive 2, %0;" ::"n"(kThreads) : "memory");
+    } else {
+      asm volatile("bar.sync 2, %0;" ::"n"(kThreads) : "memory");
+      init_cursor();
+    }
   } else {
     cur.u = blockIdx.x;
     cur.U = static_cast<long long>(a.num_seqs) * a.max_parts;
@@ -616,7 +679,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t qrow_bytes = static_cast<uint32_t>(Hq) * D * 2;
     bool ok = true;
     // query rows of the piece's sequence into query slot qi & 1 (lane 0)
-    auto stage_q = [&](const Piece& p, int qi) {
+    auto stage_q = [&](const Piece& pp, int qi) {
       if (lane != 0 || !ok) return;
       const int k = qi & 1;
       if (qi >= 2 && !mbar_wait(bar_qempty + k * 8, ((qi >> 1) - 1) & 1)) {
@@ -632,16 +695,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t chunk = static_cast<uint32_t>(G) * D * 2;
       for (int h = 0; h < Hkv; ++h)
         bulk_load(sbase + L.q_off + k * L.q_bytes + h * chunk,
-                  a.q + static_cast<long long>(p.s) * Hq * D + h * G * D, chunk,
+                  a.q + static_cast<long long>(pp.s) * Hq * D + h * G * D, chunk,
                   bar_qfull + k * 8);
     };
-    Piece p{};
-    int qi = 0, jbp = 0;
-    bool have_p = next_piece(a, pre, lens_c, cur, p, false);
-    if (have_p) {
-      stage_q(p, qi++);
-      jbp = p.j0;
+    int qi = 0;
+    if (a.mode != kModeBalanced) {
+      have_p = next_piece(a, pre, lens_c, cur, p, false);
+      jbp = have_p ? p.j0 : 0;
     }
+    if (have_p) stage_q(p, qi++);
     // next chunk of up to 32 blocks, staging the queries of every piece reached
     auto next_chunk2 = [&](int& s, int& jb, int& n) -> bool {
       while (have_p) {
@@ -659,9 +721,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       return false;
     };
-    int s, jb, n;
-    bool have = next_chunk2(s, jb, n);
-    int ids = have ? load_ids(a, s, jb, n, lane) : 0;
+    int s, jb, n, ids;
+    bool have;
+    if (a.mode == kModeBalanced) {
+      have = have_c;
+      s = c_s;
+      jb = c_jb;
+      n = c_n;
+      ids = have ? check_id(a, ids_raw, n, lane) : 0;
+    } else {
+      have = next_chunk2(s, jb, n);
+      ids = have ? load_ids(a, s, jb, n, lane) : 0;
+    }
     uint32_t g = 0;
     ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
     while (have && ok) {

@@ -313,3 +313,44 @@ def test_decode_is_bitwise_deterministic_on_one_block_pieces(pa, cuda_device, pa
     torch.cuda.synchronize()
     for o in outs[1:]:
         assert torch.equal(o.view(torch.int16), outs[0].view(torch.int16))
+
+
+def test_decode_lengths_written_by_the_previous_kernel(pa, cuda_device):
+    """The balanced decode plans its split from the lengths before it waits on
+    the previous kernel, then checks them again; here the previous kernel on
+    the stream (a scatter, launched as the decode's programmatic primary)
+    writes new lengths into the very buffer the decode reads them from.
+    Every decode must follow the new lengths."""
+    w = W.decode_batch(64, 1, 900, 32, 8, 128, seed=41)
+    dw = DeviceWorkload(w, cuda_device)
+    dw.scatter(pa)
+    S, Hq, D = w.num_decode_seqs, w.num_q_heads, w.head_dim
+    kc, vc = oracle_scattered(w)
+    rng = np.random.default_rng(5)
+    full = w.seq_lens.astype(np.int32)  # the tables hold blocks up to these lengths
+    lens_sets = [full, rng.integers(1, full + 1).astype(np.int32),
+                 np.maximum(1, full // 3).astype(np.int32)]
+    refs = [oracle.decode(w.q, kc, vc, w.block_tables, ls, w.scale)[0] for ls in lens_sets]
+    # the lengths live in a scatter destination: 16-byte slots of a pool with
+    # one kv head of 8 columns, so slot j holds lengths 4j .. 4j+3
+    nslot = S // 4
+    meta_k = torch.zeros((nslot // 16 + 1, 16, 1, 8), dtype=torch.bfloat16, device=cuda_device)
+    meta_v = torch.zeros_like(meta_k)
+    lens_dev = meta_k.view(torch.int32).view(-1)[:S]
+    rows = [torch.from_numpy(ls.view(np.int16).reshape(nslot, 1, 8).copy()).view(torch.bfloat16)
+            .to(cuda_device) for ls in lens_sets]
+    slots = torch.arange(nslot, dtype=torch.int64, device=cuda_device)
+    ws = pa.alloc_workspace(pa.pa_decode_workspace_size(S, Hq, 8, D, w.max_blocks_per_seq, 16, 0),
+                            cuda_device)
+    outs = []
+    for i in range(24):
+        k = i % 3
+        pa.pa_reshape_and_cache(rows[k], rows[k], meta_k, meta_v, slots)
+        out = torch.empty((S, Hq, D), dtype=torch.bfloat16, device=cuda_device)
+        pa.pa_decode(out, dw.dq, dw.k_cache, dw.v_cache, dw.dtables, lens_dev, w.scale,
+                     partition_tokens=0, workspace=ws)
+        outs.append((k, out))
+    torch.cuda.synchronize()
+    for k, out in outs:
+        assert_close(out, refs[k], f"lengths set {k}")
+    assert pa.pa_device_error_flags() == 0
