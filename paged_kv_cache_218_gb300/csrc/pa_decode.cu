@@ -228,24 +228,28 @@ __device__ __forceinline__ void attend_block(uint32_t kbase, uint32_t vbase, uin
                                              int lane) {
   constexpr int KS = D / 16;
   const int i = lane >> 3, r = lane & 7;
-  // two independent accumulation chains halve the dependent MMA latency
-  float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb[4] = {0.f, 0.f, 0.f, 0.f};
+  // four independent accumulation chains of KS/4 k-steps each cut the
+  // dependent MMA latency
+  float sc[4][4];
+#pragma unroll
+  for (int c = 0; c < 4; ++c) sc[c][0] = sc[c][1] = sc[c][2] = sc[c][3] = 0.f;
   const int ktok = r + ((i & 1) << 3);
 #pragma unroll
   for (int ks = 0; ks < KS; ks += 2) {
     uint32_t a0[4], a1[4];
     ldsm_x4(swz(kbase, ktok, ks * 2 + (i >> 1), half), a0);
     ldsm_x4(swz(kbase, ktok, (ks + 1) * 2 + (i >> 1), half), a1);
-    mma_bf16_16816(sa, a0, qf[ks][0], qf[ks][1]);
-    mma_bf16_16816(sb, a1, qf[ks + 1][0], qf[ks + 1][1]);
+    mma_bf16_16816(sc[ks & 3], a0, qf[ks][0], qf[ks][1]);
+    mma_bf16_16816(sc[(ks + 1) & 3], a1, qf[ks + 1][0], qf[ks + 1][1]);
   }
   // S^T: [token lane/4][heads 2q, 2q+1], [token lane/4 + 8][same heads]
   const int t0 = lane >> 2;
   const bool v0 = t0 < valid, v1 = t0 + 8 < valid;
-  const float x0 = v0 ? (sa[0] + sb[0]) * scale_log2 : -INFINITY;
-  const float x1 = v0 ? (sa[1] + sb[1]) * scale_log2 : -INFINITY;
-  const float x2 = v1 ? (sa[2] + sb[2]) * scale_log2 : -INFINITY;
-  const float x3 = v1 ? (sa[3] + sb[3]) * scale_log2 : -INFINITY;
+  auto score = [&](int e) { return (sc[0][e] + sc[1][e]) + (sc[2][e] + sc[3][e]); };
+  const float x0 = v0 ? score(0) * scale_log2 : -INFINITY;
+  const float x1 = v0 ? score(1) * scale_log2 : -INFINITY;
+  const float x2 = v1 ? score(2) * scale_log2 : -INFINITY;
+  const float x3 = v1 ? score(3) * scale_log2 : -INFINITY;
   float mxa = fmaxf(x0, x2), mxb = fmaxf(x1, x3);
 #pragma unroll
   for (int off = 4; off < 32; off <<= 1) {
@@ -327,7 +331,22 @@ __device__ __forceinline__ void attend_block_fp8(uint32_t kbase, uint32_t vbase,
       kw[r][4 * h + 3] = v.w;
     }
   }
-  float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb[4] = {0.f, 0.f, 0.f, 0.f};
+  // the V bytes are read now, so that their latency hides under the scores
+  uint32_t vw[4][4];
+#pragma unroll
+  for (int r = 0; r < 4; ++r) {
+    const int tok = 2 * c + (r & 1) + 8 * (r >> 1);
+    const uint4 v = lds128(vbase + tok * 128 + ((g ^ (tok & 7)) << 4));
+    vw[r][0] = v.x;
+    vw[r][1] = v.y;
+    vw[r][2] = v.z;
+    vw[r][3] = v.w;
+  }
+  // four independent MMA chains of two k-steps each (short dependency chains:
+  // this path is bound by the latency of a consumer warp's work per block)
+  float sc[4][4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) sc[i][0] = sc[i][1] = sc[i][2] = sc[i][3] = 0.f;
 #pragma unroll
   for (int ks = 0; ks < KS; ++ks) {
     uint32_t ka[4];
@@ -335,17 +354,14 @@ __device__ __forceinline__ void attend_block_fp8(uint32_t kbase, uint32_t vbase,
     ka[1] = e4m3x2_to_f16x2(kw[1][ks]);
     ka[2] = e4m3x2_to_f16x2(kw[0][ks] >> 16);
     ka[3] = e4m3x2_to_f16x2(kw[1][ks] >> 16);
-    if (ks & 1)
-      mma_f16_16816(sb, ka, qf[ks][0], qf[ks][1]);
-    else
-      mma_f16_16816(sa, ka, qf[ks][0], qf[ks][1]);
+    mma_f16_16816(sc[ks & 3], ka, qf[ks][0], qf[ks][1]);
   }
   const int t0 = lane >> 2;
   const bool v0 = t0 < valid, v1 = t0 + 8 < valid;
-  const float x0 = v0 ? (sa[0] + sb[0]) * sl2 : -INFINITY;
-  const float x1 = v0 ? (sa[1] + sb[1]) * sl2 : -INFINITY;
-  const float x2 = v1 ? (sa[2] + sb[2]) * sl2 : -INFINITY;
-  const float x3 = v1 ? (sa[3] + sb[3]) * sl2 : -INFINITY;
+  const float x0 = v0 ? ((sc[0][0] + sc[1][0]) + (sc[2][0] + sc[3][0])) * sl2 : -INFINITY;
+  const float x1 = v0 ? ((sc[0][1] + sc[1][1]) + (sc[2][1] + sc[3][1])) * sl2 : -INFINITY;
+  const float x2 = v1 ? ((sc[0][2] + sc[1][2]) + (sc[2][2] + sc[3][2])) * sl2 : -INFINITY;
+  const float x3 = v1 ? ((sc[0][3] + sc[1][3]) + (sc[2][3] + sc[3][3])) * sl2 : -INFINITY;
   float mxa = fmaxf(x0, x2), mxb = fmaxf(x1, x3);
 #pragma unroll
   for (int off = 4; off < 32; off <<= 1) {
@@ -374,16 +390,6 @@ __device__ __forceinline__ void attend_block_fp8(uint32_t kbase, uint32_t vbase,
     const int q2 = c * 2;
     keep01 = (q2 < valid ? 0x0000ffffu : 0u) | (q2 + 1 < valid ? 0xffff0000u : 0u);
     keep23 = (q2 + 8 < valid ? 0x0000ffffu : 0u) | (q2 + 9 < valid ? 0xffff0000u : 0u);
-  }
-  uint32_t vw[4][4];
-#pragma unroll
-  for (int r = 0; r < 4; ++r) {
-    const int tok = 2 * c + (r & 1) + 8 * (r >> 1);
-    const uint4 v = lds128(vbase + tok * 128 + ((g ^ (tok & 7)) << 4));
-    vw[r][0] = v.x;
-    vw[r][1] = v.y;
-    vw[r][2] = v.z;
-    vw[r][3] = v.w;
   }
 #pragma unroll
   for (int mt = 0; mt < KS; ++mt) {
