@@ -47,6 +47,9 @@ CONFIG_TEXT = {
     "sarathi_hybrid": "Sarathi hybrid batch: prefill chunk of 512 queries at positions "
                       "1536-2047 + 128 decodes with seq_lens U[256,4096], 32 q / 8 kv heads, "
                       "head_dim 128, token budget 640",
+    "shared_prompt_batch": "shared system prompt: 128 seqs in 16 groups of 8, each group aliasing "
+                           "one 2048-token prompt, private suffixes lognormal(median 256, sigma 1), "
+                           "32 q / 8 kv heads, head_dim 128",
 }
 
 
@@ -154,7 +157,8 @@ def reduce_over_ranks(elapsed_ms, units, device=None):
 def make_workload(name):
     from paged_kv_cache_218_gb300 import workload as W
     return {"llama3_8b_decode_layer": W.llama3_8b_layer, "long_context_split_kv": W.long_context_split,
-            "cow_prefix_mix": W.cow_mix, "sarathi_hybrid": W.sarathi_hybrid}[name]()
+            "cow_prefix_mix": W.cow_mix, "sarathi_hybrid": W.sarathi_hybrid,
+            "shared_prompt_batch": W.shared_prompt_batch}[name]()
 
 
 class Replica:
@@ -383,8 +387,8 @@ def run_gpu(args, rank, world, local_rank):
     e2e = run_e2e(args, w, reps, ws, dev, pa, dist, s_chunk, max_q, T, hws)
     fp8 = measure_fp8_decode(args, w, reps, ws, dev, pa) if (use_graphs and w.head_dim == 128) \
         else None
-    casc = measure_cascade(args, w, reps, dev, pa) if (use_graphs and args.config == "cow_prefix_mix") \
-        else None
+    casc = measure_cascade(args, w, reps, dev, pa, CASCADE_GROUP[args.config]) \
+        if (use_graphs and args.config in CASCADE_GROUP) else None
     return dict(w=w, elapsed_ms=elapsed_ms, kv_all=kv_all, dec_ms=dec_ms, chunk_ms=chunk_ms,
                 clocks=clocks, e2e=e2e, launches=launches_per_step * K, graphs=use_graphs,
                 fp8=fp8, cascade=casc)
@@ -445,10 +449,14 @@ def measure_fp8_decode(args, w, reps, ws, dev, pa):
             "scales": "per kv head, max |x| / 448"}
 
 
-def measure_cascade(args, w, reps, dev, pa, group=4):
-    """Cascade decode of the copy-on-write mix (each group's shared prefix
-    attended once for its members, then each suffix): two launches per call,
-    timed like the plain decode over back-to-back calls from graphs of R."""
+# batches whose consecutive sequences share prefix blocks, and their group size
+CASCADE_GROUP = {"cow_prefix_mix": 4, "shared_prompt_batch": 8}
+
+
+def measure_cascade(args, w, reps, dev, pa, group):
+    """Cascade decode of a batch with shared prefixes (each group's shared
+    prefix attended once for its members, then each suffix): two launches per
+    call, timed like the plain decode over back-to-back calls from graphs of R."""
     import torch
 
     from paged_kv_cache_218_gb300 import workload as W

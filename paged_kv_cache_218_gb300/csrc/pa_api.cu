@@ -636,16 +636,22 @@ int pa_decode_fp8(void* out, const void* q, const void* k_cache, const void* v_c
                      workspace_bytes, stream);
 }
 
-static size_t cascade_prefix_bytes(int num_seqs, int Hq) {
-  return (static_cast<size_t>(num_seqs) * Hq * 128 * 4 + 255) / 256 * 256 +
-         (static_cast<size_t>(num_seqs) * Hq * 4 + 255) / 256 * 256;
+// Cascade workspace before the decode's: the prefix result (o [S, Hq, 128],
+// lse [S, Hq]), the partials of prefix parts 1.. (same shapes, each), and one
+// ticket per (group, kv-head subset) -- at most S * Hkv of them.
+static size_t round256(size_t b) { return (b + 255) / 256 * 256; }
+
+static size_t cascade_prefix_bytes(int num_seqs, int Hq, int Hkv) {
+  const size_t o = round256(static_cast<size_t>(num_seqs) * Hq * 128 * 4);
+  const size_t l = round256(static_cast<size_t>(num_seqs) * Hq * 4);
+  return (o + l) * kMaxPrefixParts + round256(static_cast<size_t>(num_seqs) * Hkv * 4);
 }
 
 size_t pa_cascade_workspace_size(int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
                                  int max_blocks_per_seq, int block_size, int partition_tokens) {
   if (head_dim != 128 || num_seqs < 0) return 0;
   if (check_shape(num_q_heads, num_kv_heads, head_dim, block_size) != PA_OK) return 0;
-  return cascade_prefix_bytes(num_seqs, num_q_heads) +
+  return cascade_prefix_bytes(num_seqs, num_q_heads, num_kv_heads) +
          pa_decode_workspace_size(num_seqs, num_q_heads, num_kv_heads, head_dim,
                                   max_blocks_per_seq, block_size, partition_tokens);
 }
@@ -674,16 +680,21 @@ int pa_cascade_decode(void* out, const void* q, const void* k_cache, const void*
   if (!cascade_shape(num_kv_heads, num_q_heads / num_kv_heads, max_group_size, &c.kv_per_cta,
                      &c.warps_per_kv, &c.stages))
     return PA_ERR_UNSUPPORTED;
-  const size_t pre = cascade_prefix_bytes(num_seqs, num_q_heads);
+  const size_t pre = cascade_prefix_bytes(num_seqs, num_q_heads, num_kv_heads);
   if (!workspace || workspace_bytes < pre || !aligned(workspace, 256)) return PA_ERR_WORKSPACE;
   if (!out || !q || !k_cache || !v_cache || !block_tables || !seq_lens) return PA_ERR_INVALID;
   if (!aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16)) return PA_ERR_INVALID;
   DeviceInfo* d;
   if (int rc = current_device_info(&d)) return rc;
-  float* pre_o = static_cast<float*>(workspace);
-  float* pre_lse = reinterpret_cast<float*>(
-      static_cast<char*>(workspace) +
-      (static_cast<size_t>(num_seqs) * num_q_heads * 128 * 4 + 255) / 256 * 256);
+  char* wsb = static_cast<char*>(workspace);
+  const size_t o_bytes = round256(static_cast<size_t>(num_seqs) * num_q_heads * 128 * 4);
+  const size_t l_bytes = round256(static_cast<size_t>(num_seqs) * num_q_heads * 4);
+  float* pre_o = reinterpret_cast<float*>(wsb);
+  float* pre_lse = reinterpret_cast<float*>(wsb + o_bytes);
+  float* part_o = reinterpret_cast<float*>(wsb + o_bytes + l_bytes);
+  float* part_lse = reinterpret_cast<float*>(wsb + o_bytes + l_bytes +
+                                             (kMaxPrefixParts - 1) * o_bytes);
+  int* tickets = reinterpret_cast<int*>(wsb + (o_bytes + l_bytes) * kMaxPrefixParts);
   if (num_groups > 0) {
     c.q = static_cast<const __nv_bfloat16*>(q);
     c.seq_lens = seq_lens;
@@ -702,6 +713,16 @@ int pa_cascade_decode(void* out, const void* q, const void* k_cache, const void*
     c.num_kv_heads = num_kv_heads;
     c.group = num_q_heads / num_kv_heads;
     c.scale_log2 = scale * 1.4426950408889634f;
+    // too few (group, subset) units to fill the GPU: split each prefix over
+    // up to kMaxPrefixParts CTAs
+    const int units = num_groups * (num_kv_heads / c.kv_per_cta);
+    c.parts = units >= d->num_sms ? 1 : d->num_sms / units;
+    c.parts = c.parts < 1 ? 1 : (c.parts > kMaxPrefixParts ? kMaxPrefixParts : c.parts);
+    if (static_cast<int64_t>(units) > static_cast<int64_t>(num_seqs) * num_kv_heads)
+      c.parts = 1;  // more units than ticket slots: no split
+    c.part_o = part_o;
+    c.part_lse = part_lse;
+    c.tickets = tickets;
     CUtensorMap tk, tv;
     if (encode_pool_map(&tk, k_cache, num_blocks, num_kv_heads, head_dim, -c.kv_per_cta) ||
         encode_pool_map(&tv, v_cache, num_blocks, num_kv_heads, head_dim, -c.kv_per_cta))

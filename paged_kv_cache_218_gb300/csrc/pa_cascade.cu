@@ -8,8 +8,11 @@
 // suffix pass is the paged decode started from this pass's result
 // (DecodeArgs::init_o / init_lse), which is the log-sum-exp merge.
 //
-// One CTA per (group, subset of kv heads): the producer warp streams the
-// group's prefix blocks once -- per block one TMA box per 64-column half and
+// One CTA per (group, subset of kv heads) -- or, when there are too few of
+// those to fill the GPU, a few CTAs each taking an equal share of the
+// prefix's blocks, whose partial results the last of them to finish merges
+// by log-sum-exp.  The producer warp streams the CTA's prefix blocks once --
+// per block one TMA box per 64-column half and
 // pool covering 16 tokens x the subset's kv heads -- and every consumer warp
 // uses each block for 16 query rows, a row being one (member, q head) pair of
 // one kv head.  So a prefix byte read from HBM serves every member.
@@ -68,7 +71,8 @@ __global__ void __launch_bounds__(kCThreads, 1)
   const int KH = a.kv_per_cta, G = a.group, Mmax = a.max_group, wpk = a.warps_per_kv;
   const int Hq = a.num_q_heads;
   const int nsub = a.num_kv_heads / KH;
-  const int grp = blockIdx.x / nsub, hs = blockIdx.x % nsub;
+  const int part = blockIdx.x % a.parts, unit = blockIdx.x / a.parts;
+  const int grp = unit / nsub, hs = unit % nsub;
   const int NS = a.stages;
   const CLayout L = cascade_layout(KH, Mmax, G, NS);
   const uint32_t bar_full = sbase + L.bar_off;
@@ -117,6 +121,8 @@ __global__ void __launch_bounds__(kCThreads, 1)
   }
   __syncthreads();
   const int nbp = misc[1], M = misc[2], s0 = misc[3], lmax = misc[4];
+  // this CTA's share of the prefix blocks
+  const int j_lo = part * nbp / a.parts, j_hi = (part + 1) * nbp / a.parts;
   volatile int* abort_flag = misc;
 
   if (warp == kCW) {
@@ -134,8 +140,8 @@ __global__ void __launch_bounds__(kCThreads, 1)
                     G * 256, bar_q);
     }
     const uint64_t pol = l2_policy_evict_first();
-    for (int jb = 0; jb < nbp && ok; jb += 32) {
-      const int n = min(32, nbp - jb);
+    for (int jb = j_lo; jb < j_hi && ok; jb += 32) {
+      const int n = min(32, j_hi - jb);
       int id = 0;
       if (lane < n) {
         id = a.prefix_tables[static_cast<long long>(grp) * a.max_prefix_blocks + jb + lane];
@@ -146,10 +152,10 @@ __global__ void __launch_bounds__(kCThreads, 1)
       }
       for (int i = 0; i < n && ok; ++i) {
         const int blk = __shfl_sync(0xffffffffu, id, i);
-        const int j = jb + i;
-        const int st = j % NS;
+        const int jj = jb + i - j_lo;  // place in this CTA's stream
+        const int st = jj % NS;
         if (lane == 0) {
-          if (j >= NS && !mbar_wait(bar_empty + st * 8, ((j / NS) - 1) & 1)) {
+          if (jj >= NS && !mbar_wait(bar_empty + st * 8, ((jj / NS) - 1) & 1)) {
             atomicOr(a.err, PA_DEVERR_TIMEOUT);
             ok = false;
           } else {
@@ -206,10 +212,10 @@ __global__ void __launch_bounds__(kCThreads, 1)
   const float sl2 = a.scale_log2;
   const uint32_t half = KH * kHeadBox;
 
-  for (int j = 0; j < nbp; ++j) {
-    const int st = j % NS;
+  for (int j = j_lo; j < j_hi; ++j) {
+    const int st = (j - j_lo) % NS;
     if (warp_flag(abort_flag)) break;
-    if (!mbar_wait_warp(bar_full + st * 8, (j / NS) & 1)) {
+    if (!mbar_wait_warp(bar_full + st * 8, ((j - j_lo) / NS) & 1)) {
       if (lane == 0) atomicOr(a.err, PA_DEVERR_TIMEOUT);
       *abort_flag = 1;
       break;
@@ -309,25 +315,79 @@ __global__ void __launch_bounds__(kCThreads, 1)
     lA += __shfl_xor_sync(0xffffffffu, lA, off);
     lB += __shfl_xor_sync(0xffffffffu, lB, off);
   }
-  if (!active) return;
-  const float ia = lA > 0.f ? 1.f / lA : 0.f, ib = lB > 0.f ? 1.f / lB : 0.f;
-  const int kvg = hs * KH + kh;
-  if (ma < M) {
-    const long long row = static_cast<long long>(s0 + ma) * Hq + kvg * G + (Ra % G);
+  // part 0 writes into the prefix result itself, the others into their own
+  // partial buffers (a row without a visible token gets o = 0, lse = -inf)
+  const size_t rows_all = static_cast<size_t>(a.num_seqs) * Hq;
+  float* dst_o = part == 0 ? a.pre_o : a.part_o + (part - 1) * rows_all * 128;
+  float* dst_l = part == 0 ? a.pre_lse : a.part_lse + (part - 1) * rows_all;
+  if (active) {
+    const float ia = lA > 0.f ? 1.f / lA : 0.f, ib = lB > 0.f ? 1.f / lB : 0.f;
+    const int kvg = hs * KH + kh;
+    if (ma < M) {
+      const long long row = static_cast<long long>(s0 + ma) * Hq + kvg * G + (Ra % G);
 #pragma unroll
-    for (int nd = 0; nd < 16; ++nd)
-      *reinterpret_cast<float2*>(a.pre_o + row * 128 + nd * 8 + 2 * c) =
-          make_float2(o[nd][0] * ia, o[nd][1] * ia);
-    if (c == 0) a.pre_lse[row] = lA > 0.f ? (mA + __log2f(lA)) * kLn2C : -INFINITY;
-  }
-  if (mb < M) {
-    const long long row = static_cast<long long>(s0 + mb) * Hq + kvg * G + (Rb % G);
+      for (int nd = 0; nd < 16; ++nd)
+        *reinterpret_cast<float2*>(dst_o + row * 128 + nd * 8 + 2 * c) =
+            make_float2(o[nd][0] * ia, o[nd][1] * ia);
+      if (c == 0) dst_l[row] = lA > 0.f ? (mA + __log2f(lA)) * kLn2C : -INFINITY;
+    }
+    if (mb < M) {
+      const long long row = static_cast<long long>(s0 + mb) * Hq + kvg * G + (Rb % G);
 #pragma unroll
-    for (int nd = 0; nd < 16; ++nd)
-      *reinterpret_cast<float2*>(a.pre_o + row * 128 + nd * 8 + 2 * c) =
-          make_float2(o[nd][2] * ib, o[nd][3] * ib);
-    if (c == 0) a.pre_lse[row] = lB > 0.f ? (mB + __log2f(lB)) * kLn2C : -INFINITY;
+      for (int nd = 0; nd < 16; ++nd)
+        *reinterpret_cast<float2*>(dst_o + row * 128 + nd * 8 + 2 * c) =
+            make_float2(o[nd][2] * ib, o[nd][3] * ib);
+      if (c == 0) dst_l[row] = lB > 0.f ? (mB + __log2f(lB)) * kLn2C : -INFINITY;
+    }
   }
+  if (a.parts == 1) return;
+  // ---- the last part of this (group, subset) to finish merges all parts of
+  // its rows by log-sum-exp, in part order, into the prefix result
+  const int ctid = tid;
+  named_barrier(1, kCW * 32);
+  if (ctid == 0) misc[5] = atom_add_acq_rel_gpu(a.tickets + unit, 1);
+  named_barrier(1, kCW * 32);
+  if (misc[5] != a.parts - 1) return;
+  const int rows = M * KH * G;  // member-major: (m, kv head of the subset, q head)
+  for (int e = ctid; e < rows * 32; e += kCW * 32) {
+    const int r = e >> 5, f4 = e & 31;
+    const int m = r / (KH * G), h = (r / G) % KH, gq = r % G;
+    const long long row = static_cast<long long>(s0 + m) * Hq + (hs * KH + h) * G + gq;
+    float lse[kMaxPrefixParts];
+    float4 ov[kMaxPrefixParts];
+    float L = -INFINITY;
+#pragma unroll
+    for (int p = 0; p < kMaxPrefixParts; ++p) {
+      if (p < a.parts) {
+        const float* po = p == 0 ? a.pre_o : a.part_o + (p - 1) * rows_all * 128;
+        const float* pl = p == 0 ? a.pre_lse : a.part_lse + (p - 1) * rows_all;
+        lse[p] = __ldcg(pl + row);
+        ov[p] = __ldcg(reinterpret_cast<const float4*>(po + row * 128) + f4);
+        L = fmaxf(L, lse[p]);
+      }
+    }
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    float wsum = 0.f;
+    if (L > -INFINITY) {
+#pragma unroll
+      for (int p = 0; p < kMaxPrefixParts; ++p) {
+        if (p < a.parts) {
+          const float w = __expf(lse[p] - L);
+          acc.x += w * ov[p].x;
+          acc.y += w * ov[p].y;
+          acc.z += w * ov[p].z;
+          acc.w += w * ov[p].w;
+          wsum += w;
+        }
+      }
+    }
+    const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
+    __syncwarp();  // a warp holds one row: every lane has read part 0's lse
+    reinterpret_cast<float4*>(a.pre_o + row * 128)[f4] =
+        make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
+    if (f4 == 0) a.pre_lse[row] = wsum > 0.f ? L + __logf(wsum) : -INFINITY;
+  }
+  if (ctid == 0) a.tickets[unit] = 0;
 }
 
 }  // namespace
@@ -368,7 +428,8 @@ cudaError_t launch_cascade_prefix(const CascadeArgs& a, const CUtensorMap* tm_k,
     }
   }
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(static_cast<unsigned>(a.num_groups * (a.num_kv_heads / a.kv_per_cta)));
+  cfg.gridDim = dim3(static_cast<unsigned>(a.num_groups * (a.num_kv_heads / a.kv_per_cta) *
+                                          a.parts));
   cfg.blockDim = dim3(kCThreads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;

@@ -111,8 +111,14 @@ struct CascadeArgs {
   int kv_per_cta;   // kv heads per CTA
   int warps_per_kv; // consumer warps per kv head (16 query rows each)
   int stages;       // K/V ring depth
+  int parts;        // CTAs that split one (group, kv-head subset)'s prefix blocks
+  float* part_o;    // parts > 1: partials of parts 1.. [parts - 1][S, Hq, 128]
+  float* part_lse;  // parts > 1: [parts - 1][S, Hq]
+  int* tickets;     // parts > 1: [num_groups * subsets] (self-resetting)
   float scale_log2;
 };
+
+constexpr int kMaxPrefixParts = 4;  // cascade: most CTAs per (group, kv-head subset)
 
 // Balanced-mode workspace layout (shared by the size query and the launch):
 // per-CTA merge tickets, then two partial slots per CTA of Hq*(D+1) floats.

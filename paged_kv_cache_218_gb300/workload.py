@@ -255,11 +255,12 @@ def long_context_split(seed: int = 1003, poison: bool = False,
 
 def cow_mix(seed: int = 1004, poison: bool = False, num_seqs: int = 256,
             group: int = 4, prefix_tokens: int = 256, Hq: int = 64, Hkv: int = 8,
-            D: int = 128, max_len: int = 8192) -> Workload:
+            D: int = 128, max_len: int = 8192, median: float = 512.0, len_offset: int = 0,
+            name: str = "cow_prefix_mix") -> Workload:
     """Continuous-batching mix with copy-on-write prefix sharing.
 
-    Lengths lognormal(median 512, sigma 1), rounded half-to-even and clipped to
-    [1, max_len].  Consecutive groups of ``group`` sequences alias the same
+    Lengths ``len_offset`` + lognormal(median ``median``, sigma 1), rounded
+    half-to-even and clipped to [1, max_len].  Consecutive groups of ``group`` sequences alias the same
     physical prefix blocks (``prefix_tokens`` tokens); a shared block's
     refcount is the number of members that reference it.  A member whose new
     token lands in a shared block with refcount > 1 first receives a private
@@ -268,7 +269,7 @@ def cow_mix(seed: int = 1004, poison: bool = False, num_seqs: int = 256,
     rng = np.random.default_rng(seed)
     bs = BLOCK_SIZE
     z = rng.standard_normal(num_seqs)
-    lens = np.clip(np.rint(np.exp(math.log(512.0) + z)), 1, max_len).astype(np.int32)
+    lens = np.clip(len_offset + np.rint(np.exp(math.log(median) + z)), 1, max_len).astype(np.int32)
     max_blocks = _blocks_for(max_len)
     pb = prefix_tokens // bs
     # logical block lists: ('shared', group, j) or ('private', seq, j)
@@ -314,7 +315,7 @@ def cow_mix(seed: int = 1004, poison: bool = False, num_seqs: int = 256,
         refcount[phys[key]] = r
     cow_pairs = np.array([(phys[shared], phys[("cow", s, j)]) for s, j, shared in cow],
                          dtype=np.int64).reshape(-1, 2)
-    w = _finish("cow_prefix_mix", seed, rng, lens, bt, nb, refcount, Hq, Hkv, D,
+    w = _finish(name, seed, rng, lens, bt, nb, refcount, Hq, Hkv, D,
                 1.0 / math.sqrt(D), False, cow_pairs=cow_pairs)
     if poison:
         # poison what no sequence reads, judged on the post-copy tables.  A
@@ -335,6 +336,18 @@ def cow_mix(seed: int = 1004, poison: bool = False, num_seqs: int = 256,
             w.k_cache[dst] = BF16_NAN
             w.v_cache[dst] = BF16_NAN
     return w
+
+
+def shared_prompt_batch(seed: int = 1006, poison: bool = False) -> Workload:
+    """A long system prompt shared by groups of requests (the case cascade
+    attention is for): 128 sequences in 16 groups of 8, each group aliasing one
+    2048-token prompt (128 blocks) followed by a private suffix of
+    lognormal(median 256, sigma 1) tokens; Llama-3-8B heads (32 q / 8 kv,
+    head_dim 128).  No member writes into the shared prompt, so there are no
+    copy-on-write pairs."""
+    return cow_mix(seed=seed, poison=poison, num_seqs=128, group=8, prefix_tokens=2048, Hq=32,
+                   Hkv=8, D=128, max_len=8192, median=256.0, len_offset=2048,
+                   name="shared_prompt_batch")
 
 
 def sarathi_hybrid(seed: int = 1005, poison: bool = False, chunk_tokens: int = 512,
@@ -422,6 +435,7 @@ CONFIGS = {
     "long_context_split_kv": long_context_split,
     "cow_prefix_mix": cow_mix,
     "sarathi_hybrid": sarathi_hybrid,
+    "shared_prompt_batch": shared_prompt_batch,
 }
 
 

@@ -52,6 +52,14 @@ def test_cascade_cow_mix_full_size(pa, cuda_device, partition):
     assert sb.max() == 16 and (sb == 16).sum() > 150
 
 
+@pytest.mark.parametrize("partition", [0, -1])
+def test_cascade_shared_prompt_batch_full_size(pa, cuda_device, partition):
+    """Groups of 8 sharing a 2048-token prompt (32 member x head rows per kv
+    head, the most one prefix CTA takes), at full size."""
+    go, pt, sb = run(pa, cuda_device, W.shared_prompt_batch(), 8, partition)
+    assert (sb == 128).all()
+
+
 SHAPES = [  # num_seqs, group, prefix_tokens, Hq, Hkv, max_len
     (40, 8, 512, 32, 8, 2048),   # 8 members x group 4 = 32 rows
     (30, 3, 96, 16, 2, 600),     # 24 rows, two kv heads

@@ -80,6 +80,23 @@ def test_cow_mix_aliasing_and_refcounts():
         assert w.refcount[dst] == 1 and w.refcount[src] >= 1
 
 
+def test_shared_prompt_batch_groups_share_exactly_the_prompt():
+    w = W.shared_prompt_batch()
+    assert len(w.seq_lens) == 128 and w.seq_lens.min() > 2048 and len(w.cow_pairs) == 0
+    for g in range(16):
+        rows = w.block_tables[8 * g:8 * g + 8]
+        # the 128 prompt blocks are the same physical blocks for all 8 members ...
+        assert (rows[:, :128] == rows[0, :128]).all()
+        assert (w.refcount[rows[0, :128]] == 8).all()
+        # ... and no block after the prompt is shared
+        for s in range(8 * g, 8 * g + 8):
+            own = w.block_tables[s, 128:(int(w.seq_lens[s]) + 15) // 16]
+            assert (w.refcount[own] == 1).all()
+    go, pt, sb = W.cascade_groups(w, 8)
+    assert (sb == 128).all() and pt.shape == (16, 128)
+    assert (pt == w.block_tables[::8, :128]).all()
+
+
 def test_hybrid_layout():
     w = W.sarathi_hybrid()
     assert w.num_chunks == 1 and list(w.cu_q_lens) == [0, 512]
