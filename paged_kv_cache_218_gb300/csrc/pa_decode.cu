@@ -309,16 +309,10 @@ __device__ __forceinline__ void attend_block(uint32_t kbase, uint32_t vbase, uin
 //    pairs of two tokens are interleaved with prmt before the conversion.
 // The scores come out in units of sl2 (the query's power-of-two scale and the
 // K scale folded in); the V scale is applied to the finished output.
-template <int D>
-__device__ __forceinline__ void attend_block_fp8(uint32_t kbase, uint32_t vbase,
-                                                 const uint32_t (&qf)[D / 16][2],
-                                                 float (&o)[D / 16][4], float& m0, float& m1,
-                                                 float& l0, float& l1, int valid, float sl2,
-                                                 int lane) {
-  static_assert(D == 128, "the E4M3 path has 128-byte token rows");
-  constexpr int KS = D / 16;
+// Pieces of the E4M3 block routines below (head_dim 128).
+// The block's K bytes of this lane: tokens g and g + 8, 32 bytes each.
+__device__ __forceinline__ void fp8_load_k(uint32_t kbase, int lane, uint32_t (&kw)[2][8]) {
   const int g = lane >> 2, c = lane & 3;
-  uint32_t kw[2][8];
 #pragma unroll
   for (int r = 0; r < 2; ++r) {
     const int tok = g + 8 * r;
@@ -331,8 +325,12 @@ __device__ __forceinline__ void attend_block_fp8(uint32_t kbase, uint32_t vbase,
       kw[r][4 * h + 3] = v.w;
     }
   }
-  // the V bytes are read now, so that their latency hides under the scores
-  uint32_t vw[4][4];
+}
+
+// The block's V bytes of this lane: dims [16g, 16g + 16) of tokens 2c, 2c+1,
+// 2c+8, 2c+9.
+__device__ __forceinline__ void fp8_load_v(uint32_t vbase, int lane, uint32_t (&vw)[4][4]) {
+  const int g = lane >> 2, c = lane & 3;
 #pragma unroll
   for (int r = 0; r < 4; ++r) {
     const int tok = 2 * c + (r & 1) + 8 * (r >> 1);
@@ -342,13 +340,19 @@ __device__ __forceinline__ void attend_block_fp8(uint32_t kbase, uint32_t vbase,
     vw[r][2] = v.z;
     vw[r][3] = v.w;
   }
-  // four independent MMA chains of two k-steps each (short dependency chains:
-  // this path is bound by the latency of a consumer warp's work per block)
+}
+
+// Scores x[e] of S^T (fragment element e: tokens lane/4 and lane/4 + 8, heads
+// 2c and 2c + 1) in sl2 units, -inf for tokens at or past `valid`.  Four
+// independent MMA chains of two k-steps each: this path is bound by the
+// latency of a consumer warp's work per block.
+__device__ __forceinline__ void fp8_scores(const uint32_t (&kw)[2][8], const uint32_t (&qf)[8][2],
+                                           float sl2, int valid, int lane, float (&x)[4]) {
   float sc[4][4];
 #pragma unroll
   for (int i = 0; i < 4; ++i) sc[i][0] = sc[i][1] = sc[i][2] = sc[i][3] = 0.f;
 #pragma unroll
-  for (int ks = 0; ks < KS; ++ks) {
+  for (int ks = 0; ks < 8; ++ks) {
     uint32_t ka[4];
     ka[0] = e4m3x2_to_f16x2(kw[0][ks]);
     ka[1] = e4m3x2_to_f16x2(kw[1][ks]);
@@ -358,41 +362,23 @@ __device__ __forceinline__ void attend_block_fp8(uint32_t kbase, uint32_t vbase,
   }
   const int t0 = lane >> 2;
   const bool v0 = t0 < valid, v1 = t0 + 8 < valid;
-  const float x0 = v0 ? ((sc[0][0] + sc[1][0]) + (sc[2][0] + sc[3][0])) * sl2 : -INFINITY;
-  const float x1 = v0 ? ((sc[0][1] + sc[1][1]) + (sc[2][1] + sc[3][1])) * sl2 : -INFINITY;
-  const float x2 = v1 ? ((sc[0][2] + sc[1][2]) + (sc[2][2] + sc[3][2])) * sl2 : -INFINITY;
-  const float x3 = v1 ? ((sc[0][3] + sc[1][3]) + (sc[2][3] + sc[3][3])) * sl2 : -INFINITY;
-  float mxa = fmaxf(x0, x2), mxb = fmaxf(x1, x3);
 #pragma unroll
-  for (int off = 4; off < 32; off <<= 1) {
-    mxa = fmaxf(mxa, __shfl_xor_sync(0xffffffffu, mxa, off));
-    mxb = fmaxf(mxb, __shfl_xor_sync(0xffffffffu, mxb, off));
-  }
-  const float mna = fmaxf(m0, mxa), mnb = fmaxf(m1, mxb);
-  const float aa = fast_exp2(m0 - mna), ab = fast_exp2(m1 - mnb);
-  const float pa0 = fast_exp2(x0 - mna), pb0 = fast_exp2(x1 - mnb);
-  const float pa1 = fast_exp2(x2 - mna), pb1 = fast_exp2(x3 - mnb);
-  l0 = l0 * aa + pa0 + pa1;
-  l1 = l1 * ab + pb0 + pb1;
-  m0 = mna;
-  m1 = mnb;
-#pragma unroll
-  for (int mt = 0; mt < KS; ++mt) {
-    o[mt][0] *= aa;
-    o[mt][1] *= ab;
-    o[mt][2] *= aa;
-    o[mt][3] *= ab;
-  }
-  const uint32_t b0 = movmatrix_trans(pack_f16x2(pa0, pb0));
-  const uint32_t b1 = movmatrix_trans(pack_f16x2(pa1, pb1));
+  for (int e = 0; e < 4; ++e)
+    x[e] = (e < 2 ? v0 : v1) ? ((sc[0][e] + sc[1][e]) + (sc[2][e] + sc[3][e])) * sl2 : -INFINITY;
+}
+
+// O^T += V^T P^T for one block: P^T fragments b0, b1; V halves of tokens at or
+// past `valid` zeroed (their p is 0, but their bytes may hold anything).
+__device__ __forceinline__ void fp8_pv(const uint32_t (&vw)[4][4], uint32_t b0, uint32_t b1,
+                                       int valid, int lane, float (&o)[8][4]) {
   uint32_t keep01 = 0xffffffffu, keep23 = 0xffffffffu;
-  if (valid < 16) {  // masked tokens have p = 0, but their V bytes may hold anything
-    const int q2 = c * 2;
+  if (valid < 16) {
+    const int q2 = (lane & 3) * 2;
     keep01 = (q2 < valid ? 0x0000ffffu : 0u) | (q2 + 1 < valid ? 0xffff0000u : 0u);
     keep23 = (q2 + 8 < valid ? 0x0000ffffu : 0u) | (q2 + 9 < valid ? 0xffff0000u : 0u);
   }
 #pragma unroll
-  for (int mt = 0; mt < KS; ++mt) {
+  for (int mt = 0; mt < 8; ++mt) {
     const int j = mt >> 1;
     const uint32_t sel = (mt & 1) ? 0x7362u : 0x5140u;  // bytes 2mt, 2mt+1 of two tokens
     const uint32_t t01 = prmt(vw[0][j], vw[1][j], sel);
@@ -404,6 +390,95 @@ __device__ __forceinline__ void attend_block_fp8(uint32_t kbase, uint32_t vbase,
     va[3] = e4m3x2_to_f16x2(t23 >> 16) & keep23;
     mma_f16_16816(o[mt], va, b0, b1);
   }
+}
+
+template <int D>
+__device__ __forceinline__ void attend_block_fp8(uint32_t kbase, uint32_t vbase,
+                                                 const uint32_t (&qf)[D / 16][2],
+                                                 float (&o)[D / 16][4], float& m0, float& m1,
+                                                 float& l0, float& l1, int valid, float sl2,
+                                                 int lane) {
+  static_assert(D == 128, "the E4M3 path has 128-byte token rows");
+  uint32_t kw[2][8], vw[4][4];
+  fp8_load_k(kbase, lane, kw);
+  fp8_load_v(vbase, lane, vw);  // read now: the latency hides under the scores
+  float x[4];
+  fp8_scores(kw, qf, sl2, valid, lane, x);
+  float mxa = fmaxf(x[0], x[2]), mxb = fmaxf(x[1], x[3]);
+#pragma unroll
+  for (int off = 4; off < 32; off <<= 1) {
+    mxa = fmaxf(mxa, __shfl_xor_sync(0xffffffffu, mxa, off));
+    mxb = fmaxf(mxb, __shfl_xor_sync(0xffffffffu, mxb, off));
+  }
+  const float mna = fmaxf(m0, mxa), mnb = fmaxf(m1, mxb);
+  const float aa = fast_exp2(m0 - mna), ab = fast_exp2(m1 - mnb);
+  const float pa0 = fast_exp2(x[0] - mna), pb0 = fast_exp2(x[1] - mnb);
+  const float pa1 = fast_exp2(x[2] - mna), pb1 = fast_exp2(x[3] - mnb);
+  l0 = l0 * aa + pa0 + pa1;
+  l1 = l1 * ab + pb0 + pb1;
+  m0 = mna;
+  m1 = mnb;
+#pragma unroll
+  for (int mt = 0; mt < 8; ++mt) {
+    o[mt][0] *= aa;
+    o[mt][1] *= ab;
+    o[mt][2] *= aa;
+    o[mt][3] *= ab;
+  }
+  fp8_pv(vw, movmatrix_trans(pack_f16x2(pa0, pb0)), movmatrix_trans(pack_f16x2(pa1, pb1)), valid,
+         lane, o);
+}
+
+// Two consecutive blocks of one piece (the first one full, the second with
+// `valid` tokens) in one step: both score chains at once, one online-softmax
+// update over the 32 tokens, one rescale of the accumulators, then both PV
+// products.  Twice the independent work per dependency chain.
+template <int D>
+__device__ __forceinline__ void attend_pair_fp8(uint32_t kbase0, uint32_t vbase0, uint32_t kbase1,
+                                                uint32_t vbase1, const uint32_t (&qf)[D / 16][2],
+                                                float (&o)[D / 16][4], float& m0, float& m1,
+                                                float& l0, float& l1, int valid, float sl2,
+                                                int lane) {
+  static_assert(D == 128, "the E4M3 path has 128-byte token rows");
+  float x[4], y[4];
+  {
+    uint32_t kw[2][8], kv[2][8];
+    fp8_load_k(kbase0, lane, kw);
+    fp8_load_k(kbase1, lane, kv);
+    fp8_scores(kw, qf, sl2, 16, lane, x);
+    fp8_scores(kv, qf, sl2, valid, lane, y);
+  }
+  float mxa = fmaxf(fmaxf(x[0], x[2]), fmaxf(y[0], y[2]));
+  float mxb = fmaxf(fmaxf(x[1], x[3]), fmaxf(y[1], y[3]));
+#pragma unroll
+  for (int off = 4; off < 32; off <<= 1) {
+    mxa = fmaxf(mxa, __shfl_xor_sync(0xffffffffu, mxa, off));
+    mxb = fmaxf(mxb, __shfl_xor_sync(0xffffffffu, mxb, off));
+  }
+  const float mna = fmaxf(m0, mxa), mnb = fmaxf(m1, mxb);
+  const float aa = fast_exp2(m0 - mna), ab = fast_exp2(m1 - mnb);
+  const float pa0 = fast_exp2(x[0] - mna), pb0 = fast_exp2(x[1] - mnb);
+  const float pa1 = fast_exp2(x[2] - mna), pb1 = fast_exp2(x[3] - mnb);
+  const float qa0 = fast_exp2(y[0] - mna), qb0 = fast_exp2(y[1] - mnb);
+  const float qa1 = fast_exp2(y[2] - mna), qb1 = fast_exp2(y[3] - mnb);
+  l0 = l0 * aa + ((pa0 + pa1) + (qa0 + qa1));
+  l1 = l1 * ab + ((pb0 + pb1) + (qb0 + qb1));
+  m0 = mna;
+  m1 = mnb;
+#pragma unroll
+  for (int mt = 0; mt < 8; ++mt) {
+    o[mt][0] *= aa;
+    o[mt][1] *= ab;
+    o[mt][2] *= aa;
+    o[mt][3] *= ab;
+  }
+  uint32_t vw[4][4];
+  fp8_load_v(vbase0, lane, vw);
+  fp8_pv(vw, movmatrix_trans(pack_f16x2(pa0, pb0)), movmatrix_trans(pack_f16x2(pa1, pb1)), 16,
+         lane, o);
+  fp8_load_v(vbase1, lane, vw);
+  fp8_pv(vw, movmatrix_trans(pack_f16x2(qa0, qb0)), movmatrix_trans(pack_f16x2(qa1, qb1)), valid,
+         lane, o);
 }
 
 // Head-dimension index of output fragment row g (+8 when half = 1) of m-tile
@@ -957,6 +1032,31 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int valid = min(kBlockSize, pc.len - j * kBlockSize);
         if constexpr (KV8) {
           const uint32_t kb = sbase + st * L.stage_bytes + hw * L.head_bytes;
+          if (wph == 1 && j + 1 < pc.j1) {
+            // the piece's next block too (this warp holds every block of its
+            // kv head): both in one step.  The first one is full, since the
+            // piece goes on past it.
+            const uint32_t st2 = (g + 1) % NS;
+            if (!mbar_wait_warp(bar_full + st2 * 8, ((g + 1) / NS) & 1)) {
+              if (lane == 0) atomicOr(a.err, PA_DEVERR_TIMEOUT);
+              *abort_flag = 1;
+              __syncwarp();
+              if (lane == 0) mbar_arrive(bar_empty + st * 8);
+              continue;
+            }
+            const uint32_t kb2 = sbase + st2 * L.stage_bytes + hw * L.head_bytes;
+            attend_pair_fp8<D>(kb, kb + Hkv * L.head_bytes, kb2, kb2 + Hkv * L.head_bytes, qf, o,
+                               m0, m1, l0, l1, min(kBlockSize, pc.len - (j + 1) * kBlockSize),
+                               sl2, lane);
+            __syncwarp();
+            if (lane == 0) {
+              mbar_arrive(bar_empty + st * 8);
+              mbar_arrive(bar_empty + st2 * 8);
+            }
+            ++j;
+            ++g;
+            continue;
+          }
           attend_block_fp8<D>(kb, kb + Hkv * L.head_bytes, qf, o, m0, m1, l0, l1, valid, sl2,
                               lane);
         } else {
