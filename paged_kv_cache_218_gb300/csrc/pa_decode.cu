@@ -220,16 +220,16 @@ __device__ __forceinline__ uint32_t swz(uint32_t base, int tok, int chunk, uint3
   return base + (chunk >> 3) * half + tok * 128 + (((chunk & 7) ^ (tok & 7)) << 4);
 }
 
+// Scores x[e] of S^T for one bf16 block (fragment element e: tokens lane/4
+// and lane/4 + 8, heads 2q and 2q + 1) in log2 units, -inf at or past
+// `valid`.  Four independent accumulation chains of KS/4 k-steps each cut the
+// dependent MMA latency.
 template <int D>
-__device__ __forceinline__ void attend_block(uint32_t kbase, uint32_t vbase, uint32_t half,
-                                             const uint32_t (&qf)[D / 16][2],
-                                             float (&o)[D / 16][4], float& m0, float& m1,
-                                             float& l0, float& l1, int valid, float scale_log2,
-                                             int lane) {
+__device__ __forceinline__ void bf16_scores(uint32_t kbase, uint32_t half,
+                                            const uint32_t (&qf)[D / 16][2], float scale_log2,
+                                            int valid, int lane, float (&x)[4]) {
   constexpr int KS = D / 16;
   const int i = lane >> 3, r = lane & 7;
-  // four independent accumulation chains of KS/4 k-steps each cut the
-  // dependent MMA latency
   float sc[4][4];
 #pragma unroll
   for (int c = 0; c < 4; ++c) sc[c][0] = sc[c][1] = sc[c][2] = sc[c][3] = 0.f;
@@ -242,41 +242,24 @@ __device__ __forceinline__ void attend_block(uint32_t kbase, uint32_t vbase, uin
     mma_bf16_16816(sc[ks & 3], a0, qf[ks][0], qf[ks][1]);
     mma_bf16_16816(sc[(ks + 1) & 3], a1, qf[ks + 1][0], qf[ks + 1][1]);
   }
-  // S^T: [token lane/4][heads 2q, 2q+1], [token lane/4 + 8][same heads]
   const int t0 = lane >> 2;
   const bool v0 = t0 < valid, v1 = t0 + 8 < valid;
-  auto score = [&](int e) { return (sc[0][e] + sc[1][e]) + (sc[2][e] + sc[3][e]); };
-  const float x0 = v0 ? score(0) * scale_log2 : -INFINITY;
-  const float x1 = v0 ? score(1) * scale_log2 : -INFINITY;
-  const float x2 = v1 ? score(2) * scale_log2 : -INFINITY;
-  const float x3 = v1 ? score(3) * scale_log2 : -INFINITY;
-  float mxa = fmaxf(x0, x2), mxb = fmaxf(x1, x3);
 #pragma unroll
-  for (int off = 4; off < 32; off <<= 1) {
-    mxa = fmaxf(mxa, __shfl_xor_sync(0xffffffffu, mxa, off));
-    mxb = fmaxf(mxb, __shfl_xor_sync(0xffffffffu, mxb, off));
-  }
-  const float mna = fmaxf(m0, mxa), mnb = fmaxf(m1, mxb);
-  const float aa = fast_exp2(m0 - mna), ab = fast_exp2(m1 - mnb);
-  const float pa0 = fast_exp2(x0 - mna), pb0 = fast_exp2(x1 - mnb);
-  const float pa1 = fast_exp2(x2 - mna), pb1 = fast_exp2(x3 - mnb);
-  l0 = l0 * aa + pa0 + pa1;
-  l1 = l1 * ab + pb0 + pb1;
-  m0 = mna;
-  m1 = mnb;
-#pragma unroll
-  for (int mt = 0; mt < KS; ++mt) {
-    o[mt][0] *= aa;
-    o[mt][1] *= ab;
-    o[mt][2] *= aa;
-    o[mt][3] *= ab;
-  }
-  // P^T as the B operand (k = token, n = head): transpose the two 8x8 halves
-  const uint32_t b0 = movmatrix_trans(pack_bf16x2(pa0, pb0));
-  const uint32_t b1 = movmatrix_trans(pack_bf16x2(pa1, pb1));
+  for (int e = 0; e < 4; ++e)
+    x[e] = (e < 2 ? v0 : v1) ? ((sc[0][e] + sc[1][e]) + (sc[2][e] + sc[3][e])) * scale_log2
+                             : -INFINITY;
+}
+
+// O^T += V^T P^T for one bf16 block: P^T fragments b0, b1; V rows of tokens at
+// or past `valid` zeroed (their p is 0, but their rows may hold anything).
+template <int D>
+__device__ __forceinline__ void bf16_pv(uint32_t vbase, uint32_t half, uint32_t b0, uint32_t b1,
+                                        int valid, int lane, float (&o)[D / 16][4]) {
+  constexpr int KS = D / 16;
+  const int i = lane >> 3, r = lane & 7;
   const int vtok = r + ((i >> 1) << 3);
   uint32_t keep01 = 0xffffffffu, keep23 = 0xffffffffu;
-  if (valid < 16) {  // masked tokens have p = 0, but their V rows may hold anything
+  if (valid < 16) {
     const int q2 = (lane & 3) * 2;
     keep01 = (q2 < valid ? 0x0000ffffu : 0u) | (q2 + 1 < valid ? 0xffff0000u : 0u);
     keep23 = (q2 + 8 < valid ? 0x0000ffffu : 0u) | (q2 + 9 < valid ? 0xffff0000u : 0u);
@@ -291,6 +274,84 @@ __device__ __forceinline__ void attend_block(uint32_t kbase, uint32_t vbase, uin
     a[3] &= keep23;
     mma_bf16_16816(o[mt], a, b0, b1);
   }
+}
+
+template <int D>
+__device__ __forceinline__ void attend_block(uint32_t kbase, uint32_t vbase, uint32_t half,
+                                             const uint32_t (&qf)[D / 16][2],
+                                             float (&o)[D / 16][4], float& m0, float& m1,
+                                             float& l0, float& l1, int valid, float scale_log2,
+                                             int lane) {
+  constexpr int KS = D / 16;
+  float x[4];
+  bf16_scores<D>(kbase, half, qf, scale_log2, valid, lane, x);
+  float mxa = fmaxf(x[0], x[2]), mxb = fmaxf(x[1], x[3]);
+#pragma unroll
+  for (int off = 4; off < 32; off <<= 1) {
+    mxa = fmaxf(mxa, __shfl_xor_sync(0xffffffffu, mxa, off));
+    mxb = fmaxf(mxb, __shfl_xor_sync(0xffffffffu, mxb, off));
+  }
+  const float mna = fmaxf(m0, mxa), mnb = fmaxf(m1, mxb);
+  const float aa = fast_exp2(m0 - mna), ab = fast_exp2(m1 - mnb);
+  const float pa0 = fast_exp2(x[0] - mna), pb0 = fast_exp2(x[1] - mnb);
+  const float pa1 = fast_exp2(x[2] - mna), pb1 = fast_exp2(x[3] - mnb);
+  l0 = l0 * aa + pa0 + pa1;
+  l1 = l1 * ab + pb0 + pb1;
+  m0 = mna;
+  m1 = mnb;
+#pragma unroll
+  for (int mt = 0; mt < KS; ++mt) {
+    o[mt][0] *= aa;
+    o[mt][1] *= ab;
+    o[mt][2] *= aa;
+    o[mt][3] *= ab;
+  }
+  // P^T as the B operand (k = token, n = head): transpose the two 8x8 halves
+  bf16_pv<D>(vbase, half, movmatrix_trans(pack_bf16x2(pa0, pb0)),
+             movmatrix_trans(pack_bf16x2(pa1, pb1)), valid, lane, o);
+}
+
+// Two consecutive bf16 blocks of one piece (the first full), as
+// attend_pair_fp8 does for E4M3.
+template <int D>
+__device__ __forceinline__ void attend_pair(uint32_t kbase0, uint32_t vbase0, uint32_t kbase1,
+                                            uint32_t vbase1, uint32_t half,
+                                            const uint32_t (&qf)[D / 16][2],
+                                            float (&o)[D / 16][4], float& m0, float& m1,
+                                            float& l0, float& l1, int valid, float scale_log2,
+                                            int lane) {
+  constexpr int KS = D / 16;
+  float x[4], y[4];
+  bf16_scores<D>(kbase0, half, qf, scale_log2, 16, lane, x);
+  bf16_scores<D>(kbase1, half, qf, scale_log2, valid, lane, y);
+  float mxa = fmaxf(fmaxf(x[0], x[2]), fmaxf(y[0], y[2]));
+  float mxb = fmaxf(fmaxf(x[1], x[3]), fmaxf(y[1], y[3]));
+#pragma unroll
+  for (int off = 4; off < 32; off <<= 1) {
+    mxa = fmaxf(mxa, __shfl_xor_sync(0xffffffffu, mxa, off));
+    mxb = fmaxf(mxb, __shfl_xor_sync(0xffffffffu, mxb, off));
+  }
+  const float mna = fmaxf(m0, mxa), mnb = fmaxf(m1, mxb);
+  const float aa = fast_exp2(m0 - mna), ab = fast_exp2(m1 - mnb);
+  const float pa0 = fast_exp2(x[0] - mna), pb0 = fast_exp2(x[1] - mnb);
+  const float pa1 = fast_exp2(x[2] - mna), pb1 = fast_exp2(x[3] - mnb);
+  const float qa0 = fast_exp2(y[0] - mna), qb0 = fast_exp2(y[1] - mnb);
+  const float qa1 = fast_exp2(y[2] - mna), qb1 = fast_exp2(y[3] - mnb);
+  l0 = l0 * aa + ((pa0 + pa1) + (qa0 + qa1));
+  l1 = l1 * ab + ((pb0 + pb1) + (qb0 + qb1));
+  m0 = mna;
+  m1 = mnb;
+#pragma unroll
+  for (int mt = 0; mt < KS; ++mt) {
+    o[mt][0] *= aa;
+    o[mt][1] *= ab;
+    o[mt][2] *= aa;
+    o[mt][3] *= ab;
+  }
+  bf16_pv<D>(vbase0, half, movmatrix_trans(pack_bf16x2(pa0, pb0)),
+             movmatrix_trans(pack_bf16x2(pa1, pb1)), 16, lane, o);
+  bf16_pv<D>(vbase1, half, movmatrix_trans(pack_bf16x2(qa0, qb0)),
+             movmatrix_trans(pack_bf16x2(qa1, qb1)), valid, lane, o);
 }
 
 // One 16-token block of E4M3 K/V for one kv head (head_dim 128).  The stage
@@ -1030,33 +1091,43 @@ __global__ void __launch_bounds__(kThreads, 1)
           continue;
         }
         const int valid = min(kBlockSize, pc.len - j * kBlockSize);
-        if constexpr (KV8) {
-          const uint32_t kb = sbase + st * L.stage_bytes + hw * L.head_bytes;
-          if (wph == 1 && j + 1 < pc.j1) {
-            // the piece's next block too (this warp holds every block of its
-            // kv head): both in one step.  The first one is full, since the
-            // piece goes on past it.
-            const uint32_t st2 = (g + 1) % NS;
-            if (!mbar_wait_warp(bar_full + st2 * 8, ((g + 1) / NS) & 1)) {
-              if (lane == 0) atomicOr(a.err, PA_DEVERR_TIMEOUT);
-              *abort_flag = 1;
-              __syncwarp();
-              if (lane == 0) mbar_arrive(bar_empty + st * 8);
-              continue;
-            }
-            const uint32_t kb2 = sbase + st2 * L.stage_bytes + hw * L.head_bytes;
-            attend_pair_fp8<D>(kb, kb + Hkv * L.head_bytes, kb2, kb2 + Hkv * L.head_bytes, qf, o,
-                               m0, m1, l0, l1, min(kBlockSize, pc.len - (j + 1) * kBlockSize),
-                               sl2, lane);
+        if (wph == 1 && NS >= 4 && j + 1 < pc.j1) {
+          // the piece's next block too (this warp holds every block of its kv
+          // head): both in one step.  The first one is full, since the piece
+          // goes on past it.  Only with a ring of four stages or more (the
+          // E4M3 pools' six): holding two of three stages starves the
+          // producer (measured 48.8 -> 51.9 us on the Llama-3-8B layer).
+          const uint32_t st2 = (g + 1) % NS;
+          if (!mbar_wait_warp(bar_full + st2 * 8, ((g + 1) / NS) & 1)) {
+            if (lane == 0) atomicOr(a.err, PA_DEVERR_TIMEOUT);
+            *abort_flag = 1;
             __syncwarp();
-            if (lane == 0) {
-              mbar_arrive(bar_empty + st * 8);
-              mbar_arrive(bar_empty + st2 * 8);
-            }
-            ++j;
-            ++g;
+            if (lane == 0) mbar_arrive(bar_empty + st * 8);
             continue;
           }
+          const int valid2 = min(kBlockSize, pc.len - (j + 1) * kBlockSize);
+          if constexpr (KV8) {
+            const uint32_t kb = sbase + st * L.stage_bytes + hw * L.head_bytes;
+            const uint32_t kb2 = sbase + st2 * L.stage_bytes + hw * L.head_bytes;
+            attend_pair_fp8<D>(kb, kb + Hkv * L.head_bytes, kb2, kb2 + Hkv * L.head_bytes, qf, o,
+                               m0, m1, l0, l1, valid2, sl2, lane);
+          } else {
+            const uint32_t kb = sbase + st * L.stage_bytes + hw * kBoxBytes;
+            const uint32_t kb2 = sbase + st2 * L.stage_bytes + hw * kBoxBytes;
+            attend_pair<D>(kb, kb + Hkv * L.head_bytes, kb2, kb2 + Hkv * L.head_bytes,
+                           Hkv * kBoxBytes, qf, o, m0, m1, l0, l1, valid2, a.scale_log2, lane);
+          }
+          __syncwarp();
+          if (lane == 0) {
+            mbar_arrive(bar_empty + st * 8);
+            mbar_arrive(bar_empty + st2 * 8);
+          }
+          ++j;
+          ++g;
+          continue;
+        }
+        if constexpr (KV8) {
+          const uint32_t kb = sbase + st * L.stage_bytes + hw * L.head_bytes;
           attend_block_fp8<D>(kb, kb + Hkv * L.head_bytes, qf, o, m0, m1, l0, l1, valid, sl2,
                               lane);
         } else {
