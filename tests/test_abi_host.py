@@ -83,6 +83,52 @@ def test_workspace_sizes(lib):
     assert _ws(lib, 64, 32, 8, 128, 128, 16, 24) == 0
 
 
+def test_hybrid_and_cascade_workspace_sizes(lib):
+    f = lib.pa_hybrid_workspace_size
+    f.restype = ctypes.c_size_t
+    f.argtypes = [ctypes.c_int] * 6
+    dec = _ws(lib, 128, 32, 8, 128, 256, 16, 0)
+    # the balanced decode's workspace after 256 bytes for the chunk's finish counter
+    assert f(128, 32, 8, 128, 256, 16) == 256 + dec
+    assert f(128, 32, 8, 96, 256, 16) == 0
+    g = lib.pa_cascade_workspace_size
+    g.restype = ctypes.c_size_t
+    g.argtypes = [ctypes.c_int] * 7
+    S, Hq, Hkv = 256, 64, 8
+    o = -(-S * Hq * 128 * 4 // 256) * 256
+    l = -(-S * Hq * 4 // 256) * 256
+    t = -(-S * Hkv * 4 // 256) * 256
+    # prefix result and the partials of up to three more prefix parts, tickets, then the decode's
+    assert g(S, Hq, Hkv, 128, 512, 16, 0) == 4 * (o + l) + t + _ws(lib, S, Hq, Hkv, 128, 512, 16, 0)
+    assert g(S, Hq, Hkv, 64, 512, 16, 0) == 0
+
+
+def test_hybrid_checks_arguments_before_launching(lib):
+    f = lib.pa_hybrid_attention
+    P, I = ctypes.c_void_p, ctypes.c_int
+    f.argtypes = [P, P, P, I, P, P, P, I, I, I, P, P, P, P, I, P, I, P, P, P, I, I, I, I,
+                  ctypes.c_int64, ctypes.c_float, I, P, ctypes.c_size_t, P]
+    f.restype = I
+
+    def call(**kw):
+        a = dict(oc=P(256), qc=P(256), cbt=P(256), cmb=4, cu=P(256), qs=P(256), csl=P(256),
+                 C=1, T=32, mq=32, clse=None, od=P(256), qd=P(256), dbt=P(256), dmb=4,
+                 dsl=P(256), S=2, dlse=None, k=P(256), v=P(256), Hq=8, Hkv=2, D=128, bs=16,
+                 nb=10, scale=0.1, cs=0, ws=P(256), wsb=1 << 30, st=None)
+        a.update(kw)
+        return f(*a.values())
+
+    assert call(D=64) == -2              # the chunk's tensor-core path needs head_dim 128
+    assert call(Hq=6, Hkv=2) == -2       # group 3 does not tile 128 rows
+    assert call(scale=0.0) == -1
+    assert call(cs=-1) == -1             # chunk_sms must be >= 0
+    assert call(S=-1) == -1
+    assert call(ws=None) == -4           # workspace missing
+    assert call(wsb=100) == -4           # workspace too small
+    assert call(ws=P(272)) == -4         # workspace misaligned
+    assert call(oc=None) == -1
+
+
 def _decode_args(**kw):
     P = ctypes.c_void_p
     a = dict(out=P(16), q=P(16), k=P(16), v=P(16), bt=P(16), mb=4, sl=P(16), S=2, Hq=8, Hkv=2,
