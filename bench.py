@@ -64,9 +64,15 @@ def load_peaks():
 
 
 def source_hash(files):
+    """Hash of the kernel sources' code: comments and runs of white space are
+    dropped first, so that only a change of code invalidates a profile."""
+    import re
     h = hashlib.sha256()
     for f in files:
-        h.update(open(os.path.join(ROOT, "paged_kv_cache_218_gb300", "csrc", f), "rb").read())
+        text = open(os.path.join(ROOT, "paged_kv_cache_218_gb300", "csrc", f)).read()
+        text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+        text = re.sub(r"//[^\n]*", " ", text)
+        h.update(re.sub(r"\s+", " ", text).strip().encode())
     return h.hexdigest()[:16]
 
 

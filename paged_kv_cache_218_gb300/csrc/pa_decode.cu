@@ -676,9 +676,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();  // barriers initialized before any warp uses them
   // Launched as a programmatic dependent of the previous kernel on the stream,
   // the CTA may get here while that kernel still runs.  Until griddep_wait()
-  // returns it reads no global memory; it only asks L2 for the lines of this
-  // launch's lengths, block tables and queries (at most 4 MB of each), spread
-  // over every thread of the grid, so that the reads after the wait hit L2.
+  // returns it writes no global memory, and it reads only lengths and start
+  // blocks, for a plan that is checked after the wait (below).  It also asks
+  // L2 for the lines of this launch's lengths, block tables and queries (at
+  // most 4 MB of each), spread over every thread of the grid, so that the
+  // reads after the wait hit L2.
   {
     const long long nthr = static_cast<long long>(gridDim.x) * kThreads;
     const long long me = static_cast<long long>(blockIdx.x) * kThreads + tid;
