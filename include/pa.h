@@ -266,7 +266,10 @@ int pa_merge_partials(void *out, float *out_lse, const float *part_out, const fl
  *   cu_q_lens  device int32 [num_chunks + 1]; q_start_pos, seq_lens int32 [num_chunks]
  *   max_q_len  host int, an upper bound of every chunk's query count
  *   out_lse    device fp32 [total_q_tokens, num_q_heads] or NULL
- * head_dim must be 128 for this call.
+ * head_dim must be 128 for this call.  A chunk whose metadata is inconsistent
+ * (rows outside [0, total_q_tokens), q_start_pos + q_len > seq_len, or
+ * seq_len beyond its table row) is skipped, its rows left unwritten, and
+ * sets PA_DEVERR_CHUNK.
  */
 int pa_prefill_chunk(void *out, const void *q, const void *k_cache, const void *v_cache,
                      const int32_t *block_tables, int max_blocks_per_seq,

@@ -869,6 +869,7 @@ static int prefill_impl(void* out, const void* q, const void* k_cache, const voi
   a.num_blocks = num_blocks;
   a.max_blocks = max_blocks_per_seq;
   a.num_chunks = num_chunks;
+  a.total_q = total_q_tokens;
   a.num_q_heads = num_q_heads;
   a.num_kv_heads = num_kv_heads;
   a.group = group;

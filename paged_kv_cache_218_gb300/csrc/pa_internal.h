@@ -82,6 +82,7 @@ struct PrefillArgs {
   int64_t num_blocks;
   int max_blocks;
   int num_chunks;
+  int total_q;               // rows of q and out; cu_q_lens must stay within
   int num_q_heads;
   int num_kv_heads;
   int group;

@@ -17,8 +17,10 @@
 //    request rate, not bandwidth, bounds this pipeline).
 //  * Warp roles.  Warp 9 loads: Q once, then K and V tiles of 128 keys, each
 //    assembled from eight 16-token paged blocks by TMA (128-byte swizzle), in
-//    rings of two K and three V tiles (a K tile is free once its scores are
-//    done, a V tile only once its PV product is).  Warp 8 issues the tensor-core work from one thread:
+//    rings of two K and two V tiles (a K tile is free once its scores are
+//    done, a V tile only once its PV product is).  Deeper rings only lengthen
+//    the queue: per-tile traces show each SM taking in K/V at about 57 GB/s
+//    whatever the depth, the arrival latency growing with the tiles in flight.  Warp 8 issues the tensor-core work from one thread:
 //    S = Q K^T into one of two tensor-memory score buffers (tcgen05.mma,
 //    M = N = 128, K = 16, bf16 in, fp32 accumulate) and O += P V into a third
 //    region.  Warps 0-7 run the softmax: two warps per tensor-memory lane
@@ -58,7 +60,7 @@ constexpr int kTileKeys = 128;
 constexpr int kHalf = 128 * 128;  // a 64-column half of a 128-row operand: 128 rows x 128 B
 constexpr int kQOff = 0;
 constexpr int kNK = 2;                  // K tiles in flight (freed as soon as their scores are done)
-constexpr int kNV = 3;                  // V tiles in flight (held until their PV product is done)
+constexpr int kNV = 2;                  // V tiles in flight (held until their PV product is done)
 constexpr int kTileBytes = 2 * kHalf;   // one K or V tile: 128 keys x 128 columns
 constexpr int kKOff = kQOff + 2 * kHalf;
 constexpr int kVOff = kKOff + kNK * kTileBytes;
@@ -183,7 +185,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int q0 = a.cu_q_lens[c], q1 = a.cu_q_lens[c + 1];
   const int p0 = a.q_start_pos[c], n = a.seq_lens[c];
   const int qlen = q1 - q0;
-  if (qlen < 0 || p0 < 0 || p0 + qlen > n || n > a.max_blocks * kBlockSize) {
+  if (q0 < 0 || q1 > a.total_q || qlen < 0 || p0 < 0 || p0 + qlen > n ||
+      n > a.max_blocks * kBlockSize) {
     if (tid == 0 && m == 0 && kvh == 0) atomicOr(a.err, PA_DEVERR_CHUNK);
     chunk_exit(a, tid);
     return;

@@ -155,6 +155,35 @@ def test_prefill_flags_inconsistent_chunks(pa, cuda_device):
     assert_close(out[:20], ref[:20], "good chunk beside a bad one")
 
 
+def test_prefill_flags_chunk_rows_past_the_query_tensor(pa, cuda_device):
+    # the second chunk's rows end past total_q_tokens: it is skipped (no row
+    # beyond the output tensor is written) and the first chunk is still exact
+    w = W.prefill_batch([(0, 20), (10, 20)], Hq=8, Hkv=2, D=128, seed=10)
+    dw = DeviceWorkload(w, cuda_device)
+    dw.scatter(pa)
+    C = w.num_chunks
+    T = int(w.cu_q_lens[C])
+    # chunk 1 (30 tokens in its sequence) claims rows 20 .. 49 from position 0:
+    # consistent with its sequence, but T = 40 rows exist
+    cu_bad = w.cu_q_lens.copy()
+    cu_bad[C] = T + 10
+    start_bad = w.q_start_pos.copy()
+    start_bad[1] = 0
+    Hq, D = w.num_q_heads, w.head_dim
+    buf = torch.full((T + 64, Hq, D), 7.0, dtype=torch.bfloat16, device=cuda_device)
+    pa.pa_device_error_flags(reset=True)
+    pa.pa_prefill_chunk(buf[:T], dw.q[:T], dw.k_cache, dw.v_cache, dw.block_tables[:C],
+                        torch.from_numpy(cu_bad).to(cuda_device),
+                        torch.from_numpy(start_bad).to(cuda_device), dw.seq_lens[:C], 30,
+                        w.scale)
+    torch.cuda.synchronize()
+    assert pa.pa_device_error_flags() & pa.PA_DEVERR_CHUNK
+    assert bool((buf[T:] == 7.0).all()), "rows past the tensor were written"
+    assert bool((buf[20:T] == 7.0).all()), "the skipped chunk wrote rows"
+    ref, _ = _oracle_prefill(w)
+    assert_close(buf[:20], ref[:20], "good chunk beside one past the tensor")
+
+
 def test_prefill_rejects_unsupported_shapes(pa, cuda_device):
     w = W.prefill_batch([(0, 20)], Hq=6, Hkv=2, D=128, seed=10)  # group 3 does not tile 128 rows
     dw = DeviceWorkload(w, cuda_device)
