@@ -203,6 +203,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int kmax = p0 + min(qlen, tc0 + kCluster * tpt);
   const int nkt = (kmax + kTileKeys - 1) / kTileKeys;
   const int nb_vis = (kmax + kBlockSize - 1) / kBlockSize;
+  // the loader reads the block ids of its first two K tiles now, so that the
+  // table's latency overlaps the set-up below instead of delaying the first load
+  int id_t0 = -1, id_t1 = -1;
+  if (warp == kLoadWarp && lane < 8 / kCluster) {
+    const long long row = static_cast<long long>(c) * a.max_blocks;
+    const int jb = lane * kCluster + rank;
+    if (jb < nb_vis) id_t0 = a.block_tables[row + jb];
+    if (jb + 8 < nb_vis) id_t1 = a.block_tables[row + jb + 8];
+  }
 
   if (tid == 0) {
     mbar_init(bar_q, 1);
@@ -257,7 +266,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int jb = j * 8 + bl;
           id = -1;
           if (jb < nb_vis) {
-            id = a.block_tables[static_cast<long long>(c) * a.max_blocks + jb];
+            id = j == 0   ? id_t0
+                 : j == 1 ? id_t1
+                          : a.block_tables[static_cast<long long>(c) * a.max_blocks + jb];
             if (id < 0 || id >= a.num_blocks) {
               atomicOr(a.err, PA_DEVERR_BLOCK_ID);
               id = -1;
