@@ -457,6 +457,7 @@ def measure_fp8_decode(args, w, reps, ws, dev, pa):
 
 # batches whose consecutive sequences share prefix blocks, and their group size
 CASCADE_GROUP = {"cow_prefix_mix": 4, "shared_prompt_batch": 8}
+E2E_PASSES = 4  # passes over the replicas per end-to-end graph round
 
 
 def measure_cascade(args, w, reps, dev, pa, group):
@@ -514,17 +515,20 @@ def run_e2e(args, w, reps, ws, dev, pa, dist, s_chunk, max_q, T, hws):
     the hybrid batch) from one pinned host buffer in one copy, runs the step's
     kernels on views of the uploaded buffer, and reads its outputs back into
     pinned host memory.  Three streams pipeline the steps: uploads run ahead of
-    the kernels, read-backs follow them.  With graphs (the default) one CUDA
-    graph holds a round of R steps, one per replica, and rounds replay back to
-    back; without, the steps are issued one by one and a replica's buffers are
-    reused only after the step that last used them has finished its kernels
-    (for the upload) and its read-back (for the outputs)."""
+    the kernels, read-backs follow them.  A replica's buffers are reused only
+    after the step that last used them has finished its kernels (for the
+    upload) and its read-back (for the outputs).  With graphs (the default) one
+    CUDA graph holds a round of E2E_PASSES passes over the R replicas, and
+    rounds replay back to back (a round's first upload and last read-back do
+    not overlap the next round, so longer rounds spread that cost); without,
+    the steps are issued one by one."""
     import torch
 
     R = len(reps)
     K = max(args.warmup + 1, min(args.steps, args.e2e_steps))
+    RS = R * E2E_PASSES  # steps per graph round
     if not args.no_graphs:
-        K = (K + R - 1) // R * R
+        K = (K + RS - 1) // RS * RS
     hybrid = w.num_chunks > 0
     s0, q0, S, C = w.decode_seq0, w.q_decode_row0, w.num_decode_seqs, w.num_chunks
     P = args.partition_tokens
@@ -594,21 +598,27 @@ def run_e2e(args, w, reps, ws, dev, pa, dist, s_chunk, max_q, T, hws):
         ev_dn[j].record(s_dn)
         used[j] = True
 
-    def round_body():  # R pipelined steps, captured into one graph
+    def round_body():  # E2E_PASSES x R pipelined steps, captured into one graph
         cap = torch.cuda.current_stream()
         s_up.wait_stream(cap)
         s_dn.wait_stream(cap)
-        for j in range(R):
-            with torch.cuda.stream(s_up):
-                arenas[j].copy_(host, non_blocking=True)
-            ev_up[j].record(s_up)
-            cap.wait_event(ev_up[j])
-            kernels(j)
-            ev_k[j].record(cap)
-            s_dn.wait_event(ev_k[j])
-            with torch.cuda.stream(s_dn):
-                for dst, src in zip(host_out[j], results[j]):
-                    dst.copy_(src, non_blocking=True)
+        for p in range(E2E_PASSES):
+            for j in range(R):
+                if p > 0:  # arena j and replica j's outputs are reused
+                    s_up.wait_event(ev_k[j])
+                with torch.cuda.stream(s_up):
+                    arenas[j].copy_(host, non_blocking=True)
+                ev_up[j].record(s_up)
+                cap.wait_event(ev_up[j])
+                if p > 0:
+                    cap.wait_event(ev_dn[j])
+                kernels(j)
+                ev_k[j].record(cap)
+                s_dn.wait_event(ev_k[j])
+                with torch.cuda.stream(s_dn):
+                    for dst, src in zip(host_out[j], results[j]):
+                        dst.copy_(src, non_blocking=True)
+                ev_dn[j].record(s_dn)
         cap.wait_stream(s_up)
         cap.wait_stream(s_dn)
 
@@ -620,7 +630,7 @@ def run_e2e(args, w, reps, ws, dev, pa, dist, s_chunk, max_q, T, hws):
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g):
             round_body()
-        for _ in range(max(1, args.warmup // R)):
+        for _ in range(max(1, args.warmup // RS)):
             g.replay()
     else:
         for i in range(args.warmup):
@@ -633,7 +643,7 @@ def run_e2e(args, w, reps, ws, dev, pa, dist, s_chunk, max_q, T, hws):
     torch.cuda.synchronize()
     a.record(comp)
     if g is not None:
-        for _ in range(K // R):
+        for _ in range(K // RS):
             g.replay()
     else:
         s_up.wait_stream(comp)
@@ -646,7 +656,8 @@ def run_e2e(args, w, reps, ws, dev, pa, dist, s_chunk, max_q, T, hws):
         raise RuntimeError("device error flags set in the end-to-end run")
     ms, kv_all = reduce_over_ranks(a.elapsed_time(b), kv_bytes_decode(w) * K, dev)
     return dict(ms=ms, steps=K, h2d=total, d2h=d2h, kv_all=kv_all,
-                pipeline=(f"one CUDA graph per round of {R} steps; " if g is not None else "")
+                pipeline=(f"one CUDA graph per round of {RS} steps ({E2E_PASSES} passes over "
+                          f"{R} replicas); " if g is not None else "")
                 + "upload (one copy from pinned host memory), kernels and read-back on three "
                   "streams, uploads running ahead of the kernels and read-backs following them")
 
