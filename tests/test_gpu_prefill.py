@@ -155,6 +155,34 @@ def test_prefill_flags_inconsistent_chunks(pa, cuda_device):
     assert_close(out[:20], ref[:20], "good chunk beside a bad one")
 
 
+def test_prefill_flags_block_ids_outside_the_pool(pa, cuda_device):
+    # chunk 0: an id past the pool in its first K/V tile (ids read ahead of
+    # the set-up); chunk 1: a negative id in its third tile (ids read with the
+    # tile); chunk 2 is clean and must stay exact.  Bad ids read as zeros.
+    w = W.prefill_batch([(0, 40), (300, 20), (100, 50)], Hq=8, Hkv=2, D=128, seed=11)
+    dw = DeviceWorkload(w, cuda_device)
+    dw.scatter(pa)
+    C = w.num_chunks
+    T = int(w.cu_q_lens[C])
+    nb = dw.k_cache.shape[0]
+    bt = w.block_tables[:C].copy()
+    bt[0, 1] = nb + 5
+    bt[1, 17] = -7
+    out = torch.full((T, w.num_q_heads, w.head_dim), float("nan"), dtype=torch.bfloat16,
+                     device=cuda_device)
+    pa.pa_device_error_flags(reset=True)
+    pa.pa_prefill_chunk(out, dw.q[:T], dw.k_cache, dw.v_cache, torch.from_numpy(bt).to(cuda_device),
+                        torch.from_numpy(w.cu_q_lens).to(cuda_device),
+                        torch.from_numpy(w.q_start_pos).to(cuda_device), dw.seq_lens[:C],
+                        int(np.max(np.diff(w.cu_q_lens))), w.scale)
+    torch.cuda.synchronize()
+    assert pa.pa_device_error_flags() & pa.PA_DEVERR_BLOCK_ID
+    ref, _ = _oracle_prefill(w)
+    r2 = slice(int(w.cu_q_lens[2]), int(w.cu_q_lens[3]))
+    assert_close(out[r2], ref[r2], "clean chunk beside chunks with bad block ids")
+    assert bool(torch.isfinite(out).all()), "bad block ids must read as zeros, not garbage"
+
+
 def test_prefill_flags_chunk_rows_past_the_query_tensor(pa, cuda_device):
     # the second chunk's rows end past total_q_tokens: it is skipped (no row
     # beyond the output tensor is written) and the first chunk is still exact
