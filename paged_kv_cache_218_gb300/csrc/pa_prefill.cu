@@ -25,13 +25,18 @@
 //    M = N = 128, K = 16, bf16 in, fp32 accumulate) and O += P V into a third
 //    region.  Warps 0-7 run the softmax: two warps per tensor-memory lane
 //    quadrant, each owning 64 of a row's 128 score columns.
+//  * Three score buffers.  Scores of a tile can be computed as soon as its K
+//    tile lands (while the softmax still works on the two before it), so a K
+//    tile leaves its ring slot soon after it arrives: with two rings of two,
+//    how long a tile holds its slot sets the pace, not the tensor cores.
 //  * Pipelining.  Loader and MMA issuer poll their barriers and issue
-//    whatever is ready, so scores of tile j+1 are computed while the softmax
-//    works on tile j (two score buffers) and PV of tile j-1 runs meanwhile.
+//    whatever is ready, so scores of the next tiles are computed while the
+//    softmax works on tile j and PV of tile j-1 runs meanwhile.
 //  * Softmax per row: tcgen05.ld of its scores, causal mask, row maximum
 //    shared by the two half-row owners, p = 2^(x - m) rounded to bf16 and
-//    stored back into tensor memory (tcgen05.st), double buffered, where the
-//    PV product reads it as its A operand.  The running maximum only
+//    stored back into tensor memory (tcgen05.st) over the first half of the
+//    score columns it came from, where the PV product reads it as its A
+//    operand; a score buffer takes new scores once that PV product is done.  The running maximum only
 //    moves (and O in tensor memory is only rescaled) when the row maximum
 //    grows by more than 2^8, which keeps every p below 256 and the fp32
 //    accumulators far from overflow; the final division uses the same
@@ -70,9 +75,11 @@ constexpr int kRedOff2 = kRedOff + 2 * 2 * 128 * 4;  // row-sum exchange
 constexpr int kBarOff = kRedOff2 + 2 * 128 * 4;
 constexpr int kSmemBytes = kBarOff + 256;
 static_assert(kNK <= 3 && kNV <= 3, "barrier slots");
-constexpr uint32_t kTmemCols = 512;  // S0 [0,128), S1 [128,256), O [256,384), P0, P1
-constexpr uint32_t kTmemO = 256;
-constexpr uint32_t kTmemP = 384;     // P (bf16 pairs): 64 columns per buffer
+// S0 [0,128), S1 [128,256), S2 [256,384), O [384,512); P of a tile (bf16
+// pairs) over its scores: keys 64h .. 64h+63 at columns 64h .. 64h+31
+constexpr int kNS = 3;  // score buffers
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kTmemO = 384;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
 constexpr float kLn2 = 0.6931471805599453f;
 
@@ -152,13 +159,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t bar_k_empty = bar_q + 32;   // [3]
   const uint32_t bar_v_full = bar_q + 56;    // [3] (kNV used)
   const uint32_t bar_v_empty = bar_q + 80;   // [3]
-  const uint32_t bar_s_full = bar_q + 104;   // [2]
-  const uint32_t bar_s_free = bar_q + 120;   // [2]
-  const uint32_t bar_p_full = bar_q + 136;   // [2]: softmax of even / odd tiles done
-  const uint32_t bar_o_done = bar_q + 152;   // [2]: PV of even / odd tiles done
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kBarOff + 168);
+  const uint32_t bar_s_full = bar_q + 104;   // [3]: scores of tile j in buffer j % 3
+  const uint32_t bar_p_full = bar_q + 128;   // [3]: softmax of tile j done
+  const uint32_t bar_o_done = bar_q + 152;   // [3]: PV of tile j done
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kBarOff + 176);
   int* ids_smem = reinterpret_cast<int*>(smem + kIdsOff);      // [4 tiles][8 blocks]
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kBarOff + 172);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kBarOff + 180);
   float* red_max = reinterpret_cast<float*>(smem + kRedOff);   // [2 parity][2 half][128]
   float* red_sum = reinterpret_cast<float*>(smem + kRedOff2);  // [2 half][128]
 
@@ -223,9 +229,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(bar_v_full + 8 * k, 1);
       mbar_init(bar_v_empty + 8 * k, kCluster);
     }
-    for (int k = 0; k < 2; ++k) {
+    for (int k = 0; k < kNS; ++k) {
       mbar_init(bar_s_full + 8 * k, 1);
-      mbar_init(bar_s_free + 8 * k, kSoftmaxWarps);
       mbar_init(bar_p_full + 8 * k, kSoftmaxWarps);
       mbar_init(bar_o_done + 8 * k, 1);
     }
@@ -341,34 +346,34 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint64_t t_last = global_ns();  // time of the last issue
       while (ok && jp < nkt) {
         bool progressed = false;
-        // S(js) = Q K_js^T into score buffer js & 1, once K_js landed and the
-        // softmax has read that buffer's previous tile
+        // S(js) = Q K_js^T into score buffer js % 3, once K_js landed and PV
+        // of tile js-3 has read its P from that buffer
         if (js < nkt && mbar_test_wait(bar_k_full + 8 * (js % kNK), (js / kNK) & 1) &&
-            (js < 2 || mbar_test_wait(bar_s_free + 8 * (js & 1), ((js >> 1) - 1) & 1))) {
+            (js < kNS || mbar_test_wait(bar_o_done + 8 * (js % kNS), ((js / kNS) - 1) & 1))) {
           tc_fence_after();
           const uint32_t kt = sbase + kKOff + (js % kNK) * kTileBytes;
 #pragma unroll
           for (int ks = 0; ks < 8; ++ks) {
             const uint32_t koff = (ks >> 2) * kHalf + (ks & 3) * 32;
-            tc_mma_f16(tmem + (js & 1) * 128, smem_desc(sbase + kQOff + koff, 16, 1024),
+            tc_mma_f16(tmem + (js % kNS) * 128, smem_desc(sbase + kQOff + koff, 16, 1024),
                        smem_desc(kt + koff, 16, 1024), idesc_s, ks > 0);
           }
-          tc_commit(bar_s_full + 8 * (js & 1));
+          tc_commit(bar_s_full + 8 * (js % kNS));
           tc_commit_multicast(bar_k_empty + 8 * (js % kNK), kMask);
           ++js;
           progressed = true;
         }
         // O += P_jp V_jp once the softmax wrote P_jp and V_jp landed
-        if (jp < js && mbar_test_wait(bar_p_full + 8 * (jp & 1), (jp >> 1) & 1) &&
+        if (jp < js && mbar_test_wait(bar_p_full + 8 * (jp % kNS), (jp / kNS) & 1) &&
             mbar_test_wait(bar_v_full + 8 * (jp % kNV), (jp / kNV) & 1)) {
           tc_fence_after();
           const uint32_t vt = sbase + kVOff + (jp % kNV) * kTileBytes;
 #pragma unroll
           for (int ks = 0; ks < 8; ++ks)
-            tc_mma_f16_tmem_a(tmem + kTmemO, tmem + kTmemP + (jp & 1) * 64 + ks * 8,
+            tc_mma_f16_tmem_a(tmem + kTmemO, tmem + (jp % kNS) * 128 + (ks >> 2) * 64 + (ks & 3) * 8,
                               smem_desc(vt + ks * 16 * 128, kHalf, 1024), idesc_o,
                               (jp > 0 || ks > 0) ? 1u : 0u);
-          tc_commit(bar_o_done + 8 * (jp & 1));
+          tc_commit(bar_o_done + 8 * (jp % kNS));
           tc_commit_multicast(bar_v_empty + 8 * (jp % kNV), kMask);
           ++jp;
           progressed = true;
@@ -395,13 +400,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     float m_run = -INFINITY, l_run = 0.f;
     uint32_t v[64];
     for (int j = 0; j < nkt; ++j) {
-      const int b = j & 1;
-      wait_or_abort_warp(bar_s_full + 8 * b, (j >> 1) & 1, abort_flag, a.err);
+      const int b = j & 1;        // row maximum exchange buffer
+      const int b3 = j % kNS;     // score buffer
+      wait_or_abort_warp(bar_s_full + 8 * b3, (j / kNS) & 1, abort_flag, a.err);
       tc_fence_after();
-      tmem_ld64(tmem + lane_off + b * 128 + hc * 64, v);
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar_s_free + 8 * b);
+      tmem_ld64(tmem + lane_off + b3 * 128 + hc * 64, v);
 
       const int kb = j * kTileKeys + hc * 64;
       const int nvis = lim - kb + 1;  // visible columns of this half (may be <= 0 or > 64)
@@ -458,7 +461,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       // O is rescaled only when a row maximum moved; then PV of the previous
       // tile must have landed first
       if (j >= 1 && __any_sync(0xffffffffu, alpha != 1.f)) {
-        wait_or_abort_warp(bar_o_done + 8 * ((j - 1) & 1), ((j - 1) >> 1) & 1, abort_flag, a.err);
+        wait_or_abort_warp(bar_o_done + 8 * ((j - 1) % kNS), ((j - 1) / kNS) & 1, abort_flag,
+                           a.err);
         tc_fence_after();
         const uint32_t ocol = tmem + lane_off + kTmemO + hc * 64;
 #pragma unroll
@@ -470,13 +474,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           tmem_st32(ocol + 32 * cc, w);
         }
       }
-      // P buffer j & 1 is free once PV of tile j-2 has read it
-      if (j >= 2) {
-        wait_or_abort_warp(bar_o_done + 8 * (j & 1), ((j >> 1) - 1) & 1, abort_flag, a.err);
-        tc_fence_after();
-      }
-      // keys hc*64 .. hc*64+63 of row r = columns hc*32 .. +31 of P buffer j & 1
-      tmem_st32(tmem + lane_off + kTmemP + (j & 1) * 64 + hc * 32, pk);
+      // keys hc*64 .. hc*64+63 of row r -> columns hc*64 .. hc*64+31 of score
+      // buffer b3, which this warp alone has read (its partner's half is
+      // disjoint); PV of tile j-3 finished with it before S(j) was computed
+      tmem_st32(tmem + lane_off + b3 * 128 + hc * 64, pk);
       // the sequence's last block may end inside this tile: its slots past
       // seq_len hold no token and must not reach the PV product
       if ((n & (kBlockSize - 1)) != 0) {
@@ -498,11 +499,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       fence_proxy_async_smem();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(bar_p_full + 8 * (j & 1));
+      if (lane == 0) mbar_arrive(bar_p_full + 8 * b3);
     }
 
     // ---- epilogue: O / l -> bf16, and lse
-    wait_or_abort_warp(bar_o_done + 8 * ((nkt - 1) & 1), ((nkt - 1) >> 1) & 1, abort_flag, a.err);
+    wait_or_abort_warp(bar_o_done + 8 * ((nkt - 1) % kNS), ((nkt - 1) / kNS) & 1, abort_flag,
+                       a.err);
     tc_fence_after();
     red_sum[hc * 128 + r] = l_run;
     named_barrier(1 + qd, 64);
