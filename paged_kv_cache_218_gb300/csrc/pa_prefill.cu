@@ -20,11 +20,12 @@
 //    rings of two K and two V tiles (a K tile is free once its scores are
 //    done, a V tile only once its PV product is).  Deeper rings only lengthen
 //    the queue: per-tile traces show each SM taking in K/V at about 57 GB/s
-//    whatever the depth, the arrival latency growing with the tiles in flight.  Warp 8 issues the tensor-core work from one thread:
-//    S = Q K^T into one of two tensor-memory score buffers (tcgen05.mma,
-//    M = N = 128, K = 16, bf16 in, fp32 accumulate) and O += P V into a third
-//    region.  Warps 0-7 run the softmax: two warps per tensor-memory lane
-//    quadrant, each owning 64 of a row's 128 score columns.
+//    whatever the depth, the arrival latency growing with the tiles in
+//    flight.  Warp 8 issues the tensor-core work from one thread: S = Q K^T
+//    into one of three tensor-memory score buffers (tcgen05.mma, M = N = 128,
+//    K = 16, bf16 in, fp32 accumulate) and O += P V into a fourth region.
+//    Warps 0-7 run the softmax: two warps per tensor-memory lane quadrant,
+//    each owning 64 of a row's 128 score columns.
 //  * Three score buffers.  Scores of a tile can be computed as soon as its K
 //    tile lands (while the softmax still works on the two before it), so a K
 //    tile leaves its ring slot soon after it arrives: with two rings of two,
