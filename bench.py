@@ -681,11 +681,23 @@ def run_oracle(w, min_seconds):
 
 
 def cpu_baseline_obj(w, min_seconds):
+    """The oracle on every host core (OpenMP over sequence and kv head), then
+    a bounded single-threaded sample of the same work (at most a few seconds,
+    at least one pass)."""
+    import oracle
     sec, passes, cores, kvb = run_oracle(w, min_seconds)
+    n_all = oracle.num_threads()
+    oracle.set_num_threads(1)
+    try:
+        sec1, passes1, _, _ = run_oracle(w, min(3.0, min_seconds / 4))
+    finally:
+        oracle.set_num_threads(n_all)
     return {"value": kvb / sec / 1e9, "unit": "GB/s", "cores": cores, "kind": "oracle",
             "sample": f"fp64 oracle decode over the whole batch ({w.num_decode_seqs} seqs, "
                       f"{kvb / 1e6:.1f} MB of bf16 KV), repeated {passes}x in {sec * passes:.1f} s; "
-                      f"slot scatter excluded", "tokens_per_s": w.num_decode_seqs / sec}
+                      f"slot scatter excluded", "tokens_per_s": w.num_decode_seqs / sec,
+            "single_thread": {"value": kvb / sec1 / 1e9, "unit": "GB/s", "cores": 1,
+                              "sample": f"the same pass repeated {passes1}x on one thread"}}
 
 
 def block_manager_timing(steps=64, seqs=256, group=4, system_tokens=256):

@@ -71,3 +71,16 @@ def test_reference_arm_under_two_ranks_prints_from_rank_0_only():
     lines = _lines(r.stdout)
     assert len(lines) == 1, r.stdout
     _check_line(lines[0], steps=2, warmup=3, n_gpus=2)
+
+
+def test_cpu_baseline_reports_all_cores_and_one_thread():
+    import bench
+    import oracle
+    from paged_kv_cache_218_gb300 import workload as W
+    n_all = oracle.num_threads()
+    cb = bench.cpu_baseline_obj(W.tiny(), 0.2)
+    assert oracle.num_threads() == n_all  # the thread count is restored
+    assert cb["kind"] == "oracle" and cb["unit"] == "GB/s" and cb["value"] > 0
+    assert cb["cores"] == n_all
+    st = cb["single_thread"]
+    assert st["cores"] == 1 and st["unit"] == "GB/s" and st["value"] > 0 and st["sample"]
