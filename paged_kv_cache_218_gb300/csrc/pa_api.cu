@@ -70,8 +70,24 @@ bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p
 // lands as [head][token][64 columns].
 // elem = 1: an E4M3 pool (bytes); only the all-heads view, whose box is a
 // whole 128-byte token row (head_dim 128) x 16 tokens x Hkv heads.
+// rows == kPool2D: the pool as a 2-D tensor (Hkv * D columns, tokens), box =
+// 64 columns x 16 tokens: one head's half of a block, as the 3-D box with
+// rows = 16 but cheaper for the TMA unit.
+constexpr int kPool2D = 1 << 20;
 int encode_pool_map_uncached(CUtensorMap* m, const void* pool, int64_t num_blocks, int Hkv, int D,
                              int rows, int elem) {
+  if (rows == kPool2D) {
+    cuuint64_t dims2[2] = {static_cast<cuuint64_t>(Hkv) * D,
+                           static_cast<cuuint64_t>(num_blocks) * kBlockSize};
+    cuuint64_t strides2[1] = {static_cast<cuuint64_t>(Hkv) * D * elem};
+    cuuint32_t box2[2] = {static_cast<cuuint32_t>(128 / elem), static_cast<cuuint32_t>(kBlockSize)};
+    cuuint32_t estr2[2] = {1, 1};
+    CUresult r = g_encode(m, elem == 1 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+                          2, const_cast<void*>(pool), dims2, strides2, box2, estr2,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? PA_OK : PA_ERR_CUDA;
+  }
   cuuint64_t dims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(Hkv),
                         static_cast<cuuint64_t>(num_blocks) * kBlockSize};
   cuuint64_t strides[2] = {static_cast<cuuint64_t>(D) * elem,
@@ -882,8 +898,8 @@ static int prefill_impl(void* out, const void* q, const void* k_cache, const voi
   a.scale_log2 = scale * 1.4426950408889634f;
   CUtensorMap tm_q, tm_k, tm_v;
   if (encode_q_map(&tm_q, q, total_q_tokens, num_q_heads, head_dim, group, tokens_per_tile) ||
-      encode_pool_map(&tm_k, k_cache, num_blocks, num_kv_heads, head_dim, kBlockSize) ||
-      encode_pool_map(&tm_v, v_cache, num_blocks, num_kv_heads, head_dim, kBlockSize))
+      encode_pool_map(&tm_k, k_cache, num_blocks, num_kv_heads, head_dim, kPool2D) ||
+      encode_pool_map(&tm_v, v_cache, num_blocks, num_kv_heads, head_dim, kPool2D))
     return PA_ERR_CUDA;
   const int64_t tiles = static_cast<int64_t>(a.tiles_per_chunk) * num_chunks * num_kv_heads;
   return launch_prefill(a, &tm_q, &tm_k, &tm_v, static_cast<int>(tiles),

@@ -12,7 +12,7 @@ namespace pa {
 constexpr int kBlockSize = 16;
 constexpr int kMaxGroup = 8;            // q heads per kv head handled by one MMA column tile
 constexpr int kMaxSeqsBalanced = 16000; // per-CTA prefix of block counts lives in shared memory
-constexpr int kMaxCluster = 4;          // prefill: most query tiles per cluster
+constexpr int kMaxCluster = 2;          // prefill: most query tiles per cluster (a CTA pair)
 
 enum DecodeMode : int {
   kModeSinglePass = 0,  // one work item per (sequence, kv head)
@@ -135,7 +135,7 @@ bool decode_supported(int head_dim, int num_kv_heads, int num_q_heads, int mode,
 cudaError_t launch_merge(const MergeArgs& a, cudaStream_t stream);
 cudaError_t launch_prefill(const PrefillArgs& a, const CUtensorMap* tm_q, const CUtensorMap* tm_k,
                            const CUtensorMap* tm_v, int grid_tiles, cudaStream_t stream);
-size_t prefill_smem_bytes();
+size_t prefill_smem_bytes(bool co_scheduled);
 bool cascade_shape(int num_kv_heads, int group, int max_group, int* kv_per_cta, int* warps_per_kv,
                    int* stages);
 cudaError_t launch_cascade_prefix(const CascadeArgs& a, const CUtensorMap* tm_k,
