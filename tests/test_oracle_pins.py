@@ -219,11 +219,13 @@ def test_paged_equals_contiguous_layout():
 
 
 def test_aliasing_with_copy_on_write_equals_private_copies():
+    """The whole copy-on-write batch through oracle.decode (the function every
+    GPU parity test compares against): outputs and lse are bit for bit those
+    of the same batch with every aliased block replaced by a private copy."""
     w = W.cow_mix()
     assert len(w.cow_pairs) > 0 and w.refcount.max() > 1
     kc, vc = _scattered(w)
-    sel = [(s, h) for s in range(0, 256, 5) for h in (0, 37)]
-    out, _ = oracle.decode_pairs(w.q, kc, vc, w.block_tables, w.seq_lens, w.scale, sel)
+    out, lse = oracle.decode(w.q, kc, vc, w.block_tables, w.seq_lens, w.scale)
     # de-alias: give every (sequence, logical block) its own physical block
     S, mb = w.block_tables.shape
     need = [(int(n) + 15) // 16 for n in w.seq_lens]
@@ -238,40 +240,92 @@ def test_aliasing_with_copy_on_write_equals_private_copies():
             vc2[r] = vc[w.block_tables[s, j]]
             bt2[s, j] = r
             r += 1
-    out2, _ = oracle.decode_pairs(w.q, kc2, vc2, bt2, w.seq_lens, w.scale, sel)
+    # the batch really shares blocks: fewer physical blocks than logical ones
+    assert len(np.unique(w.block_tables[w.block_tables >= 0])) < total
+    out2, lse2 = oracle.decode(w.q, kc2, vc2, bt2, w.seq_lens, w.scale)
     assert np.array_equal(out, out2)
+    assert np.array_equal(lse, lse2)
 
 
 def test_cow_copy_protects_the_other_members():
     """Without the copy, a member's scatter into a shared block would change
-    what the other members of its group read."""
+    what the other members of its group read (whole batch, oracle.decode)."""
     w = W.cow_mix()
-    s_cow = None
-    for s, n in enumerate(w.seq_lens):
-        j = (int(n) - 1) // 16
-        if any(int(w.block_tables[s, j]) == int(d) for _, d in w.cow_pairs):
-            s_cow = s
-            break
-    assert s_cow is not None
     kc, vc = _scattered(w)
-    g0 = (s_cow // 4) * 4
-    others = [s for s in range(g0, g0 + 4) if s != s_cow]
-    sel = [(s, 0) for s in others]
-    good, _ = oracle.decode_pairs(w.q, kc, vc, w.block_tables, w.seq_lens, w.scale, sel)
-    # what would happen without copy-on-write: write through the shared block
+    good, _ = oracle.decode(w.q, kc, vc, w.block_tables, w.seq_lens, w.scale)
+    # what would happen without copy-on-write: write through the shared blocks
     bt_bad = w.block_tables.copy()
     for src, dst in w.cow_pairs:
         bt_bad[bt_bad == dst] = src
     slots_bad = w.slot_mapping.copy()
-    n = int(w.seq_lens[s_cow])
-    slots_bad[s_cow] = int(bt_bad[s_cow, (n - 1) // 16]) * 16 + (n - 1) % 16
+    writers = []
+    for s, n in enumerate(w.seq_lens):
+        j = (int(n) - 1) // 16
+        if any(int(w.block_tables[s, j]) == int(d) for _, d in w.cow_pairs):
+            slots_bad[s] = int(bt_bad[s, j]) * 16 + (int(n) - 1) % 16
+            writers.append(s)
+    assert writers
     kb, vb = oracle.reshape_and_cache(w.key, w.value, w.k_cache, w.v_cache, slots_bad)
-    bad, _ = oracle.decode_pairs(w.q, kb, vb, bt_bad, w.seq_lens, w.scale, sel)
-    readers = [i for i, s in enumerate(others)
-               if int(w.seq_lens[s]) > (n - 1) and
-               int(bt_bad[s, (n - 1) // 16]) == int(bt_bad[s_cow, (n - 1) // 16])]
-    if readers:
-        assert any(not np.array_equal(good[i], bad[i]) for i in readers)
+    bad, _ = oracle.decode(w.q, kb, vb, bt_bad, w.seq_lens, w.scale)
+    # a group member that reads the slot a writer overwrote sees other data
+    readers = set()
+    for s_w in writers:
+        n = int(w.seq_lens[s_w])
+        blk = int(bt_bad[s_w, (n - 1) // 16])
+        g0 = (s_w // 4) * 4
+        for s in range(g0, g0 + 4):
+            if s != s_w and int(w.seq_lens[s]) > n - 1 and int(bt_bad[s, (n - 1) // 16]) == blk:
+                readers.add(s)
+    assert readers
+    for s in readers:
+        assert not np.array_equal(good[s], bad[s])
+    # members whose blocks no writer touched read the same as with the copies
+    touched = {int(bt_bad[s_w, (int(w.seq_lens[s_w]) - 1) // 16]) for s_w in writers}
+    for s in range(len(w.seq_lens)):
+        nb = (int(w.seq_lens[s]) + 15) // 16
+        if s not in writers and not touched & set(int(b) for b in bt_bad[s, :nb]):
+            assert np.array_equal(good[s], bad[s])
+
+
+@pytest.mark.parametrize("make", [W.llama3_8b_layer, W.cow_mix])
+def test_decode_pairs_equals_decode_rows(make):
+    """oracle.decode_pairs (the sampled form used at full size) returns, bit for
+    bit, the rows of oracle.decode for each listed (sequence, q head): pins its
+    kv-head mapping and its output row.  Pairs include both sides of every
+    group boundary, duplicates and an unsorted order."""
+    w = make()
+    kc, vc = _scattered(w)
+    out, lse = oracle.decode(w.q, kc, vc, w.block_tables, w.seq_lens, w.scale)
+    S, Hq = w.q.shape[:2]
+    G = Hq // w.k_cache.shape[2]
+    rng = np.random.default_rng(7)
+    sel = [(int(s), g * G + d) for s in rng.choice(S, 24, replace=False)
+           for g in range(Hq // G) for d in (0, G - 1)]
+    sel += [(int(s), int(h)) for s, h in zip(rng.integers(0, S, 200), rng.integers(0, Hq, 200))]
+    sel += sel[:10]
+    sel = [sel[i] for i in rng.permutation(len(sel))]
+    assert len(sel) >= 400
+    po, pl = oracle.decode_pairs(w.q, kc, vc, w.block_tables, w.seq_lens, w.scale, sel)
+    for i, (s, h) in enumerate(sel):
+        assert np.array_equal(po[i], out[s, h]), (s, h)
+        assert pl[i] == lse[s, h], (s, h)
+
+
+def test_decode_pairs_brute_force_at_group_boundaries():
+    """decode_pairs against a numpy full-matrix restatement at group 8 (the
+    copy-on-write mix), for the first and last q head of several kv heads."""
+    w = W.cow_mix()
+    kc, vc = _scattered(w)
+    G = w.q.shape[1] // w.k_cache.shape[2]
+    sel = [(s, h) for s in (0, 3, 101, 255) for h in (0, G - 1, G, 3 * G + 7, 63)]
+    po, pl = oracle.decode_pairs(w.q, kc, vc, w.block_tables, w.seq_lens, w.scale, sel)
+    for i, (s, h) in enumerate(sel):
+        n = int(w.seq_lens[s])
+        K = ind.gather(kc, w.block_tables[s], h // G, n)
+        V = ind.gather(vc, w.block_tables[s], h // G, n)
+        ref, ref_lse = ind.softmax_attention_np(ind.to_f64(w.q[s, h]), K, V, w.scale)
+        np.testing.assert_allclose(po[i], ref, rtol=1e-11, atol=1e-12)
+        assert abs(pl[i] - ref_lse) < 1e-11
 
 
 # ---------------------------------------------------------------- split + merge
