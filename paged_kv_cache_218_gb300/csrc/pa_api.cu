@@ -524,16 +524,14 @@ size_t pa_decode_workspace_size(int num_seqs, int num_q_heads, int num_kv_heads,
   return balanced_workspace_bytes(num_sms, num_q_heads, head_dim);
 }
 
-// pa_decode and pa_decode_fp8: the same launch; kv_fp8 selects E4M3 pools.
-static int decode_impl(void* out, const void* q, const void* k_cache, const void* v_cache,
-                       const float* k_scales, const float* v_scales, bool kv_fp8,
-                       const int32_t* block_tables, int max_blocks_per_seq,
-                       const int32_t* seq_lens, int num_seqs, int num_q_heads,
-                       int num_kv_heads, int head_dim, int block_size, int64_t num_blocks,
-                       float scale, int partition_tokens, float* out_lse, void* workspace,
-                       size_t workspace_bytes, void* stream, const int32_t* start_blocks = nullptr,
-                       const float* init_o = nullptr, const float* init_lse = nullptr,
-                       int grid_override = 0) {
+// Argument checks of a decode call (everything but the workspace), made
+// before anything is enqueued.  PA_OK with num_seqs == 0: nothing to do.
+static int decode_check(const void* out, const void* q, const void* k_cache, const void* v_cache,
+                        const float* k_scales, const float* v_scales, bool kv_fp8,
+                        const int32_t* block_tables, int max_blocks_per_seq,
+                        const int32_t* seq_lens, int num_seqs, int num_q_heads,
+                        int num_kv_heads, int head_dim, int block_size, int64_t num_blocks,
+                        float scale, int partition_tokens, const float* out_lse) {
   if (int rc = check_shape(num_q_heads, num_kv_heads, head_dim, block_size)) return rc;
   if (kv_fp8 && head_dim != 128) return PA_ERR_UNSUPPORTED;
   if (num_seqs < 0 || max_blocks_per_seq <= 0 || num_blocks <= 0) return PA_ERR_INVALID;
@@ -551,6 +549,25 @@ static int decode_impl(void* out, const void* q, const void* k_cache, const void
   if (mode == kModeBalanced && num_seqs > kMaxSeqsBalanced) return PA_ERR_UNSUPPORTED;
   if (!decode_supported(head_dim, num_kv_heads, num_q_heads, mode, num_seqs, kv_fp8))
     return PA_ERR_UNSUPPORTED;
+  return PA_OK;
+}
+
+// pa_decode and pa_decode_fp8: the same launch; kv_fp8 selects E4M3 pools.
+static int decode_impl(void* out, const void* q, const void* k_cache, const void* v_cache,
+                       const float* k_scales, const float* v_scales, bool kv_fp8,
+                       const int32_t* block_tables, int max_blocks_per_seq,
+                       const int32_t* seq_lens, int num_seqs, int num_q_heads,
+                       int num_kv_heads, int head_dim, int block_size, int64_t num_blocks,
+                       float scale, int partition_tokens, float* out_lse, void* workspace,
+                       size_t workspace_bytes, void* stream, const int32_t* start_blocks = nullptr,
+                       const float* init_o = nullptr, const float* init_lse = nullptr,
+                       int grid_override = 0) {
+  if (int rc = decode_check(out, q, k_cache, v_cache, k_scales, v_scales, kv_fp8, block_tables,
+                            max_blocks_per_seq, seq_lens, num_seqs, num_q_heads, num_kv_heads,
+                            head_dim, block_size, num_blocks, scale, partition_tokens, out_lse))
+    return rc;
+  if (num_seqs == 0) return PA_OK;
+  const int mode = decode_mode(partition_tokens);
   DeviceInfo* d;
   if (int rc = current_device_info(&d)) return rc;
 
@@ -766,8 +783,12 @@ int pa_decode_noalloc(void* out, const void* q, const void* k_cache, const void*
                       const int32_t* seq_lens, int num_seqs, int num_q_heads, int num_kv_heads,
                       int head_dim, int block_size, int64_t num_blocks, float scale,
                       float* out_lse, void* stream) {
-  if (int rc = check_shape(num_q_heads, num_kv_heads, head_dim, block_size)) return rc;
-  if (num_seqs < 0 || max_blocks_per_seq <= 0 || num_blocks <= 0) return PA_ERR_INVALID;
+  // every argument is checked before the scratch is touched: a rejected call
+  // enqueues nothing
+  if (int rc = decode_check(out, q, k_cache, v_cache, nullptr, nullptr, false, block_tables,
+                            max_blocks_per_seq, seq_lens, num_seqs, num_q_heads, num_kv_heads,
+                            head_dim, block_size, num_blocks, scale, 0, out_lse))
+    return rc;
   if (num_seqs == 0) return PA_OK;
   DeviceInfo* d;
   if (int rc = current_device_info(&d)) return rc;
