@@ -76,9 +76,10 @@ def source_hash(files):
     return h.hexdigest()[:16]
 
 
-def profile_traffic(kernel_files, summary: str):
-    """Per-launch DRAM bytes recorded by an ncu capture in profiles/, valid only
-    while the kernel sources still hash to the value the summary was taken at."""
+def profile_traffic(kernel_files, summary: str, key: str = "traffic_bytes_per_launch"):
+    """A figure recorded by an ncu capture in profiles/ (by default the per-launch
+    DRAM bytes), valid only while the kernel sources still hash to the value
+    the summary was taken at; None otherwise."""
     try:
         fields = {}
         for line in open(os.path.join(ROOT, "profiles", summary)):
@@ -87,7 +88,7 @@ def profile_traffic(kernel_files, summary: str):
                 fields[k.strip()] = v.strip().strip("`")
         if fields.get("source_sha256_16") != source_hash(kernel_files):
             return None
-        return float(fields["traffic_bytes_per_launch"])
+        return float(fields[key])
     except Exception:
         return None
 
@@ -395,9 +396,10 @@ def run_gpu(args, rank, world, local_rank):
         else None
     casc = measure_cascade(args, w, reps, dev, pa, CASCADE_GROUP[args.config]) \
         if (use_graphs and args.config in CASCADE_GROUP) else None
+    prefill = measure_prefill_chunk(args, dev, pa) if use_graphs else None
     return dict(w=w, elapsed_ms=elapsed_ms, kv_all=kv_all, dec_ms=dec_ms, chunk_ms=chunk_ms,
                 clocks=clocks, e2e=e2e, launches=launches_per_step * K, graphs=use_graphs,
-                fp8=fp8, cascade=casc)
+                fp8=fp8, cascade=casc, prefill=prefill)
 
 
 def measure_fp8_decode(args, w, reps, ws, dev, pa):
@@ -453,6 +455,61 @@ def measure_fp8_decode(args, w, reps, ws, dev, pa):
             "kv_bytes_per_token": 2 * Hkv * D, "tokens_per_s": S / (ms * 1e-3),
             "achieved_gbs": alg / (ms * 1e-3) / 1e9,
             "scales": "per kv head, max |x| / 448"}
+
+
+PREFILL_REPLICAS = 16  # chunk replicas in rotation: ~290 MB, more than L2
+
+
+def measure_prefill_chunk(args, dev, pa):
+    """The Sarathi batch's prefill chunk alone (512 queries at positions
+    1536-2047 attending causally over 2048 paged keys; Llama-3-8B heads) on
+    the tensor cores: PREFILL_REPLICAS independent copies of the chunk's
+    state rotate, so no launch finds its K/V or queries in L2, timed as
+    back-to-back launches from CUDA graphs of one launch per copy."""
+    import torch
+
+    from paged_kv_cache_218_gb300 import workload as W
+    w = W.sarathi_hybrid(num_decode=0)
+    reps = [Replica(w, dev)]
+    for _ in range(PREFILL_REPLICAS - 1):
+        reps.append(Replica(w, dev, src=reps[0]))
+    T = int(w.cu_q_lens[w.num_chunks])
+    max_q = int(max(w.cu_q_lens[1:] - w.cu_q_lens[:-1]))
+    for r in reps:
+        pa.pa_reshape_and_cache(r.key, r.value, r.k_cache, r.v_cache, r.slot_mapping)
+
+    def chunk(r):
+        pa.pa_prefill_chunk(r.out_chunk, r.q[:T], r.k_cache, r.v_cache,
+                            r.block_tables[:w.num_chunks], r.cu, r.qs,
+                            r.seq_lens[:w.num_chunks], max_q, w.scale)
+
+    for _ in range(3):
+        for r in reps:
+            chunk(r)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        for r in reps:
+            chunk(r)
+    g.replay()
+    torch.cuda.synchronize()
+    n = max(1, min(args.steps, args.kernel_steps) // PREFILL_REPLICAS)
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(n):
+        g.replay()
+    b.record()
+    torch.cuda.synchronize()
+    if pa.pa_device_error_flags() != 0:
+        raise RuntimeError("device error flags set by the prefill chunk")
+    ms = a.elapsed_time(b) / (n * PREFILL_REPLICAS)
+    del reps
+    return {"launch_ms": ms, "gflop": chunk_flops(w) / 1e9, "kernel": "prefill_kernel<2>",
+            "workload": "prefill chunk of 512 queries at positions 1536-2047 over its 2048 "
+                        "paged keys, 32 q / 8 kv heads, head_dim 128 (the Sarathi batch's chunk)",
+            "l2": f"{PREFILL_REPLICAS} copies of the chunk's K/V, queries and output in rotation "
+                  "(~290 MB) > 129 MB L2",
+            "timing": f"back-to-back launches from CUDA graphs of {PREFILL_REPLICAS}; "
+                      "time / launches"}
 
 
 # batches whose consecutive sequences share prefix blocks, and their group size
@@ -964,16 +1021,16 @@ def main():
                               peak_source=f"{peak_src} (hbm_gbs)",
                               tokens_per_s_vs_bf16=f["tokens_per_s"] /
                               (w.num_decode_seqs / (res["dec_ms"] * 1e-3)))
+    if res.get("prefill") is not None:
+        pf = res["prefill"]
+        tf = pf["gflop"] / pf["launch_ms"]  # GFLOP / ms = TFLOP/s
+        line["prefill_chunk"] = dict(pf, bound="tensor", tflops=tf, peak=bf16,
+                                     frac_of_bf16_peak=tf / bf16,
+                                     peak_source=f"{peak_src} (bf16_tflops, burst: timed alone)",
+                                     tensor_pipe_ncu=profile_traffic(
+                                         ["pa_prefill.cu", "pa_ptx.cuh", "pa_internal.h"],
+                                         "prefill_kernel_sarathi_chunk.md", "tensor_pipe_active_pct"))
     if res["chunk_ms"] is not None:
-        fl = chunk_flops(w)
-        line["prefill_chunk"] = {"tflops": fl / (res["chunk_ms"] * 1e-3) / 1e12,
-                                 "frac_of_bf16_peak": fl / (res["chunk_ms"] * 1e-3) / 1e12 / bf16,
-                                 "peak": bf16, "gflop": fl / 1e9, "launch_ms": res["chunk_ms"],
-                                 "peak_source": f"{peak_src} (bf16_tflops)",
-                                 "timing": ("back-to-back chunk-only launches (graphs of "
-                                            f"{args.replicas}); time / launches") if res["graphs"]
-                                           else "CUDA events around each chunk launch while "
-                                                "the decode runs beside it"}
         if res["graphs"]:
             line["hybrid_step"] = {
                 "step_ms": step_ms, "decode_alone_ms": res["dec_ms"],
