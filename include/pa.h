@@ -374,6 +374,35 @@ int pa_validate_metadata(const int32_t *block_tables, int max_blocks_per_seq,
  */
 int pa_device_error_flags(unsigned int *flags, int reset);
 
+/*
+ * Test entry points of the failure path (no product call needs them).  Each
+ * makes one launch of the kernel its name gives, with the same arguments as
+ * pa_decode (workspace and mode included; no lse) / pa_prefill_chunk (no
+ * lse), in which the producer / loader warps issue no load at all and every
+ * mbarrier wait is bounded by wait_limit_us (1 .. 2,000,000 us) instead of
+ * the default two seconds.  Every wait therefore runs out with no copy in
+ * flight: the kernel sets PA_DEVERR_TIMEOUT, skips the rest of its waits,
+ * frees its tensor memory and returns; the outputs are unspecified.  The
+ * call itself returns PA_OK once launched (PA_ERR_INVALID for a limit out of
+ * range, or any status the plain call would return).  A decode's balanced-
+ * split tickets are left at zero, so the same workspace serves the next
+ * call.  The pages have no counterpart: these exist to exercise the kernels'
+ * bounded waits on a GPU without faulting or hanging it.
+ */
+int pa_test_decode_stalled(void *out, const void *q, const void *k_cache, const void *v_cache,
+                           const int32_t *block_tables, int max_blocks_per_seq,
+                           const int32_t *seq_lens, int num_seqs, int num_q_heads,
+                           int num_kv_heads, int head_dim, int block_size, int64_t num_blocks,
+                           float scale, int partition_tokens, void *workspace,
+                           size_t workspace_bytes, unsigned int wait_limit_us, void *stream);
+int pa_test_prefill_stalled(void *out, const void *q, const void *k_cache, const void *v_cache,
+                            const int32_t *block_tables, int max_blocks_per_seq,
+                            const int32_t *cu_q_lens, const int32_t *q_start_pos,
+                            const int32_t *seq_lens, int num_chunks, int total_q_tokens,
+                            int max_q_len, int num_q_heads, int num_kv_heads, int head_dim,
+                            int block_size, int64_t num_blocks, float scale,
+                            unsigned int wait_limit_us, void *stream);
+
 #ifdef __cplusplus
 }
 #endif

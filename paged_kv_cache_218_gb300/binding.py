@@ -64,6 +64,10 @@ _SIGS = {
     "pa_hybrid_attention": ([_P, _P, _P, _I, _P, _P, _P, _I, _I, _I, _P,
                              _P, _P, _P, _I, _P, _I, _P,
                              _P, _P, _I, _I, _I, _I, _L, _F, _I, _P, _S, _P], _I),
+    "pa_test_decode_stalled": ([_P, _P, _P, _P, _P, _I, _P, _I, _I, _I, _I, _I, _L, _F, _I, _P,
+                                _S, ctypes.c_uint, _P], _I),
+    "pa_test_prefill_stalled": ([_P, _P, _P, _P, _P, _I, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I,
+                                 _L, _F, ctypes.c_uint, _P], _I),
 }
 for _name, (_args, _res) in _SIGS.items():
     _fn = getattr(_lib, _name)
@@ -380,3 +384,48 @@ def pa_device_error_flags(reset: bool = True) -> int:
     v = ctypes.c_uint(0)
     _check("pa_device_error_flags", _lib.pa_device_error_flags(ctypes.byref(v), int(reset)))
     return int(v.value)
+
+
+# ---------------------------------------------------------------- failure-path tests
+
+def pa_test_decode_stalled(out, q, k_cache, v_cache, block_tables, seq_lens, scale,
+                           partition_tokens=0, workspace=None, wait_limit_us=1000,
+                           stream=None) -> None:
+    """One decode launch whose producer issues no load, every wait bounded by
+    wait_limit_us: the kernel must report PA_DEVERR_TIMEOUT and return."""
+    _need(out, "out", torch.bfloat16, 3)
+    _need(q, "q", torch.bfloat16, 3)
+    _need(k_cache, "k_cache", torch.bfloat16, 4)
+    _need(v_cache, "v_cache", torch.bfloat16, 4)
+    _need(block_tables, "block_tables", torch.int32, 2)
+    _need(seq_lens, "seq_lens", torch.int32, 1)
+    S, Hq, D = q.shape
+    nb, bs, Hkv, _ = k_cache.shape
+    _check("pa_test_decode_stalled", _lib.pa_test_decode_stalled(
+        _ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables),
+        block_tables.shape[1], _ptr(seq_lens), S, Hq, Hkv, D, bs, nb, float(scale),
+        int(partition_tokens), _ptr(workspace),
+        0 if workspace is None else workspace.numel() * workspace.element_size(), int(wait_limit_us),
+        _stream(stream)))
+
+
+def pa_test_prefill_stalled(out, q, k_cache, v_cache, block_tables, cu_q_lens, q_start_pos,
+                            seq_lens, max_q_len, scale, wait_limit_us=1000,
+                            stream=None) -> None:
+    """One prefill-chunk launch whose loaders issue no load, every wait
+    bounded by wait_limit_us: the kernel must report PA_DEVERR_TIMEOUT."""
+    _need(out, "out", torch.bfloat16, 3)
+    _need(q, "q", torch.bfloat16, 3)
+    _need(k_cache, "k_cache", torch.bfloat16, 4)
+    _need(v_cache, "v_cache", torch.bfloat16, 4)
+    _need(block_tables, "block_tables", torch.int32, 2)
+    for t, name in ((cu_q_lens, "cu_q_lens"), (q_start_pos, "q_start_pos"),
+                    (seq_lens, "seq_lens")):
+        _need(t, name, torch.int32, 1)
+    T, Hq, D = q.shape
+    nb, bs, Hkv, _ = k_cache.shape
+    C = q_start_pos.shape[0]
+    _check("pa_test_prefill_stalled", _lib.pa_test_prefill_stalled(
+        _ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables),
+        block_tables.shape[1], _ptr(cu_q_lens), _ptr(q_start_pos), _ptr(seq_lens), C, T,
+        int(max_q_len), Hq, Hkv, D, bs, nb, float(scale), int(wait_limit_us), _stream(stream)))

@@ -561,7 +561,7 @@ static int decode_impl(void* out, const void* q, const void* k_cache, const void
                        float scale, int partition_tokens, float* out_lse, void* workspace,
                        size_t workspace_bytes, void* stream, const int32_t* start_blocks = nullptr,
                        const float* init_o = nullptr, const float* init_lse = nullptr,
-                       int grid_override = 0) {
+                       int grid_override = 0, int stall_loads = 0, uint64_t wait_ns = 0) {
   if (int rc = decode_check(out, q, k_cache, v_cache, k_scales, v_scales, kv_fp8, block_tables,
                             max_blocks_per_seq, seq_lens, num_seqs, num_q_heads, num_kv_heads,
                             head_dim, block_size, num_blocks, scale, partition_tokens, out_lse))
@@ -592,6 +592,8 @@ static int decode_impl(void* out, const void* q, const void* k_cache, const void
   a.start_blocks = start_blocks;
   a.init_o = init_o;
   a.init_lse = init_lse;
+  a.stall_loads = stall_loads;
+  a.wait_ns = wait_ns;  // 0: the default limit
   int grid = decode_grid(d->num_sms, mode, a.group, kv_fp8);
   if (grid_override > 0) grid = grid_override < d->num_sms ? grid_override : d->num_sms;
   if (mode == kModeSinglePass) {
@@ -884,7 +886,7 @@ static int prefill_impl(void* out, const void* q, const void* k_cache, const voi
                         const int32_t* seq_lens, int num_chunks, int total_q_tokens, int max_q_len,
                         int num_q_heads, int num_kv_heads, int head_dim, int block_size,
                         int64_t num_blocks, float scale, float* out_lse, void* stream,
-                        unsigned int* done_ctr) {
+                        unsigned int* done_ctr, int stall_loads = 0, uint64_t wait_ns = 0) {
   bool done = false;
   if (int rc = prefill_check(out, q, k_cache, v_cache, block_tables, max_blocks_per_seq,
                              cu_q_lens, q_start_pos, seq_lens, num_chunks, total_q_tokens,
@@ -912,6 +914,8 @@ static int prefill_impl(void* out, const void* q, const void* k_cache, const voi
   a.group = group;
   a.after_decode = done_ctr ? 1 : 0;
   a.done_ctr = done_ctr;
+  a.stall_loads = stall_loads;
+  a.wait_ns = wait_ns;  // 0: the default limit
   const int tokens_per_tile = 128 / group;
   a.tiles_per_chunk = (max_q_len + tokens_per_tile - 1) / tokens_per_tile;
   const int cl = prefill_cluster(done_ctr != nullptr);
@@ -1002,6 +1006,34 @@ int pa_hybrid_attention(void* out_chunk, const void* q_chunk, const int32_t* chu
                       cu_q_lens, q_start_pos, chunk_seq_lens, num_chunks, total_q_tokens,
                       max_q_len, num_q_heads, num_kv_heads, head_dim, block_size, num_blocks,
                       scale, chunk_lse, stream, static_cast<unsigned int*>(workspace));
+}
+
+int pa_test_decode_stalled(void* out, const void* q, const void* k_cache, const void* v_cache,
+                           const int32_t* block_tables, int max_blocks_per_seq,
+                           const int32_t* seq_lens, int num_seqs, int num_q_heads,
+                           int num_kv_heads, int head_dim, int block_size, int64_t num_blocks,
+                           float scale, int partition_tokens, void* workspace,
+                           size_t workspace_bytes, unsigned int wait_limit_us, void* stream) {
+  if (wait_limit_us == 0 || wait_limit_us > 2000000u) return PA_ERR_INVALID;
+  return decode_impl(out, q, k_cache, v_cache, nullptr, nullptr, false, block_tables,
+                     max_blocks_per_seq, seq_lens, num_seqs, num_q_heads, num_kv_heads, head_dim,
+                     block_size, num_blocks, scale, partition_tokens, nullptr, workspace,
+                     workspace_bytes, stream, nullptr, nullptr, nullptr, 0, 1,
+                     static_cast<uint64_t>(wait_limit_us) * 1000u);
+}
+
+int pa_test_prefill_stalled(void* out, const void* q, const void* k_cache, const void* v_cache,
+                            const int32_t* block_tables, int max_blocks_per_seq,
+                            const int32_t* cu_q_lens, const int32_t* q_start_pos,
+                            const int32_t* seq_lens, int num_chunks, int total_q_tokens,
+                            int max_q_len, int num_q_heads, int num_kv_heads, int head_dim,
+                            int block_size, int64_t num_blocks, float scale,
+                            unsigned int wait_limit_us, void* stream) {
+  if (wait_limit_us == 0 || wait_limit_us > 2000000u) return PA_ERR_INVALID;
+  return prefill_impl(out, q, k_cache, v_cache, block_tables, max_blocks_per_seq, cu_q_lens,
+                      q_start_pos, seq_lens, num_chunks, total_q_tokens, max_q_len, num_q_heads,
+                      num_kv_heads, head_dim, block_size, num_blocks, scale, nullptr, stream,
+                      nullptr, 1, static_cast<uint64_t>(wait_limit_us) * 1000u);
 }
 
 int pa_validate_metadata(const int32_t* block_tables, int max_blocks_per_seq,

@@ -815,6 +815,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp == kConsumerWarps) {
     // ------------------------------------------------------------ producer
+    // a stalled test launch issues nothing: every consumer wait runs out
+    // with no copy in flight
+    if (a.stall_loads) return;
     if (lane == 0) {
       tma_prefetch_desc(&tm_k);
       tma_prefetch_desc(&tm_v);
@@ -826,7 +829,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto stage_q = [&](const Piece& pp, int qi) {
       if (lane != 0 || !ok) return;
       const int k = qi & 1;
-      if (qi >= 2 && !mbar_wait(bar_qempty + k * 8, ((qi >> 1) - 1) & 1)) {
+      if (qi >= 2 && !mbar_wait(bar_qempty + k * 8, ((qi >> 1) - 1) & 1, a.wait_ns)) {
         atomicOr(a.err, PA_DEVERR_TIMEOUT);
         ok = false;
         return;
@@ -890,7 +893,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t st = g % NS;
         const uint32_t fb = bar_full + st * 8;
         if (lane == 0) {
-          if (g >= static_cast<uint32_t>(NS) && !mbar_wait(bar_empty + st * 8, ((g / NS) - 1) & 1)) {
+          if (g >= static_cast<uint32_t>(NS) &&
+              !mbar_wait(bar_empty + st * 8, ((g / NS) - 1) & 1, a.wait_ns)) {
             atomicOr(a.err, PA_DEVERR_TIMEOUT);
             ok = false;
           } else {
@@ -978,7 +982,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // query fragments of the group (B operand: k = dim, n = head) from the
       // piece's staged query rows
       const int k = qi & 1;
-      if (!warp_flag(abort_flag) && !mbar_wait_warp(bar_qfull + k * 8, (qi >> 1) & 1)) {
+      if (!warp_flag(abort_flag) && !mbar_wait_warp(bar_qfull + k * 8, (qi >> 1) & 1, a.wait_ns)) {
         if (lane == 0) atomicOr(a.err, PA_DEVERR_TIMEOUT);
         *abort_flag = 1;
       }
@@ -1087,7 +1091,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (static_cast<int>(g % wph) != sub) continue;
         if (warp_flag(abort_flag)) continue;
         const uint32_t st = g % NS;
-        if (!mbar_wait_warp(bar_full + st * 8, (g / NS) & 1)) {
+        if (!mbar_wait_warp(bar_full + st * 8, (g / NS) & 1, a.wait_ns)) {
           if (lane == 0) atomicOr(a.err, PA_DEVERR_TIMEOUT);
           *abort_flag = 1;
           continue;
@@ -1100,7 +1104,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           // E4M3 pools' six): holding two of three stages starves the
           // producer (measured 48.8 -> 51.9 us on the Llama-3-8B layer).
           const uint32_t st2 = (g + 1) % NS;
-          if (!mbar_wait_warp(bar_full + st2 * 8, ((g + 1) / NS) & 1)) {
+          if (!mbar_wait_warp(bar_full + st2 * 8, ((g + 1) / NS) & 1, a.wait_ns)) {
             if (lane == 0) atomicOr(a.err, PA_DEVERR_TIMEOUT);
             *abort_flag = 1;
             __syncwarp();
@@ -1360,6 +1364,7 @@ cudaError_t launch_decode(DecodeArgs a, const CUtensorMap* tm_k, const CUtensorM
                           int head_dim, int grid, cudaStream_t stream) {
   const int pre = a.mode == kModeBalanced ? balanced_pre_ints(a.num_seqs) : 0;
   const int elem = a.kv_fp8 ? 1 : 2;
+  if (a.wait_ns == 0) a.wait_ns = kWaitLimitNs;
   a.warps_per_head = warps_per_head(a.num_kv_heads);
   a.stages = pick_stages(head_dim, a.num_kv_heads, a.num_q_heads, pre, elem);
   const size_t smem = make_layout(head_dim, a.num_kv_heads, a.num_q_heads, a.warps_per_head,

@@ -52,6 +52,8 @@ struct DecodeArgs {
   const int32_t* start_blocks;
   const float* init_o;
   const float* init_lse;
+  uint64_t wait_ns;  // limit of every mbarrier wait (normally kWaitLimitNs)
+  int stall_loads;   // test launch: the producer issues no load, every wait runs out
 };
 
 struct MergeArgs {
@@ -90,6 +92,8 @@ struct PrefillArgs {
   float scale_log2;
   int after_decode;          // co-scheduled behind a decode on the same stream
   unsigned int* done_ctr;    // after_decode: CTAs finished (self-resetting)
+  uint64_t wait_ns;          // limit of every mbarrier wait (normally kWaitLimitNs)
+  int stall_loads;           // test launch: the loaders issue no load, every wait runs out
 };
 
 struct CascadeArgs {

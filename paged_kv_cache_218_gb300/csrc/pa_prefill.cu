@@ -151,8 +151,8 @@ __host__ __device__ constexpr uint32_t instr_desc(uint32_t b_mn, uint32_t m) {
 // fences, so the polls keep the cheap CTA-scope form (a cluster-scope
 // acquire on every poll measured several hundred ns per loader step).
 template <int kPair>
-__device__ __forceinline__ bool bar_wait(uint32_t bar, uint32_t parity) {
-  return mbar_wait(bar, parity);
+__device__ __forceinline__ bool bar_wait(uint32_t bar, uint32_t parity, uint64_t limit_ns) {
+  return mbar_wait(bar, parity, limit_ns);
 }
 
 template <int kPair>
@@ -164,11 +164,11 @@ __device__ __forceinline__ bool bar_test(uint32_t bar, uint32_t parity) {
 // the CTA (so every role still reaches its barriers).
 template <int kPair>
 __device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, volatile int* abort,
-                                              unsigned int* err) {
+                                              const PrefillArgs& a) {
   if (*abort) return false;
-  if (bar_wait<kPair>(bar, parity)) return true;
+  if (bar_wait<kPair>(bar, parity, a.wait_ns)) return true;
   *abort = 1;
-  atomicOr(err, PA_DEVERR_TIMEOUT);
+  atomicOr(a.err, PA_DEVERR_TIMEOUT);
   return false;
 }
 
@@ -176,16 +176,16 @@ __device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, vol
 // memory loads and stores: the lanes reconverge and agree on the result.
 template <int kPair>
 __device__ __forceinline__ bool wait_or_abort_warp(uint32_t bar, uint32_t parity,
-                                                   volatile int* abort, unsigned int* err) {
+                                                   volatile int* abort, const PrefillArgs& a) {
   bool ok = !warp_flag(abort);
   if (ok) {
-    ok = bar_wait<kPair>(bar, parity);
+    ok = bar_wait<kPair>(bar, parity, a.wait_ns);
     __syncwarp();
     ok = __all_sync(0xffffffffu, ok);
   }
   if (!ok && !*abort) {
     *abort = 1;
-    if ((threadIdx.x & 31) == 0) atomicOr(err, PA_DEVERR_TIMEOUT);
+    if ((threadIdx.x & 31) == 0) atomicOr(a.err, PA_DEVERR_TIMEOUT);
   }
   return ok;
 }
@@ -349,7 +349,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // K/V tiles are re-read by every query tile of the chunk: keep them in L2
     const uint64_t pol = l2_policy_evict_last();
     int jf = kIdBatch;              // tiles whose ids are in this warp's ring: [0, jf)
-    IdleClock clk;
+    IdleClock clk(a.wait_ns);
     auto timed_out = [&](bool progressed) {
       if (progressed) {
         clk.progress();
@@ -383,7 +383,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         tma_load_2d(dst, &tm_k, x, y, bar, pol);
       };
-      if (lane == 0) {
+      // a stalled test launch issues no load: every wait runs out with no
+      // copy in flight
+      if (lane == 0 && !a.stall_loads) {
         tma_prefetch_desc(&tm_q);
         tma_prefetch_desc(&tm_k);
         if (issuer) mbar_arrive_expect_tx(bar_q, kPair * 2 * kHalf);  // both Q tiles of a pair
@@ -395,7 +397,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // 64r .. 64r+63 (blocks 4r .. 4r+3); one box per lane: (block li,
       // 64-column half h).  The issuer's barrier counts the pair's whole tile.
       const int li = lane >> 1, h = lane & 1;
-      int jk = 0;
+      int jk = a.stall_loads ? nkt : 0;
       while (jk < nkt && !*abort_flag) {
         bool progressed = false;
         // the next batch of ids, half a batch ahead of the loads, into ring
@@ -431,12 +433,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (lane == 0)
         for (int sl = 0; sl < kNK && sl < nkt; ++sl)
           wait_or_abort<kPair>((kFreeByS<kPair> ? bar_s_full : bar_k_empty) + 8 * sl,
-                               ((nkt - 1 - sl) / kNK) & 1, abort_flag, a.err);
+                               ((nkt - 1 - sl) / kNK) & 1, abort_flag, a);
     } else {
       if (lane == 0) tma_prefetch_desc(&tm_v);
       // V tile j: this CTA's boxes complete on its own barrier; once landed
       // (and its slots past seq_len zeroed) the tile is reported to the issuer
-      int jv = 0, jr = 0;  // next V tile to load, next V tile to report
+      int jv = 0, jr = a.stall_loads ? nkt : 0;  // next V tile to load / to report
       while (jr < nkt && !*abort_flag) {
         bool progressed = false;
         if (jf < nkt && jv + kIdBatch / 2 >= jf) {
@@ -508,7 +510,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (lane == 0)
         for (int sl = 0; sl < kNV && sl < nkt; ++sl)
           wait_or_abort<kPair>((kFreeByPV<kPair> ? bar_o_done : bar_v_empty) + 8 * sl,
-                               ((nkt - 1 - sl) / kNV) & 1, abort_flag, a.err);
+                               ((nkt - 1 - sl) / kNV) & 1, abort_flag, a);
     }
     __syncwarp();
   } else if (warp == kMmaWarp) {
@@ -520,9 +522,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_commit<kPair>(bar);
         if constexpr (kPair == 2) tc_commit<kPair>(mapa_shared(bar, 1));
       };
-      bool ok = wait_or_abort<kPair>(bar_q, 0, abort_flag, a.err);
+      bool ok = wait_or_abort<kPair>(bar_q, 0, abort_flag, a);
       int js = 0, jp = 0;  // next score tile / next PV product to issue
-      IdleClock clk;
+      IdleClock clk(a.wait_ns);
       while (ok && jp < nkt) {
         bool progressed = false;
         // S(js) = Q K_js^T into score buffer js % 3, once K_js landed and PV
@@ -587,7 +589,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int j = 0; j < nkt; ++j) {
       const int b = j & 1;        // row maximum exchange buffer
       const int b3 = j % kNS;     // score buffer
-      wait_or_abort_warp<kPair>(bar_s_full + 8 * b3, (j / kNS) & 1, abort_flag, a.err);
+      wait_or_abort_warp<kPair>(bar_s_full + 8 * b3, (j / kNS) & 1, abort_flag, a);
       tc_fence_after();
       tmem_ld64(tmem + lane_off + b3 * 128 + hc * 64, v);
 
@@ -647,7 +649,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // tile must have landed first
       if (j >= 1 && __any_sync(0xffffffffu, alpha != 1.f)) {
         wait_or_abort_warp<kPair>(bar_o_done + 8 * ((j - 1) % kNS), ((j - 1) / kNS) & 1,
-                                  abort_flag, a.err);
+                                  abort_flag, a);
         tc_fence_after();
         const uint32_t ocol = tmem + lane_off + kTmemO + hc * 64;
 #pragma unroll
@@ -675,7 +677,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     // ---- epilogue: O / l -> bf16, and lse
     wait_or_abort_warp<kPair>(bar_o_done + 8 * ((nkt - 1) % kNS), ((nkt - 1) / kNS) & 1,
-                              abort_flag, a.err);
+                              abort_flag, a);
     tc_fence_after();
     red_sum[hc * 128 + r] = l_run;
     named_barrier(1 + qd, 64);
@@ -766,8 +768,11 @@ cudaError_t launch_prefill_as(const PrefillArgs& a, const CUtensorMap* tm_q,
 }
 }  // namespace
 
-cudaError_t launch_prefill(const PrefillArgs& a, const CUtensorMap* tm_q, const CUtensorMap* tm_k,
-                           const CUtensorMap* tm_v, int grid_tiles, cudaStream_t stream) {
+cudaError_t launch_prefill(const PrefillArgs& args, const CUtensorMap* tm_q,
+                           const CUtensorMap* tm_k, const CUtensorMap* tm_v, int grid_tiles,
+                           cudaStream_t stream) {
+  PrefillArgs a = args;
+  if (a.wait_ns == 0) a.wait_ns = kWaitLimitNs;
   return a.after_decode ? launch_prefill_as<1>(a, tm_q, tm_k, tm_v, grid_tiles, stream)
                         : launch_prefill_as<2>(a, tm_q, tm_k, tm_v, grid_tiles, stream);
 }

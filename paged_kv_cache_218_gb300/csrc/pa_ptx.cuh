@@ -8,8 +8,10 @@
 
 namespace pa {
 
-// Time limit of every spin on an mbarrier: past it the waiter gives up and
-// reports a timeout (a healthy wait lasts microseconds).
+// Default time limit of every spin on an mbarrier: past it the waiter gives
+// up and reports a timeout (a healthy wait lasts microseconds).  Launches
+// carry their limit in their arguments; only the library's stalled test
+// launches use a shorter one.
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
 
 __device__ __forceinline__ uint64_t global_ns() {
@@ -27,8 +29,10 @@ __device__ __forceinline__ uint32_t smem_u32(const void* p) {
 // costs far more than a barrier probe) and reports when the loop has made
 // no progress for kWaitLimitNs.
 struct IdleClock {
+  uint64_t limit = kWaitLimitNs;
   uint32_t rounds = 0;
   uint64_t t0 = 0;
+  __device__ __forceinline__ explicit IdleClock(uint64_t limit_ns) : limit(limit_ns) {}
   __device__ __forceinline__ void progress() { rounds = 0; }
   __device__ __forceinline__ bool expired() {
     if ((++rounds & 63u) != 0) return false;
@@ -37,7 +41,7 @@ struct IdleClock {
       t0 = now;
       return false;
     }
-    return now - t0 > kWaitLimitNs;
+    return now - t0 > limit;
   }
 };
 
@@ -87,11 +91,12 @@ __device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
 
 // Bounded wait for the phase with the given parity; false on timeout.  One
 // loop with a single exit, so the code after a wait has one copy.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity,
+                                          uint64_t limit_ns = kWaitLimitNs) {
   bool done = mbar_try_wait(bar, parity);
   const uint64_t t0 = done ? 0ull : global_ns();
   for (uint32_t it = 1; !done; ++it) {
-    if ((it & 63u) == 0 && global_ns() - t0 > kWaitLimitNs) break;
+    if ((it & 63u) == 0 && global_ns() - t0 > limit_ns) break;
     done = mbar_try_wait(bar, parity);
   }
   return done;
@@ -102,8 +107,9 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
 // lane must reach at the same instruction: the lanes leave their polling
 // loops at different times, so they reconverge here, and the result is the
 // same for all of them.
-__device__ __forceinline__ bool mbar_wait_warp(uint32_t bar, uint32_t parity) {
-  const bool ok = mbar_wait(bar, parity);
+__device__ __forceinline__ bool mbar_wait_warp(uint32_t bar, uint32_t parity,
+                                               uint64_t limit_ns = kWaitLimitNs) {
+  const bool ok = mbar_wait(bar, parity, limit_ns);
   __syncwarp();
   return __all_sync(0xffffffffu, ok);
 }
