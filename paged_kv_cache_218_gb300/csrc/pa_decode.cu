@@ -44,7 +44,10 @@ namespace {
 
 constexpr int kConsumerWarps = 8;
 constexpr int kConsumerThreads = kConsumerWarps * 32;
-constexpr int kThreads = kConsumerThreads + 32;
+constexpr int kProducerWarp = kConsumerWarps;
+constexpr int kMergeWarp = kConsumerWarps + 1;  // balanced split: tickets of mid-walk partials
+constexpr int kHandOffs = 2;  // partial pieces a CTA's walk can hand to the merge warp
+constexpr int kThreads = kConsumerThreads + 64;
 constexpr int kBoxBytes = 16 * 128;  // one TMA box: 16 token rows x 64 bf16
 constexpr int kMaxStages = 16;
 constexpr float kLn2 = 0.6931471805599453f;
@@ -91,7 +94,7 @@ __host__ __device__ inline Layout make_layout(int D, int Hkv, int Hq, int wph, i
   const int obuf = wph > 1 ? kConsumerWarps * kMaxGroup * (D + 4) * 4 : 0;
   L.ml_off = L.obuf_off + obuf;
   L.bar_off = L.ml_off + kConsumerWarps * kMaxGroup * 2 * 4;
-  L.misc_off = L.bar_off + (kMaxStages * 2 + 4) * 8;
+  L.misc_off = L.bar_off + (kMaxStages * 2 + 8) * 8;
   L.pre_off = L.misc_off + 128;  // misc: flags, tickets, scan partials, per-warp words
   L.total = L.pre_off + pre_ints * 4;
   return L;
@@ -555,18 +558,19 @@ __device__ __forceinline__ int out_dim(int mt, int g, int half) {
 // groups of the output and keeps, per group, the running maximum M, the sum
 // S = sum_k exp(lse_k - M) and the weighted sum of the pieces' outputs.  The
 // pieces are read kKB at a time with all their loads issued together, so a
-// merge of up to kKB pieces costs about one L2 round trip.  Inlined: it runs
+// merge of up to kKB pieces costs about one L2 round trip.  NT threads take
+// part (ctid in [0, NT)): the consumers, or the merge warp.  Inlined: it runs
 // inside the piece loop, where a call would save the loop's live registers to
 // the stack around it.
-template <int D>
+template <int D, int NT>
 __device__ __forceinline__ void merge_pieces(const DecodeArgs& a, int s, long long c_first,
                                              int npieces, int ctid) {
   const int Hq = a.num_q_heads;
-  constexpr int kNI = 4;  // float4 groups per thread per batch
-  constexpr int kKB = 4;  // pieces per round
+  constexpr int kNI = NT >= 256 ? 4 : 2;  // float4 groups per thread per batch
+  constexpr int kKB = NT >= 256 ? 4 : 2;  // pieces per round
   const int nf = Hq * D / 4;
   const long long row0 = static_cast<long long>(s) * Hq;
-  for (int fb0 = 0; fb0 < nf; fb0 += kNI * kConsumerThreads) {
+  for (int fb0 = 0; fb0 < nf; fb0 += kNI * NT) {
     float4 acc[kNI];
     float M[kNI], S[kNI];
 #pragma unroll
@@ -586,7 +590,7 @@ __device__ __forceinline__ void merge_pieces(const DecodeArgs& a, int s, long lo
             a.part_o + ((c_first + (k < npieces ? k : 0)) * 2 + (k == 0 ? 1 : 0)) * a.slot_floats;
 #pragma unroll
         for (int i = 0; i < kNI; ++i) {
-          const int f = fb0 + ctid + i * kConsumerThreads;
+          const int f = fb0 + ctid + i * NT;
           if (k < npieces && f < nf) {
             lk[u][i] = __ldcg(sl + Hq * D + (f * 4) / D);
             ok[u][i] = __ldcg(reinterpret_cast<const float4*>(sl) + f);
@@ -622,7 +626,7 @@ __device__ __forceinline__ void merge_pieces(const DecodeArgs& a, int s, long lo
     }
 #pragma unroll
     for (int i = 0; i < kNI; ++i) {
-      const int f = fb0 + ctid + i * kConsumerThreads;
+      const int f = fb0 + ctid + i * NT;
       if (f < nf) {
         const float inv = S[i] > 0.f ? 1.f / S[i] : 0.f;
         const uint2 pk = make_uint2(pack_bf16x2(acc[i].x * inv, acc[i].y * inv),
@@ -656,6 +660,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t bar_empty = bar_full + kMaxStages * 8;
   const uint32_t bar_qfull = bar_empty + kMaxStages * 8;  // two query slots
   const uint32_t bar_qempty = bar_qfull + 16;
+  const uint32_t bar_hand = bar_qempty + 16;   // two: a mid-walk partial handed to the merge warp
+  const uint32_t bar_tdone = bar_hand + 16;    // two: the merge warp took that piece's ticket
   const int NS = L.stages;
   const int active_warps = Hkv * wph < kConsumerWarps ? Hkv * wph : kConsumerWarps;
 
@@ -669,8 +675,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int k = 0; k < 2; ++k) {
       mbar_init(bar_qfull + k * 8, 1);
       mbar_init(bar_qempty + k * 8, active_warps);
+      mbar_init(bar_hand + k * 8, kConsumerWarps);  // one arrival per consumer warp
+      mbar_init(bar_tdone + k * 8, 1);
     }
-    misc[0] = 0;  // abort flag
+    misc[0] = 0;   // abort flag
+    misc[15] = 0;  // the walk's own pending merge (record kHandOffs), none yet
     fence_mbar_init();
   }
   __syncthreads();  // barriers initialized before any warp uses them
@@ -770,7 +779,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       jbp += c_n;
     }
   };
-  if (warp == kConsumerWarps && lens_w) {
+  if (warp == kProducerWarp && lens_w) {
     prefix(false);
     init_cursor();
     first_chunk();
@@ -785,7 +794,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (a.mode == kModeBalanced) {
     // the consumers wait on a named barrier that the producer passes without
     // waiting
-    if (warp == kConsumerWarps) {
+    if (warp == kProducerWarp) {
       bool same = false;
       if (lens_w) {
         ids_raw = have_c ? load_id_raw(a, c_s, c_jb, c_n, lane) : 0;
@@ -813,7 +822,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     cur.U = static_cast<long long>(a.num_seqs) * a.max_parts;
   }
 
-  if (warp == kConsumerWarps) {
+  if (warp == kProducerWarp) {
     // ------------------------------------------------------------ producer
     // a stalled test launch issues nothing: every consumer wait runs out
     // with no copy in flight
@@ -903,21 +912,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
         if (!ok) break;
-        if (lane == 0) {
-          // one box per 64-column half: 16 tokens x every kv head of the block
+        // one box per 64-column half and pool (16 tokens x every kv head of
+        // the block), each issued by its own lane: the TMA unit takes boxes
+        // from several threads at once, one thread's boxes one after another
+        constexpr int kBoxes = KV8 ? 2 : 2 * (D / 64);
+        if (lane < kBoxes) {
           const uint32_t kdst = sbase + st * L.stage_bytes;
           const uint32_t vdst = kdst + Hkv * L.head_bytes;
           const int y = blk * kBlockSize;
-          if constexpr (KV8) {  // E4M3: a token row of a head is 128 bytes, one box
-            tma_load_3d(kdst, &tm_k, 0, y, 0, fb, pol);
-            tma_load_3d(vdst, &tm_v, 0, y, 0, fb, pol);
-          } else {
-#pragma unroll
-            for (int h = 0; h < D / 64; ++h) {
-              tma_load_3d(kdst + h * Hkv * kBoxBytes, &tm_k, h * 64, y, 0, fb, pol);
-              tma_load_3d(vdst + h * Hkv * kBoxBytes, &tm_v, h * 64, y, 0, fb, pol);
-            }
-          }
+          const bool is_v = lane & 1;
+          const int h = lane >> 1;  // 64-column half (E4M3: the whole 128-byte row)
+          tma_load_3d((is_v ? vdst : kdst) + (KV8 ? 0 : h * Hkv * kBoxBytes), is_v ? &tm_v : &tm_k,
+                      KV8 ? 0 : h * 64, y, 0, fb, pol);
         }
         if (!got2 && (i + 1 == n || i + 1 == NS)) {
           have2 = next_chunk2(s2, jb2, n2);
@@ -939,6 +945,46 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (have_p) stage_q(p, qi++);
     }
     if (!ok) *reinterpret_cast<volatile int*>(misc) = 1;
+    return;
+  }
+
+  if (warp == kMergeWarp) {
+    // -------------------------------------------------------------- merge warp
+    // Balanced split: a partial piece that is not the last of the CTA's walk
+    // is handed over here once the consumers have published it (hand-off k
+    // on barrier k, with the sequence, its first CTA and its piece count in
+    // shared memory), so that they go on streaming the next piece while this
+    // warp takes the sequence's ticket (an L2 round trip).  A ticket taken by
+    // the consumers themselves stalled the stream: decode CTAs of two pieces
+    // streamed 8 % slower than those of one.  If the ticket is the last one,
+    // the merge is left pending for the consumers, who make it with the same
+    // code as every other merge (bitwise the same result) once their stream
+    // has ended.  A record with no pieces ends the hand-offs.  If a wait runs
+    // out, the remaining records go back to the consumers (state 2: "take
+    // the ticket yourselves"), so every published piece draws one ticket.
+    if (a.mode == kModeBalanced) {
+      for (int k = 0; k < kHandOffs; ++k) {
+        if (!mbar_wait_warp(bar_hand + k * 8, 0, a.wait_ns)) {
+          if (lane == 0) {
+            atomicOr(a.err, PA_DEVERR_TIMEOUT);
+            for (int j = k; j < kHandOffs; ++j) {
+              misc[7 + 4 * j] = 2;
+              mbar_arrive(bar_tdone + j * 8);
+            }
+          }
+          __syncwarp();
+          break;
+        }
+        volatile int* rec = misc + 4 + 4 * k;
+        if (rec[2] == 0) break;
+        if (lane == 0) {
+          const int t = atom_add_acq_rel_gpu(a.counters + rec[1], 1);
+          rec[3] = t == rec[2] - 1 ? 1 : 0;  // pending merge
+          mbar_arrive(bar_tdone + k * 8);
+        }
+        __syncwarp();
+      }
+    }
     return;
   }
 
@@ -970,6 +1016,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   Piece pc;
   uint32_t g = 0;
   int qi = 0;
+  int hand = 0;  // partial pieces handed to the merge warp so far
   // the report flag is uniform over a warp: lanes of one warp must take the
   // same path here, or the warp-synchronous MMA and matrix loads below could
   // be reached at different instructions
@@ -1300,18 +1347,76 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (hb < G) slot[Hq * D + hgb] = lseb;
         }
       }
-      // take the sequence's ticket (release of the slot stores above); the
-      // last of its pieces to draw one merges them all, here and now: the
-      // partial pieces are walked first, so this happens while the producer
-      // keeps the ring full and other CTAs use the bandwidth
       const long long cf = cta_of(pc.seg_start, cur.W, cur.C);
       const int np = static_cast<int>(cta_of(pc.seg_start + pc.nb - 1, cur.W, cur.C) - cf + 1);
+      // a piece before the walk's last: hand it to the merge warp (each
+      // warp's slot stores, ordered by __syncwarp, are released by its
+      // arrival) and go on with the next piece
+      if (hand < kHandOffs && (cur.idx < cur.end || (cur.phase == 0 && cur.lo < cur.mid))) {
+        if (ctid == 0) {
+          misc[4 + 4 * hand] = pc.s;
+          misc[5 + 4 * hand] = static_cast<int>(cf);
+          misc[6 + 4 * hand] = np;
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar_hand + hand * 8);
+        ++hand;
+        continue;
+      }
+      // the walk's last piece: take the sequence's ticket (release of the
+      // slot stores above); the last of its pieces to draw one merges them
+      // all, right after the walk (below)
       named_barrier(1, kConsumerThreads);
-      if (ctid == 0) misc[1] = atom_add_acq_rel_gpu(a.counters + cf, 1);
-      named_barrier(1, kConsumerThreads);
-      if (misc[1] == np - 1) {
-        merge_pieces<D>(a, pc.s, cf, np, ctid);
-        if (ctid == 0) a.counters[cf] = 0;
+      if (ctid == 0) {
+        const int t = atom_add_acq_rel_gpu(a.counters + cf, 1);
+        int* rec = misc + 4 + 4 * kHandOffs;
+        rec[0] = pc.s;
+        rec[1] = static_cast<int>(cf);
+        rec[2] = np;
+        rec[3] = t == np - 1 ? 1 : 0;
+      }
+    }
+  }
+  if (a.mode == kModeBalanced) {
+    // no more hand-offs: a record without pieces lets the merge warp exit
+    if (hand < kHandOffs) {
+      if (ctid == 0) misc[6 + 4 * hand] = 0;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar_hand + hand * 8);
+    }
+    // the merges whose last ticket this CTA drew: those of the merge warp's
+    // hand-offs, then the walk's last piece's (one merge site, so every
+    // merge rounds the same way)
+    named_barrier(1, kConsumerThreads);  // record kHandOffs (ctid 0's) is visible
+    for (int k = 0; k <= kHandOffs; ++k) {
+      const volatile int* rec = misc + 4 + 4 * k;
+      // the record's state, read by every consumer thread between named
+      // barriers, so that all of them take the same branches below
+      int st;
+      if (k < kHandOffs) {
+        if (k >= hand) continue;  // hand is the same in every consumer thread
+        // one thread waits for the merge warp's answer and shares it
+        if (ctid == 0) {
+          const bool ok = mbar_wait(bar_tdone + k * 8, 0, a.wait_ns);
+          if (!ok) atomicOr(a.err, PA_DEVERR_TIMEOUT);
+          misc[2] = ok ? rec[3] : 0;
+        }
+        named_barrier(1, kConsumerThreads);
+        st = misc[2];
+      } else {
+        st = rec[3];  // ctid 0's, before the barrier above the loop
+      }
+      named_barrier(1, kConsumerThreads);  // read before misc[2] changes again
+      if (st == 2) {  // the merge warp gave up before this hand-off's ticket
+        if (ctid == 0) misc[2] = atom_add_acq_rel_gpu(a.counters + rec[1], 1) == rec[2] - 1 ? 1 : 0;
+        named_barrier(1, kConsumerThreads);
+        st = misc[2];
+        named_barrier(1, kConsumerThreads);
+      }
+      if (st == 1) {
+        merge_pieces<D, kConsumerThreads>(a, rec[0], rec[1], rec[2], ctid);
+        named_barrier(1, kConsumerThreads);
+        if (ctid == 0) a.counters[rec[1]] = 0;
       }
     }
   }
