@@ -211,12 +211,16 @@ def kv_bytes_decode(w):
     return W.logical_kv_bytes(w.decode_seq_lens, w.num_kv_heads, w.head_dim)
 
 
-def decode_algorithmic_bytes(w):
+def decode_algorithmic_bytes(w, append=False):
     """Minimal bytes one decode launch must move: every K/V token once, the
-    queries, the outputs, the used block-table entries and the lengths."""
+    queries, the outputs, the used block-table entries and the lengths; with
+    the step's new token fused in (pa_decode_append), that token also written
+    to its slot (its read, from the step's key / value rows instead of the
+    pool, is already in the K/V tokens)."""
     S, Hq, D = w.num_decode_seqs, w.num_q_heads, w.head_dim
     nb = sum((int(n) + 15) // 16 for n in w.decode_seq_lens)
-    return kv_bytes_decode(w) + 2 * S * Hq * D * 2 + nb * 4 + S * 4
+    new = S * 2 * w.num_kv_heads * D * 2 if append else 0
+    return kv_bytes_decode(w) + 2 * S * Hq * D * 2 + nb * 4 + S * 4 + new
 
 
 def chunk_flops(w):
@@ -258,13 +262,28 @@ def run_gpu(args, rank, world, local_rank):
                                                           w.max_blocks_per_seq), dev)
            for _ in range(R)] if hybrid else None
     cow = len(w.cow_pairs) > 0
-    launches_per_step = 2 + (1 if P > 0 else 0) + (1 if hybrid else 0) + (1 if cow else 0)
+    # a decode-only step fuses the slot scatter into the decode (pa_decode_append)
+    launches_per_step = (2 if hybrid else 1) + (1 if P > 0 else 0) + (1 if hybrid else 0) \
+        + (1 if cow else 0)
+
+    def append(i):
+        r = reps[i % R]
+        out, q, kc, vc, bt, sl = decode_args(w, r)
+        pa.pa_decode_append(out, q, r.key, r.value, kc, vc, bt, sl, w.scale, partition_tokens=P,
+                            workspace=ws[i % R])
 
     def step(i, ev=None, cev=None):
         r = reps[i % R]
         cur = torch.cuda.current_stream()
         if cow:  # private copies of shared blocks about to be written (copy on write)
             pa.pa_copy_blocks(r.k_cache, r.v_cache, r.cow_pairs)
+        if not hybrid:  # the new tokens' slot scatter fused into the decode
+            if ev is not None:
+                ev[0].record(cur)
+            append(i)
+            if ev is not None:
+                ev[1].record(cur)
+            return
         pa.pa_reshape_and_cache(r.key, r.value, r.k_cache, r.v_cache, r.slot_mapping)
         if hybrid and ev is None:
             # the hybrid batch in one call: the chunk's tiles co-scheduled
@@ -316,9 +335,13 @@ def run_gpu(args, rank, world, local_rank):
         with torch.cuda.graph(g_round):
             for r in range(R):
                 step(r)
-        with torch.cuda.graph(g_dec_round):
+        with torch.cuda.graph(g_dec_round):  # the step's attention kernel alone
             for r in range(R):
-                pa.pa_decode(*decode_args(w, reps[r]), w.scale, partition_tokens=P, workspace=ws[r])
+                if hybrid:
+                    pa.pa_decode(*decode_args(w, reps[r]), w.scale, partition_tokens=P,
+                                 workspace=ws[r])
+                else:
+                    append(r)
         if hybrid:
             with torch.cuda.graph(g_chunk_round):
                 for r in range(R):
@@ -619,6 +642,11 @@ def run_e2e(args, w, reps, ws, dev, pa, dist, s_chunk, max_q, T, hws):
         comp = torch.cuda.current_stream()
         if "cow_pairs" in v:
             pa.pa_copy_blocks(r.k_cache, r.v_cache, v["cow_pairs"])
+        if not hybrid:  # slot scatter fused into the decode
+            pa.pa_decode_append(r.out, v["q"][q0:q0 + S], v["key"], v["value"], r.k_cache,
+                                r.v_cache, v["block_tables"][s0:], v["seq_lens"][s0:], w.scale,
+                                partition_tokens=P, workspace=ws[j])
+            return
         pa.pa_reshape_and_cache(v["key"], v["value"], r.k_cache, r.v_cache, v["slot_mapping"])
         if hybrid and not args.no_graphs:
             pa.pa_hybrid_attention(r.out_chunk, v["q"][:T], v["block_tables"][:C], v["cu"],
@@ -897,6 +925,11 @@ def profile_case(args):
         if args.profile_case == "decode":
             for _ in range(3):
                 pa.pa_decode(*args_d, w.scale, partition_tokens=0, workspace=ws)
+        elif args.profile_case == "append":
+            out, q, kc, vc, bt, sl = args_d
+            for _ in range(3):
+                pa.pa_decode_append(out, q, r.key, r.value, kc, vc, bt, sl, w.scale,
+                                    partition_tokens=0, workspace=ws)
         else:
             nb, bs, Hkv, _ = r.k_cache.shape
             kf = torch.empty((nb, bs, Hkv, D), dtype=torch.uint8, device=dev)
@@ -934,7 +967,7 @@ def main():
     ap.add_argument("--no-graphs", action="store_true",
                     help="launch every kernel from Python instead of replaying CUDA graphs")
     ap.add_argument("--profile-case", default=None,
-                    choices=["decode", "decode_fp8", "prefill", "cascade"],
+                    choices=["decode", "append", "decode_fp8", "prefill", "cascade"],
                     help="run three launches of one kernel on a small case (for ncu) and exit")
     args = ap.parse_args()
     if args.profile_case:
@@ -968,10 +1001,11 @@ def main():
     kvb = kv_bytes_decode(w)
     step_ms = res["elapsed_ms"] / K
     value = res["kv_all"] / (res["elapsed_ms"] * 1e-3) / 1e9
-    alg = decode_algorithmic_bytes(w)
+    fused = w.num_chunks == 0  # the step's decode carries the slot scatter (pa_decode_append)
+    alg = decode_algorithmic_bytes(w, append=fused)
     achieved = alg / (res["dec_ms"] * 1e-3) / 1e9
     traffic = profile_traffic(["pa_decode.cu", "pa_ptx.cuh", "pa_internal.h"],
-                              "decode_kernel_llama3_8b_decode_layer.md") \
+                              "decode_append_kernel_llama3_8b_decode_layer.md") \
         if args.config == "llama3_8b_decode_layer" else None
     e = res["e2e"]
     line = {
@@ -984,22 +1018,26 @@ def main():
                    "l2": f"{args.replicas} independent KV pools in rotation "
                          f"({args.replicas * 2 * w.k_cache.nbytes / 1e9:.2f} GB) >> 129 MB L2",
                    "parallelism": f"replicas x{world}",
-                   "launch": (f"CUDA graph per round of {args.replicas} steps (scatter, "
-                              + ("then pa_hybrid_attention: the decode on the SMs the prefill "
-                                 "chunk leaves free, the chunk beside it; "
-                                 if w.num_chunks else "decode; ")
+                   "launch": (f"CUDA graph per round of {args.replicas} steps ("
+                              + ("copy-on-write block copies, " if len(w.cow_pairs) else "")
+                              + ("scatter, then pa_hybrid_attention: the decode on the SMs the "
+                                 "prefill chunk leaves free, the chunk beside it; "
+                                 if w.num_chunks else
+                                 "pa_decode_append: the slot scatter fused into the decode; ")
                               + "programmatic dependent launches)") if res["graphs"]
                              else "eager launches from Python"},
         "tokens_per_s": w.num_decode_seqs * world * K / (res["elapsed_ms"] * 1e-3),
         "pct_of_nominal_8tbps": 100.0 * value / world / NOMINAL_HBM_GBS,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
                      "frac": achieved / hbm, "traffic": traffic,
-                     "kernel": "decode_kernel<128>", "peak_source": f"{peak_src} (hbm_gbs)",
+                     "kernel": "decode_kernel<128> with the slot scatter (pa_decode_append)"
+                               if fused else "decode_kernel<128>",
+                     "peak_source": f"{peak_src} (hbm_gbs)",
                      "bytes_per_launch": alg, "launch_ms": res["dec_ms"],
                      "launch_timing": ("CUDA events on the launching stream around back-to-back "
-                                       f"decode-only launches (graphs of {args.replicas}, one per "
-                                       "KV pool, each launch a programmatic dependent of the one "
-                                       "before); time / launches") if res["graphs"]
+                                       f"launches of that kernel alone (graphs of {args.replicas}, "
+                                       "one per KV pool, each launch a programmatic dependent of "
+                                       "the one before); time / launches") if res["graphs"]
                                       else "CUDA events around each decode launch in the timed region"},
         "e2e": {"value": e["kv_all"] / (e["ms"] * 1e-3) / 1e9, "unit": "GB/s",
                 "h2d_bytes_per_step": e["h2d"], "d2h_bytes_per_step": e["d2h"],

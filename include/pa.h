@@ -321,6 +321,29 @@ int pa_hybrid_attention(void *out_chunk, const void *q_chunk, const int32_t *chu
                         void *stream);
 
 /*
+ * pa_decode_append -- one decode step with the slot scatter fused in:
+ * sequence s's new token (row s of key / value, [num_seqs, *, Hkv, D] bf16
+ * with token strides in elements) is written into the slot of position
+ * seq_len[s] - 1 named by its block table, and sequence s's query attends
+ * over [0, seq_len[s]) with that token in place.  The result is that of
+ * pa_reshape_and_cache with slot_mapping[s] = block_tables[s][(seq_len[s] -
+ * 1) / 16] * 16 + (seq_len[s] - 1) % 16, then pa_decode, in one launch
+ * ("03 - Engines Papers", section 2 PagedAttention: the step's new K/V go
+ * into their slots, then the kernel gathers K/V from the blocks; reading of
+ * the pages: seq_len counts the new token).  A sequence with seq_len 0 has
+ * no token to write.  bf16 pools only; every other argument, mode,
+ * workspace and error as pa_decode.  The last block of every sequence must be
+ * its own (copy-on-write done before, as for pa_reshape_and_cache).
+ */
+int pa_decode_append(void *out, const void *q, const void *key, const void *value,
+                     int64_t key_token_stride, int64_t value_token_stride, void *k_cache,
+                     void *v_cache, const int32_t *block_tables, int max_blocks_per_seq,
+                     const int32_t *seq_lens, int num_seqs, int num_q_heads, int num_kv_heads,
+                     int head_dim, int block_size, int64_t num_blocks, float scale,
+                     int partition_tokens, float *out_lse, void *workspace,
+                     size_t workspace_bytes, void *stream);
+
+/*
  * Size of the static device scratch behind pa_decode_noalloc (8 MiB).
  */
 #define PA_NOALLOC_SCRATCH_BYTES (8u << 20)

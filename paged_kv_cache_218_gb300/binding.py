@@ -48,6 +48,8 @@ _SIGS = {
     "pa_decode_workspace_size": ([_I, _I, _I, _I, _I, _I, _I], _S),
     "pa_decode": ([_P, _P, _P, _P, _P, _I, _P, _I, _I, _I, _I, _I, _L, _F, _I, _P, _P, _S, _P], _I),
     "pa_merge_partials": ([_P, _P, _P, _P, _P, _I, _I, _I, _I, _P], _I),
+    "pa_decode_append": ([_P, _P, _P, _P, _L, _L, _P, _P, _P, _I, _P, _I, _I, _I, _I, _I, _L, _F,
+                          _I, _P, _P, _S, _P], _I),
     "pa_decode_noalloc": ([_P, _P, _P, _P, _P, _I, _P, _I, _I, _I, _I, _I, _L, _F, _P, _P], _I),
     "pa_prefill_chunk": ([_P, _P, _P, _P, _P, _I, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _L, _F,
                           _P, _P], _I),
@@ -263,6 +265,33 @@ def pa_decode(out, q, k_cache, v_cache, block_tables, seq_lens, scale, partition
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     _check("pa_decode", _lib.pa_decode(
         _ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables),
+        block_tables.shape[1], _ptr(seq_lens), S, Hq, Hkv, D, bs, nb, float(scale),
+        int(partition_tokens), _ptr(out_lse), _ptr(workspace), ws_bytes, _stream(stream)))
+
+
+def pa_decode_append(out, q, key, value, k_cache, v_cache, block_tables, seq_lens, scale,
+                     partition_tokens=0, out_lse=None, workspace=None, stream=None) -> None:
+    """One decode step with the slot scatter fused in: row s of key / value
+    goes into the slot of position seq_lens[s] - 1, then the decode."""
+    _need(out, "out", torch.bfloat16, 3)
+    _need(q, "q", torch.bfloat16, 3)
+    _need(key, "key", torch.bfloat16, 3, contiguous=False)
+    _need(value, "value", torch.bfloat16, 3, contiguous=False)
+    for t, n in ((key, "key"), (value, "value")):
+        if t.stride(2) != 1 or t.stride(1) != t.shape[2]:
+            raise ValueError(f"{n} must be contiguous within a token")
+    _need(k_cache, "k_cache", torch.bfloat16, 4)
+    _need(v_cache, "v_cache", torch.bfloat16, 4)
+    _need(block_tables, "block_tables", torch.int32, 2)
+    _need(seq_lens, "seq_lens", torch.int32, 1)
+    if out_lse is not None:
+        _need(out_lse, "out_lse", torch.float32, 2)
+    S, Hq, D = q.shape
+    nb, bs, Hkv, _ = k_cache.shape
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check("pa_decode_append", _lib.pa_decode_append(
+        _ptr(out), _ptr(q), _ptr(key), _ptr(value), key.stride(0), value.stride(0),
+        _ptr(k_cache), _ptr(v_cache), _ptr(block_tables),
         block_tables.shape[1], _ptr(seq_lens), S, Hq, Hkv, D, bs, nb, float(scale),
         int(partition_tokens), _ptr(out_lse), _ptr(workspace), ws_bytes, _stream(stream)))
 

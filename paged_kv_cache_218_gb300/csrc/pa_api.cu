@@ -531,7 +531,8 @@ static int decode_check(const void* out, const void* q, const void* k_cache, con
                         const int32_t* block_tables, int max_blocks_per_seq,
                         const int32_t* seq_lens, int num_seqs, int num_q_heads,
                         int num_kv_heads, int head_dim, int block_size, int64_t num_blocks,
-                        float scale, int partition_tokens, const float* out_lse) {
+                        float scale, int partition_tokens, const float* out_lse,
+                        bool append = false) {
   if (int rc = check_shape(num_q_heads, num_kv_heads, head_dim, block_size)) return rc;
   if (kv_fp8 && head_dim != 128) return PA_ERR_UNSUPPORTED;
   if (num_seqs < 0 || max_blocks_per_seq <= 0 || num_blocks <= 0) return PA_ERR_INVALID;
@@ -547,7 +548,7 @@ static int decode_check(const void* out, const void* q, const void* k_cache, con
   const int mode = decode_mode(partition_tokens);
   if (mode == kModeFixedSplit && partition_tokens % block_size) return PA_ERR_INVALID;
   if (mode == kModeBalanced && num_seqs > kMaxSeqsBalanced) return PA_ERR_UNSUPPORTED;
-  if (!decode_supported(head_dim, num_kv_heads, num_q_heads, mode, num_seqs, kv_fp8))
+  if (!decode_supported(head_dim, num_kv_heads, num_q_heads, mode, num_seqs, kv_fp8, append))
     return PA_ERR_UNSUPPORTED;
   return PA_OK;
 }
@@ -561,10 +562,13 @@ static int decode_impl(void* out, const void* q, const void* k_cache, const void
                        float scale, int partition_tokens, float* out_lse, void* workspace,
                        size_t workspace_bytes, void* stream, const int32_t* start_blocks = nullptr,
                        const float* init_o = nullptr, const float* init_lse = nullptr,
-                       int grid_override = 0, int stall_loads = 0, uint64_t wait_ns = 0) {
+                       int grid_override = 0, int stall_loads = 0, uint64_t wait_ns = 0,
+                       const void* new_k = nullptr, const void* new_v = nullptr,
+                       int64_t new_k_stride = 0, int64_t new_v_stride = 0) {
   if (int rc = decode_check(out, q, k_cache, v_cache, k_scales, v_scales, kv_fp8, block_tables,
                             max_blocks_per_seq, seq_lens, num_seqs, num_q_heads, num_kv_heads,
-                            head_dim, block_size, num_blocks, scale, partition_tokens, out_lse))
+                            head_dim, block_size, num_blocks, scale, partition_tokens, out_lse,
+                            new_k != nullptr))
     return rc;
   if (num_seqs == 0) return PA_OK;
   const int mode = decode_mode(partition_tokens);
@@ -594,6 +598,12 @@ static int decode_impl(void* out, const void* q, const void* k_cache, const void
   a.init_lse = init_lse;
   a.stall_loads = stall_loads;
   a.wait_ns = wait_ns;  // 0: the default limit
+  a.new_k = static_cast<const __nv_bfloat16*>(new_k);
+  a.new_v = static_cast<const __nv_bfloat16*>(new_v);
+  a.new_k_stride = new_k_stride;
+  a.new_v_stride = new_v_stride;
+  a.k_pool = static_cast<__nv_bfloat16*>(const_cast<void*>(k_cache));
+  a.v_pool = static_cast<__nv_bfloat16*>(const_cast<void*>(v_cache));
   int grid = decode_grid(d->num_sms, mode, a.group, kv_fp8);
   if (grid_override > 0) grid = grid_override < d->num_sms ? grid_override : d->num_sms;
   if (mode == kModeSinglePass) {
@@ -657,6 +667,27 @@ int pa_decode(void* out, const void* q, const void* k_cache, const void* v_cache
                      max_blocks_per_seq, seq_lens, num_seqs, num_q_heads, num_kv_heads, head_dim,
                      block_size, num_blocks, scale, partition_tokens, out_lse, workspace,
                      workspace_bytes, stream);
+}
+
+int pa_decode_append(void* out, const void* q, const void* key, const void* value,
+                     int64_t key_token_stride, int64_t value_token_stride, void* k_cache,
+                     void* v_cache, const int32_t* block_tables, int max_blocks_per_seq,
+                     const int32_t* seq_lens, int num_seqs, int num_q_heads, int num_kv_heads,
+                     int head_dim, int block_size, int64_t num_blocks, float scale,
+                     int partition_tokens, float* out_lse, void* workspace,
+                     size_t workspace_bytes, void* stream) {
+  if (num_seqs > 0) {
+    const int64_t row = static_cast<int64_t>(num_kv_heads) * head_dim;
+    if (!key || !value || !aligned(key, 16) || !aligned(value, 16)) return PA_ERR_INVALID;
+    if (key_token_stride < row || value_token_stride < row || key_token_stride % 8 ||
+        value_token_stride % 8)
+      return PA_ERR_INVALID;
+  }
+  return decode_impl(out, q, k_cache, v_cache, nullptr, nullptr, false, block_tables,
+                     max_blocks_per_seq, seq_lens, num_seqs, num_q_heads, num_kv_heads, head_dim,
+                     block_size, num_blocks, scale, partition_tokens, out_lse, workspace,
+                     workspace_bytes, stream, nullptr, nullptr, nullptr, 0, 0, 0, key, value,
+                     key_token_stride, value_token_stride);
 }
 
 int pa_decode_fp8(void* out, const void* q, const void* k_cache, const void* v_cache,

@@ -79,11 +79,15 @@ struct Layout {
   int stage_bytes;  // K + V of one block, all kv heads
   int stages;
   int q_bytes;      // one staged query row set: Hq x D bf16
-  int q_off, obuf_off, ml_off, bar_off, misc_off, pre_off, total;
+  int q_off, obuf_off, ml_off, nk_off, bar_off, misc_off, pre_off, total;
 };
 
+// Append: per consumer warp, its kv head's new K row and V row (D bf16 each)
+// and the id of the sequence's last block.
+__host__ __device__ constexpr int new_row_bytes(int D) { return 4 * D + 16; }
+
 __host__ __device__ inline Layout make_layout(int D, int Hkv, int Hq, int wph, int stages,
-                                              int pre_ints, int elem_bytes) {
+                                              int pre_ints, int elem_bytes, bool append = false) {
   Layout L;
   L.head_bytes = kBlockSize * D * elem_bytes;
   L.stage_bytes = 2 * Hkv * L.head_bytes;
@@ -93,7 +97,8 @@ __host__ __device__ inline Layout make_layout(int D, int Hkv, int Hq, int wph, i
   L.obuf_off = L.q_off + 2 * L.q_bytes;
   const int obuf = wph > 1 ? kConsumerWarps * kMaxGroup * (D + 4) * 4 : 0;
   L.ml_off = L.obuf_off + obuf;
-  L.bar_off = L.ml_off + kConsumerWarps * kMaxGroup * 2 * 4;
+  L.nk_off = L.ml_off + kConsumerWarps * kMaxGroup * 2 * 4;
+  L.bar_off = L.nk_off + (append ? kConsumerWarps * new_row_bytes(D) : 0);
   L.misc_off = L.bar_off + (kMaxStages * 2 + 8) * 8;
   L.pre_off = L.misc_off + 128;  // misc: flags, tickets, scan partials, per-warp words
   L.total = L.pre_off + pre_ints * 4;
@@ -639,7 +644,7 @@ __device__ __forceinline__ void merge_pieces(const DecodeArgs& a, int s, long lo
   }
 }
 
-template <int D, bool KV8>
+template <int D, bool KV8, bool AP>
 __global__ void __launch_bounds__(kThreads, 1)
     decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                   const DecodeArgs a) {
@@ -651,7 +656,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int Hkv = a.num_kv_heads, G = a.group, Hq = a.num_q_heads;
   const int wph = a.warps_per_head;
-  const Layout L = make_layout(D, Hkv, Hq, wph, a.stages, 0, KV8 ? 1 : 2);
+  const Layout L = make_layout(D, Hkv, Hq, wph, a.stages, 0, KV8 ? 1 : 2, AP);
   float* obuf = reinterpret_cast<float*>(smem + L.obuf_off);
   float* mlbuf = reinterpret_cast<float*>(smem + L.ml_off);
   int* misc = reinterpret_cast<int*>(smem + L.misc_off);
@@ -1133,6 +1138,54 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
 
+    // Append: the warp that will attend the sequence's last block tb fetches
+    // its kv head's row of the new token (and the block's id) into its
+    // shared-memory slot now, asynchronously; when block tb has landed it
+    // writes the row over position seq_len-1 of the stage -- so the token is
+    // attended whatever the pool held there -- and into the pool's slot.
+    int tail_j = -1;  // the sequence's last block, when this warp attends it
+    if constexpr (AP) {
+      const int tb = (pc.len - 1) / kBlockSize;
+      const uint32_t nbuf = sbase + L.nk_off + warp * new_row_bytes(D);
+      if (active && pc.len > 0 && tb >= pc.j0 && tb < pc.j1 &&
+          static_cast<int>((g + static_cast<uint32_t>(tb - pc.j0)) % wph) == sub) {
+        tail_j = tb;
+        if (lane < D / 4) {  // K chunks, then V chunks, of 16 bytes
+          const bool isv = lane >= D / 8;
+          const int ch = lane % (D / 8);
+          const __nv_bfloat16* src =
+              (isv ? a.new_v + pc.s * a.new_v_stride : a.new_k + pc.s * a.new_k_stride) +
+              hw * D + ch * 8;
+          cp_async_16(nbuf + (isv ? 2 * D : 0) + ch * 16, src);
+        }
+        if (lane == 0)
+          cp_async_4(nbuf + 4 * D, a.block_tables + static_cast<long long>(pc.s) * a.max_blocks + tb);
+      }
+    }
+    auto patch_tail = [&](uint32_t stg) {
+      const uint32_t nbuf = sbase + L.nk_off + warp * new_row_bytes(D);
+      cp_async_wait_all();
+      __syncwarp();
+      const int t = (pc.len - 1) & (kBlockSize - 1);
+      if (lane < D / 4) {
+        const bool isv = lane >= D / 8;
+        const int ch = lane % (D / 8);
+        const uint4 v = lds128(nbuf + (isv ? 2 * D : 0) + ch * 16);
+        const uint32_t base =
+            sbase + stg * L.stage_bytes + hw * kBoxBytes + (isv ? Hkv * L.head_bytes : 0);
+        sts128(swz(base, t, ch, Hkv * kBoxBytes), v);
+        int id;
+        asm volatile("ld.shared.u32 %0, [%1];" : "=r"(id) : "r"(nbuf + 4 * D) : "memory");
+        if (id >= 0 && id < a.num_blocks)
+          *reinterpret_cast<uint4*>((isv ? a.v_pool : a.k_pool) +
+                                    (static_cast<long long>(id) * kBlockSize + t) * Hkv * D +
+                                    hw * D + ch * 8) = v;
+      }
+      // the stage is refilled by TMA (async proxy) once released
+      fence_proxy_async_smem();
+      __syncwarp();
+    };
+
     if (active) {
       for (int j = pc.j0; j < pc.j1; ++j, ++g) {
         if (static_cast<int>(g % wph) != sub) continue;
@@ -1143,8 +1196,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           *abort_flag = 1;
           continue;
         }
+        if constexpr (AP)
+          if (j == tail_j) patch_tail(st);
         const int valid = min(kBlockSize, pc.len - j * kBlockSize);
-        if (wph == 1 && NS >= 4 && j + 1 < pc.j1) {
+        if (!AP && wph == 1 && NS >= 4 && j + 1 < pc.j1) {
           // the piece's next block too (this warp holds every block of its kv
           // head): both in one step.  The first one is full, since the piece
           // goes on past it.  Only with a ring of four stages or more (the
@@ -1158,6 +1213,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (lane == 0) mbar_arrive(bar_empty + st * 8);
             continue;
           }
+
           const int valid2 = min(kBlockSize, pc.len - (j + 1) * kBlockSize);
           if constexpr (KV8) {
             const uint32_t kb = sbase + st * L.stage_bytes + hw * L.head_bytes;
@@ -1194,6 +1250,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else {
       g += pc.j1 - pc.j0;
     }
+    if constexpr (AP)
+      if (tail_j >= 0) cp_async_wait_all();  // no copy left in flight (an aborted walk skips blocks)
 
     // ---- per-head result of this piece: normalized o and lse (log2 units)
 #pragma unroll
@@ -1424,11 +1482,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 int warps_per_head(int Hkv) { return Hkv >= kConsumerWarps ? 1 : kConsumerWarps / Hkv; }
 
-int pick_stages(int D, int Hkv, int Hq, int pre_ints, int elem_bytes) {
+int pick_stages(int D, int Hkv, int Hq, int pre_ints, int elem_bytes, bool append) {
   const int wph = warps_per_head(Hkv);
   const int budget = 227 * 1024 - 1024;  // minus alignment slack
   int st = kMaxStages;
-  while (st > 2 && make_layout(D, Hkv, Hq, wph, st, pre_ints, elem_bytes).total > budget) --st;
+  while (st > 2 && make_layout(D, Hkv, Hq, wph, st, pre_ints, elem_bytes, append).total > budget)
+    --st;
   return st;
 }
 
@@ -1456,13 +1515,13 @@ int decode_grid(int num_sms, int mode, int group, bool kv_fp8) {
 }
 
 bool decode_supported(int head_dim, int num_kv_heads, int num_q_heads, int mode, int num_seqs,
-                      bool kv_fp8) {
+                      bool kv_fp8, bool append) {
   if (num_kv_heads > kConsumerWarps) return false;
-  if (kv_fp8 && head_dim != 128) return false;
+  if (kv_fp8 && (head_dim != 128 || append)) return false;
   const int pre = mode == kModeBalanced ? balanced_pre_ints(num_seqs) : 0;
   const int wph = warps_per_head(num_kv_heads);
-  return make_layout(head_dim, num_kv_heads, num_q_heads, wph, 2, pre, kv_fp8 ? 1 : 2).total <=
-         227 * 1024 - 1024;
+  return make_layout(head_dim, num_kv_heads, num_q_heads, wph, 2, pre, kv_fp8 ? 1 : 2, append)
+             .total <= 227 * 1024 - 1024;
 }
 
 cudaError_t launch_decode(DecodeArgs a, const CUtensorMap* tm_k, const CUtensorMap* tm_v,
@@ -1471,22 +1530,25 @@ cudaError_t launch_decode(DecodeArgs a, const CUtensorMap* tm_k, const CUtensorM
   const int elem = a.kv_fp8 ? 1 : 2;
   if (a.wait_ns == 0) a.wait_ns = kWaitLimitNs;
   a.warps_per_head = warps_per_head(a.num_kv_heads);
-  a.stages = pick_stages(head_dim, a.num_kv_heads, a.num_q_heads, pre, elem);
+  const bool append = a.new_k != nullptr;
+  a.stages = pick_stages(head_dim, a.num_kv_heads, a.num_q_heads, pre, elem, append);
   const size_t smem = make_layout(head_dim, a.num_kv_heads, a.num_q_heads, a.warps_per_head,
-                                  a.stages, pre, elem).total + 1024;
+                                  a.stages, pre, elem, append).total + 1024;
   void (*kern)(const CUtensorMap, const CUtensorMap, const DecodeArgs) =
-      a.kv_fp8 ? decode_kernel<128, true>
-               : (head_dim == 128 ? decode_kernel<128, false> : decode_kernel<64, false>);
+      a.kv_fp8 ? decode_kernel<128, true, false>
+      : append ? (head_dim == 128 ? decode_kernel<128, false, true> : decode_kernel<64, false, true>)
+               : (head_dim == 128 ? decode_kernel<128, false, false>
+                                  : decode_kernel<64, false, false>);
   // raise the kernel's dynamic shared-memory limit once per device
   static std::mutex mu;
-  static int set_for[3][64] = {};
+  static int set_for[5][64] = {};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
   {
     std::lock_guard<std::mutex> lock(mu);
-    int& done = set_for[a.kv_fp8 ? 2 : (head_dim == 128 ? 1 : 0)][dev];
+    int& done = set_for[a.kv_fp8 ? 2 : (head_dim == 128 ? 1 : 0) + (append ? 3 : 0)][dev];
     if (done < static_cast<int>(smem)) {
       e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                227 * 1024);

@@ -54,6 +54,15 @@ struct DecodeArgs {
   const float* init_lse;
   uint64_t wait_ns;  // limit of every mbarrier wait (normally kWaitLimitNs)
   int stall_loads;   // test launch: the producer issues no load, every wait runs out
+  // append (pa_decode_append; null otherwise): sequence s's new token, row s
+  // of new_k / new_v (strides in elements), is written into the slot of
+  // position seq_len-1 of the pools and attended there
+  const __nv_bfloat16* new_k;
+  const __nv_bfloat16* new_v;
+  long long new_k_stride;
+  long long new_v_stride;
+  __nv_bfloat16* k_pool;
+  __nv_bfloat16* v_pool;
 };
 
 struct MergeArgs {
@@ -135,7 +144,7 @@ cudaError_t launch_decode(DecodeArgs a, const CUtensorMap* tm_k, const CUtensorM
                           int head_dim, int grid, cudaStream_t stream);
 int decode_grid(int num_sms, int mode, int group, bool kv_fp8);  // CTAs of a decode launch
 bool decode_supported(int head_dim, int num_kv_heads, int num_q_heads, int mode, int num_seqs,
-                      bool kv_fp8);
+                      bool kv_fp8, bool append = false);
 cudaError_t launch_merge(const MergeArgs& a, cudaStream_t stream);
 cudaError_t launch_prefill(const PrefillArgs& a, const CUtensorMap* tm_q, const CUtensorMap* tm_k,
                            const CUtensorMap* tm_v, int grid_tiles, cudaStream_t stream);
