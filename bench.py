@@ -286,8 +286,8 @@ def run_gpu(args, rank, world, local_rank):
             return
         pa.pa_reshape_and_cache(r.key, r.value, r.k_cache, r.v_cache, r.slot_mapping)
         if hybrid and ev is None:
-            # the hybrid batch in one call: the chunk's tiles co-scheduled
-            # beside the decode on the SMs it leaves free
+            # the hybrid batch in one call and one launch: the chunk's tile
+            # pairs beside the decode on the SMs it leaves free
             s0, q0, S_ = w.decode_seq0, w.q_decode_row0, w.num_decode_seqs
             pa.pa_hybrid_attention(r.out_chunk, r.q[:T], r.block_tables[:w.num_chunks], r.cu,
                                    r.qs, r.seq_lens[:w.num_chunks], max_q, r.out,
@@ -1004,7 +1004,8 @@ def main():
     fused = w.num_chunks == 0  # the step's decode carries the slot scatter (pa_decode_append)
     alg = decode_algorithmic_bytes(w, append=fused)
     achieved = alg / (res["dec_ms"] * 1e-3) / 1e9
-    traffic = profile_traffic(["pa_decode.cu", "pa_ptx.cuh", "pa_internal.h"],
+    traffic = profile_traffic(["pa_decode.cu", "pa_decode_body.cuh", "pa_ptx.cuh",
+                               "pa_internal.h"],
                               "decode_append_kernel_llama3_8b_decode_layer.md") \
         if args.config == "llama3_8b_decode_layer" else None
     e = res["e2e"]
@@ -1020,8 +1021,8 @@ def main():
                    "parallelism": f"replicas x{world}",
                    "launch": (f"CUDA graph per round of {args.replicas} steps ("
                               + ("copy-on-write block copies, " if len(w.cow_pairs) else "")
-                              + ("scatter, then pa_hybrid_attention: the decode on the SMs the "
-                                 "prefill chunk leaves free, the chunk beside it; "
+                              + ("scatter, then pa_hybrid_attention: one launch, the decode on "
+                                 "its first CTAs, the chunk's CTA pairs on the SMs it leaves free; "
                                  if w.num_chunks else
                                  "pa_decode_append: the slot scatter fused into the decode; ")
                               + "programmatic dependent launches)") if res["graphs"]
@@ -1066,7 +1067,8 @@ def main():
                                      frac_of_bf16_peak=tf / bf16,
                                      peak_source=f"{peak_src} (bf16_tflops, burst: timed alone)",
                                      tensor_pipe_ncu=profile_traffic(
-                                         ["pa_prefill.cu", "pa_ptx.cuh", "pa_internal.h"],
+                                         ["pa_prefill.cu", "pa_prefill_body.cuh",
+                                          "pa_ptx.cuh", "pa_internal.h"],
                                          "prefill_kernel_sarathi_chunk.md", "tensor_pipe_active_pct"))
     if res["chunk_ms"] is not None:
         if res["graphs"]:
@@ -1075,8 +1077,9 @@ def main():
                 "chunk_alone_ms": res["chunk_ms"],
                 "chunk_hidden_frac": max(0.0, min(1.0, (res["dec_ms"] + res["chunk_ms"] - step_ms)
                                                   / res["chunk_ms"])),
-                "how": "pa_hybrid_attention co-schedules the chunk's query tiles on the SMs the "
-                       "decode leaves free; step = scatter + that call"}
+                "how": "pa_hybrid_attention: one launch whose first CTAs run the decode and "
+                       "whose other CTAs run the chunk's query tiles as tensor-core CTA pairs on "
+                       "the SMs the decode leaves free; step = scatter + that call"}
     if rank == 0:
         line["cpu_baseline"] = cpu_baseline_obj(w, args.cpu_seconds)
         line["host_block_manager"] = block_manager_timing()

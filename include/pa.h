@@ -280,7 +280,7 @@ int pa_prefill_chunk(void *out, const void *q, const void *k_cache, const void *
 
 /*
  * Bytes of workspace pa_hybrid_attention needs (a balanced decode's workspace
- * plus 256 bytes); 0 on invalid sizes.
+ * plus 256 reserved bytes); 0 on invalid sizes.
  */
 size_t pa_hybrid_workspace_size(int num_decode_seqs, int num_q_heads, int num_kv_heads,
                                 int head_dim, int max_blocks_per_seq, int block_size);
@@ -293,14 +293,16 @@ size_t pa_hybrid_workspace_size(int num_decode_seqs, int num_q_heads, int num_kv
  * meaning and layouts) and the balanced decode of pa_decode with
  * partition_tokens = 0 (decode arguments).  Both read the same pools.
  *
- * Co-scheduled on one stream: the decode runs on num_sms - chunk_sms
- * persistent CTAs, and the chunk's query tiles start at once on the SMs it
- * leaves free, so the chunk's tensor-core work runs under the decode's HBM
- * streaming instead of after it.  chunk_sms = 0 picks about a fifth of the
- * SMs; values are clamped to [1, num_sms - 1].  The chunk reads nothing the
- * decode writes; the call's last kernel to finish waits for both, so work
- * queued after the call on the stream sees both results.  With no chunk (or
- * no decode) the call is pa_decode (or pa_prefill_chunk) alone.
+ * One kernel launch: its first CTAs (num_sms - chunk_sms, rounded down to
+ * an even count) run the balanced decode, one per SM, and the rest run the
+ * chunk's query tiles as tensor-core CTA pairs, which start at once on the SMs
+ * the decode leaves free, so the chunk's tensor-core work runs under the
+ * decode's HBM streaming instead of after it.  chunk_sms = 0 picks about a
+ * fifth of the SMs; values are clamped to [1, num_sms - 2].  The chunk reads
+ * nothing the decode writes; work queued after the call on the stream sees
+ * both results.  With no chunk (or no decode) the call is pa_decode (or
+ * pa_prefill_chunk) alone.  The decode of this call needs head_dim 128
+ * (PA_ERR_UNSUPPORTED otherwise), as the chunk does.
  *   workspace  device, pa_hybrid_workspace_size bytes, 256-byte aligned,
  *              zero-filled before its first use (calls leave it zeroed);
  *              one call in flight per workspace.

@@ -17,8 +17,9 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(ROOT, "_build")
 LIB = os.path.join(PKG, "libpa.so")
-SOURCES = ["pa_api.cu", "pa_decode.cu", "pa_prefill.cu", "pa_cascade.cu", "pa_block_manager.cpp"]
-HEADERS = ["pa_internal.h", "pa_ptx.cuh", os.path.join("..", "..", "include", "pa.h"),
+SOURCES = ["pa_api.cu", "pa_decode.cu", "pa_prefill.cu", "pa_hybrid.cu", "pa_cascade.cu",
+           "pa_block_manager.cpp"]
+HEADERS = ["pa_internal.h", "pa_ptx.cuh", "pa_decode_body.cuh", "pa_prefill_body.cuh", os.path.join("..", "..", "include", "pa.h"),
            os.path.join("..", "..", "include", "pa_block_manager.h")]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC,-O2", "--expt-relaxed-constexpr"]

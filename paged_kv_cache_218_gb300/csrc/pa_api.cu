@@ -553,7 +553,21 @@ static int decode_check(const void* out, const void* q, const void* k_cache, con
   return PA_OK;
 }
 
+// A launch's arguments and tensor maps, built by decode_impl / prefill_impl
+// without launching when the hybrid call fuses the two into one kernel.
+struct DecodePlan {
+  DecodeArgs a;
+  CUtensorMap tk, tv;
+  int grid;
+};
+struct PrefillPlan {
+  PrefillArgs a;
+  CUtensorMap tq, tk, tv;
+  int tiles;
+};
+
 // pa_decode and pa_decode_fp8: the same launch; kv_fp8 selects E4M3 pools.
+// plan non-null (balanced bf16 only): fill it and launch nothing.
 static int decode_impl(void* out, const void* q, const void* k_cache, const void* v_cache,
                        const float* k_scales, const float* v_scales, bool kv_fp8,
                        const int32_t* block_tables, int max_blocks_per_seq,
@@ -564,7 +578,8 @@ static int decode_impl(void* out, const void* q, const void* k_cache, const void
                        const float* init_o = nullptr, const float* init_lse = nullptr,
                        int grid_override = 0, int stall_loads = 0, uint64_t wait_ns = 0,
                        const void* new_k = nullptr, const void* new_v = nullptr,
-                       int64_t new_k_stride = 0, int64_t new_v_stride = 0) {
+                       int64_t new_k_stride = 0, int64_t new_v_stride = 0,
+                       DecodePlan* plan = nullptr) {
   if (int rc = decode_check(out, q, k_cache, v_cache, k_scales, v_scales, kv_fp8, block_tables,
                             max_blocks_per_seq, seq_lens, num_seqs, num_q_heads, num_kv_heads,
                             head_dim, block_size, num_blocks, scale, partition_tokens, out_lse,
@@ -635,6 +650,14 @@ static int decode_impl(void* out, const void* q, const void* k_cache, const void
   if (encode_pool_map(&tm_k, k_cache, num_blocks, num_kv_heads, head_dim, 0, elem) ||
       encode_pool_map(&tm_v, v_cache, num_blocks, num_kv_heads, head_dim, 0, elem))
     return PA_ERR_CUDA;
+  if (plan) {
+    if (mode != kModeBalanced || kv_fp8 || head_dim != 128) return PA_ERR_UNSUPPORTED;
+    plan->a = a;
+    plan->tk = tm_k;
+    plan->tv = tm_v;
+    plan->grid = grid;
+    return PA_OK;
+  }
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (launch_decode(a, &tm_k, &tm_v, head_dim, grid, st) != cudaSuccess) return PA_ERR_CUDA;
   if (mode == kModeFixedSplit) {
@@ -909,15 +932,15 @@ static int prefill_check(const void* out, const void* q, const void* k_cache, co
   return PA_OK;
 }
 
-// The chunk launch of pa_prefill_chunk; done_ctr non-null: co-scheduled
-// behind the decode just launched on the same stream (pa_hybrid_attention).
+// The chunk launch of pa_prefill_chunk; plan non-null: fill it and launch
+// nothing (pa_hybrid_attention).
 static int prefill_impl(void* out, const void* q, const void* k_cache, const void* v_cache,
                         const int32_t* block_tables, int max_blocks_per_seq,
                         const int32_t* cu_q_lens, const int32_t* q_start_pos,
                         const int32_t* seq_lens, int num_chunks, int total_q_tokens, int max_q_len,
                         int num_q_heads, int num_kv_heads, int head_dim, int block_size,
                         int64_t num_blocks, float scale, float* out_lse, void* stream,
-                        unsigned int* done_ctr, int stall_loads = 0, uint64_t wait_ns = 0) {
+                        PrefillPlan* plan, int stall_loads = 0, uint64_t wait_ns = 0) {
   bool done = false;
   if (int rc = prefill_check(out, q, k_cache, v_cache, block_tables, max_blocks_per_seq,
                              cu_q_lens, q_start_pos, seq_lens, num_chunks, total_q_tokens,
@@ -943,14 +966,12 @@ static int prefill_impl(void* out, const void* q, const void* k_cache, const voi
   a.num_q_heads = num_q_heads;
   a.num_kv_heads = num_kv_heads;
   a.group = group;
-  a.after_decode = done_ctr ? 1 : 0;
-  a.done_ctr = done_ctr;
   a.stall_loads = stall_loads;
   a.wait_ns = wait_ns;  // 0: the default limit
   const int tokens_per_tile = 128 / group;
   a.tiles_per_chunk = (max_q_len + tokens_per_tile - 1) / tokens_per_tile;
-  const int cl = prefill_cluster(done_ctr != nullptr);
-  a.tiles_per_chunk = (a.tiles_per_chunk + cl - 1) / cl * cl;
+  // whole CTA pairs: an odd count gets one tile more, which has no rows
+  a.tiles_per_chunk = (a.tiles_per_chunk + kMaxCluster - 1) / kMaxCluster * kMaxCluster;
   a.scale_log2 = scale * 1.4426950408889634f;
   CUtensorMap tm_q, tm_k, tm_v;
   if (encode_q_map(&tm_q, q, total_q_tokens, num_q_heads, head_dim, group, tokens_per_tile) ||
@@ -958,6 +979,14 @@ static int prefill_impl(void* out, const void* q, const void* k_cache, const voi
       encode_pool_map(&tm_v, v_cache, num_blocks, num_kv_heads, head_dim, kPool2D))
     return PA_ERR_CUDA;
   const int64_t tiles = static_cast<int64_t>(a.tiles_per_chunk) * num_chunks * num_kv_heads;
+  if (plan) {
+    plan->a = a;
+    plan->tq = tm_q;
+    plan->tk = tm_k;
+    plan->tv = tm_v;
+    plan->tiles = static_cast<int>(tiles);
+    return PA_OK;
+  }
   return launch_prefill(a, &tm_q, &tm_k, &tm_v, static_cast<int>(tiles),
                         static_cast<cudaStream_t>(stream)) == cudaSuccess
              ? PA_OK
@@ -1021,22 +1050,34 @@ int pa_hybrid_attention(void* out_chunk, const void* q_chunk, const int32_t* chu
                        decode_lse, dec_ws, dec_bytes, stream);
   DeviceInfo* d;
   if (int rc = current_device_info(&d)) return rc;
-  if (d->num_sms < 2) return PA_ERR_UNSUPPORTED;
+  if (d->num_sms < 4) return PA_ERR_UNSUPPORTED;
   // SMs left to the chunk: by default about a fifth (32 of 152), which on the
   // Sarathi batch of a 512-query chunk next to 128 decodes hides the chunk's
-  // tensor work under the decode's HBM streaming
+  // tensor work under the decode's HBM streaming.  The decode takes an even
+  // number of CTAs, so that the launch's clusters of two never mix the roles.
   int cs = chunk_sms > 0 ? chunk_sms : (d->num_sms * 21 + 50) / 100;
-  cs = cs < 1 ? 1 : (cs > d->num_sms - 1 ? d->num_sms - 1 : cs);
+  cs = cs < 1 ? 1 : (cs > d->num_sms - 2 ? d->num_sms - 2 : cs);
+  const int decode_ctas = (d->num_sms - cs) & ~1;
+  // the fused kernel holds the bf16 head_dim-128 decode only; the chunk
+  // call's checks above already required head_dim 128
+  DecodePlan dp;
   if (int rc = decode_impl(out_decode, q_decode, k_cache, v_cache, nullptr, nullptr, false,
                            decode_block_tables, decode_max_blocks, decode_seq_lens,
                            num_decode_seqs, num_q_heads, num_kv_heads, head_dim, block_size,
                            num_blocks, scale, 0, decode_lse, dec_ws, dec_bytes, stream, nullptr,
-                           nullptr, nullptr, d->num_sms - cs))
+                           nullptr, nullptr, decode_ctas, 0, 0, nullptr, nullptr, 0, 0, &dp))
     return rc;
-  return prefill_impl(out_chunk, q_chunk, k_cache, v_cache, chunk_block_tables, chunk_max_blocks,
-                      cu_q_lens, q_start_pos, chunk_seq_lens, num_chunks, total_q_tokens,
-                      max_q_len, num_q_heads, num_kv_heads, head_dim, block_size, num_blocks,
-                      scale, chunk_lse, stream, static_cast<unsigned int*>(workspace));
+  PrefillPlan pp;
+  if (int rc = prefill_impl(out_chunk, q_chunk, k_cache, v_cache, chunk_block_tables,
+                            chunk_max_blocks, cu_q_lens, q_start_pos, chunk_seq_lens, num_chunks,
+                            total_q_tokens, max_q_len, num_q_heads, num_kv_heads, head_dim,
+                            block_size, num_blocks, scale, chunk_lse, stream, &pp))
+    return rc;
+  if (dp.grid != decode_ctas) return PA_ERR_UNSUPPORTED;
+  return launch_hybrid(dp.a, &dp.tk, &dp.tv, pp.a, &pp.tq, &pp.tk, &pp.tv, dp.grid, pp.tiles,
+                       static_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? PA_OK
+             : PA_ERR_CUDA;
 }
 
 int pa_test_decode_stalled(void* out, const void* q, const void* k_cache, const void* v_cache,

@@ -99,8 +99,6 @@ struct PrefillArgs {
   int group;
   int tiles_per_chunk;  // M tiles of 128 rows per (chunk, kv head)
   float scale_log2;
-  int after_decode;          // co-scheduled behind a decode on the same stream
-  unsigned int* done_ctr;    // after_decode: CTAs finished (self-resetting)
   uint64_t wait_ns;          // limit of every mbarrier wait (normally kWaitLimitNs)
   int stall_loads;           // test launch: the loaders issue no load, every wait runs out
 };
@@ -148,11 +146,18 @@ bool decode_supported(int head_dim, int num_kv_heads, int num_q_heads, int mode,
 cudaError_t launch_merge(const MergeArgs& a, cudaStream_t stream);
 cudaError_t launch_prefill(const PrefillArgs& a, const CUtensorMap* tm_q, const CUtensorMap* tm_k,
                            const CUtensorMap* tm_v, int grid_tiles, cudaStream_t stream);
-size_t prefill_smem_bytes(bool co_scheduled);
+size_t prefill_smem_bytes();
 bool cascade_shape(int num_kv_heads, int group, int max_group, int* kv_per_cta, int* warps_per_kv,
                    int* stages);
 cudaError_t launch_cascade_prefix(const CascadeArgs& a, const CUtensorMap* tm_k,
                                   const CUtensorMap* tm_v, cudaStream_t stream);
-int prefill_cluster(bool co_scheduled);  // query tiles per cluster (the grid is a multiple of it)
+// One launch for a hybrid batch: the balanced decode (bf16, head_dim 128) on
+// its first decode_ctas CTAs and the prefill's CTA pairs on the rest.
+cudaError_t launch_hybrid(DecodeArgs d, const CUtensorMap* dk, const CUtensorMap* dv,
+                          const PrefillArgs& p, const CUtensorMap* pq, const CUtensorMap* pk,
+                          const CUtensorMap* pv, int decode_ctas, int prefill_ctas,
+                          cudaStream_t stream);
+// Shared-memory layout and warp split of a decode launch (pa_decode.cu).
+size_t decode_smem_bytes(DecodeArgs& a, int head_dim);
 
 }  // namespace pa

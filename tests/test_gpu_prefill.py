@@ -246,10 +246,9 @@ def _hybrid_ws(pa, w, dev):
 
 @pytest.mark.parametrize("chunk_sms", [0, 1, 8, 32, 64, 151, 1000])
 def test_sarathi_hybrid_co_scheduled_matches_oracle(pa, cuda_device, chunk_sms):
-    """pa_hybrid_attention: the decode on the SMs the chunk does not take,
-    the chunk's tiles beside it; both match the oracle, and the chunk is bit
-    for bit the output of pa_prefill_chunk (the same tiles, one per CTA
-    instead of four per cluster)."""
+    """pa_hybrid_attention, one launch: the decode on its first CTAs, the
+    chunk's tile pairs on the rest; both match the oracle, and the chunk is
+    bit for bit the output of pa_prefill_chunk (the same CTA-pair tiles)."""
     w, ref_c, ref_c_lse, ref_d = _hybrid()
     dw = DeviceWorkload(w, cuda_device)
     dw.scatter(pa)
@@ -267,8 +266,9 @@ def test_sarathi_hybrid_co_scheduled_matches_oracle(pa, cuda_device, chunk_sms):
 
 
 def test_sarathi_hybrid_co_scheduled_repeats_and_leaves_workspace_zeroed(pa, cuda_device):
-    """Ten calls in a row on one workspace (the chunk's finish counter and the
-    decode's tickets reset themselves); every call gives the same bits."""
+    """Ten calls in a row on one workspace (the decode's tickets reset
+    themselves, the reserved head stays zero); every call gives the same
+    bits."""
     w, _, _, ref_d = _hybrid()
     dw = DeviceWorkload(w, cuda_device)
     dw.scatter(pa)
