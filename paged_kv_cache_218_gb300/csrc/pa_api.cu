@@ -586,6 +586,7 @@ static int decode_impl(void* out, const void* q, const void* k_cache, const void
                             new_k != nullptr))
     return rc;
   if (num_seqs == 0) return PA_OK;
+  if (kv_fp8 && init_o) return PA_ERR_UNSUPPORTED;  // no E4M3 cascade suffix pass
   const int mode = decode_mode(partition_tokens);
   DeviceInfo* d;
   if (int rc = current_device_info(&d)) return rc;

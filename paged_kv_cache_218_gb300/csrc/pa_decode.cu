@@ -51,6 +51,11 @@ bool decode_supported(int head_dim, int num_kv_heads, int num_q_heads, int mode,
              .total <= 227 * 1024 - 1024;
 }
 
+// Balanced split: a sequence's fixed cost in blocks -- about the time its
+// piece takes outside the block loop (query fragments, partial result, merge
+// ticket) over the time of one block of streaming.
+static int piece_cost(bool kv_fp8) { return kv_fp8 ? 4 : 2; }
+
 size_t decode_smem_bytes(DecodeArgs& a, int head_dim) {
   const int pre = a.mode == kModeBalanced ? balanced_pre_ints(a.num_seqs) : 0;
   const int elem = a.kv_fp8 ? 1 : 2;
@@ -58,6 +63,7 @@ size_t decode_smem_bytes(DecodeArgs& a, int head_dim) {
   a.warps_per_head = warps_per_head(a.num_kv_heads);
   const bool append = a.new_k != nullptr;
   a.stages = pick_stages(head_dim, a.num_kv_heads, a.num_q_heads, pre, elem, append);
+  a.piece_cost = piece_cost(a.kv_fp8 != 0);
   return make_layout(head_dim, a.num_kv_heads, a.num_q_heads, a.warps_per_head, a.stages, pre,
                      elem, append).total +
          1024;

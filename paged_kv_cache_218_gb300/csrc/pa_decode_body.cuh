@@ -74,7 +74,9 @@ struct Cursor {
   long long idx, lo, hi;  // balanced block range [lo, hi)
   long long mid, end;     // balanced: walk [mid, hi) first, then [lo, mid)
   long long W;            // balanced: total blocks
-  int C;                  // balanced: CTAs that own a non-empty range
+  long long T;            // balanced: total cost, W + beta * S
+  int C;                  // balanced: CTAs that own a range
+  int beta;               // balanced: cost of a sequence, in blocks
   int phase;              // balanced: 0 while walking [mid, hi)
 };
 
@@ -133,9 +135,30 @@ __device__ __forceinline__ int start_block(const DecodeArgs& a, int s, int len, 
   return sb > nb ? nb : sb;
 }
 
-__device__ __forceinline__ long long cta_of(long long x, long long W, int C) {
-  // owner of global block x when CTA c owns [c*W/C, (c+1)*W/C)
-  return ((x + 1) * C + W - 1) / W - 1;
+// The balanced split charges every sequence a fixed cost of beta blocks on
+// top of its blocks: a piece costs its CTA more than its blocks (the queries'
+// fragments, the partial result and its merge ticket), so a range that starts
+// sequences gets fewer blocks.  Block x of sequence s sits at cost coordinate
+// x + beta * (s + 1); CTA c of C owns the costs [c*T/C, (c+1)*T/C) (floors),
+// T = W + beta * S.  owner_of_cost: the CTA owning cost point y.
+__device__ __forceinline__ long long owner_of_cost(long long y, long long T, int C) {
+  return ((y + 1) * C + T - 1) / T - 1;
+}
+
+// The smallest block whose cost coordinate is at least y (W if none).
+__device__ __forceinline__ long long block_at_cost(const int* pre, int S, int beta, long long y) {
+  // the first sequence s whose last cost point pre[s+1] - 1 + beta*(s+1) is >= y
+  int lo = 0, hi = S;
+  while (lo < hi) {
+    const int mid = (lo + hi) >> 1;
+    if (pre[mid + 1] + static_cast<long long>(beta) * (mid + 1) > y)
+      hi = mid;
+    else
+      lo = mid + 1;
+  }
+  if (lo == S) return pre[S];
+  const long long x = y - static_cast<long long>(beta) * (lo + 1);
+  return x > pre[lo] ? x : pre[lo];
 }
 
 // the sequence holding global block x: the largest s with pre[s] <= x
@@ -756,9 +779,12 @@ __device__ __forceinline__ void decode_cta(const CUtensorMap& tm_k, const CUtens
     cur = Cursor{};
     cur.W = pre[S];
     cur.C = static_cast<int>(cur.W < ncta ? cur.W : ncta);
+    // the per-sequence cost only once every CTA has a few blocks to stream
+    cur.beta = cur.W >= 2ll * ncta ? a.piece_cost : 0;
+    cur.T = cur.W + static_cast<long long>(cur.beta) * S;
     if (cta < cur.C) {
-      cur.lo = static_cast<long long>(cta) * cur.W / cur.C;
-      cur.hi = static_cast<long long>(cta + 1) * cur.W / cur.C;
+      cur.lo = block_at_cost(pre, S, cur.beta, static_cast<long long>(cta) * cur.T / cur.C);
+      cur.hi = block_at_cost(pre, S, cur.beta, static_cast<long long>(cta + 1) * cur.T / cur.C);
     } else {
       cur.lo = cur.hi = 0;
     }
@@ -1354,7 +1380,30 @@ __device__ __forceinline__ void decode_cta(const CUtensorMap& tm_k, const CUtens
     const bool writer = active && sub == 0;
     const int ha = 2 * q4, hb = 2 * q4 + 1;
     if (pc.kind == kFinal) {
-      if (writer) {
+      if constexpr (KV8) {
+        if (writer) {
+          // E4M3 layout: the lane holds dims [16 d0, 16 d0 + 16) of both heads,
+          // stored as two 16-byte pieces each
+          if (ha < G) {
+            uint4* dst = reinterpret_cast<uint4*>(a.out + (head0 + ha) * D + 16 * d0);
+            dst[0] = make_uint4(pack_bf16x2(o[0][0], o[0][2]), pack_bf16x2(o[1][0], o[1][2]),
+                                pack_bf16x2(o[2][0], o[2][2]), pack_bf16x2(o[3][0], o[3][2]));
+            dst[1] = make_uint4(pack_bf16x2(o[4][0], o[4][2]), pack_bf16x2(o[5][0], o[5][2]),
+                                pack_bf16x2(o[6][0], o[6][2]), pack_bf16x2(o[7][0], o[7][2]));
+          }
+          if (hb < G) {
+            uint4* dst = reinterpret_cast<uint4*>(a.out + (head0 + hb) * D + 16 * d0);
+            dst[0] = make_uint4(pack_bf16x2(o[0][1], o[0][3]), pack_bf16x2(o[1][1], o[1][3]),
+                                pack_bf16x2(o[2][1], o[2][3]), pack_bf16x2(o[3][1], o[3][3]));
+            dst[1] = make_uint4(pack_bf16x2(o[4][1], o[4][3]), pack_bf16x2(o[5][1], o[5][3]),
+                                pack_bf16x2(o[6][1], o[6][3]), pack_bf16x2(o[7][1], o[7][3]));
+          }
+          if (a.out_lse && d0 == 0) {
+            if (ha < G) a.out_lse[head0 + ha] = lsea;
+            if (hb < G) a.out_lse[head0 + hb] = lseb;
+          }
+        }
+      } else if (writer) {
 #pragma unroll
         for (int mt = 0; mt < KS; ++mt) {
           const int d = out_dim<KV8>(mt, d0, 0), d8 = out_dim<KV8>(mt, d0, 1);
@@ -1394,7 +1443,27 @@ __device__ __forceinline__ void decode_cta(const CUtensorMap& tm_k, const CUtens
     } else {
       // balanced partial: publish to this CTA's slot [Hq][D] + lse[Hq]
       float* slot = a.part_o + (static_cast<long long>(cta) * 2 + pc.which) * a.slot_floats;
-      if (writer) {
+      if constexpr (KV8) {
+        if (writer) {
+          // E4M3 layout: dims [16 d0, 16 d0 + 16) of both heads, as four
+          // 16-byte pieces each (scattered 4-byte stores cost the L1 one
+          // transaction per lane)
+          const int hga = hw * G + ha, hgb = hw * G + hb;
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            if (ha < G)
+              *reinterpret_cast<float4*>(slot + hga * D + 16 * d0 + 4 * i) =
+                  make_float4(o[2 * i][0], o[2 * i][2], o[2 * i + 1][0], o[2 * i + 1][2]);
+            if (hb < G)
+              *reinterpret_cast<float4*>(slot + hgb * D + 16 * d0 + 4 * i) =
+                  make_float4(o[2 * i][1], o[2 * i][3], o[2 * i + 1][1], o[2 * i + 1][3]);
+          }
+          if (d0 == 0) {
+            if (ha < G) slot[Hq * D + hga] = lsea;
+            if (hb < G) slot[Hq * D + hgb] = lseb;
+          }
+        }
+      } else if (writer) {
         const int hga = hw * G + ha, hgb = hw * G + hb;
 #pragma unroll
         for (int mt = 0; mt < KS; ++mt) {
@@ -1413,8 +1482,9 @@ __device__ __forceinline__ void decode_cta(const CUtensorMap& tm_k, const CUtens
           if (hb < G) slot[Hq * D + hgb] = lseb;
         }
       }
-      const long long cf = cta_of(pc.seg_start, cur.W, cur.C);
-      const int np = static_cast<int>(cta_of(pc.seg_start + pc.nb - 1, cur.W, cur.C) - cf + 1);
+      const long long c0 = pc.seg_start + static_cast<long long>(cur.beta) * (pc.s + 1);
+      const long long cf = owner_of_cost(c0, cur.T, cur.C);
+      const int np = static_cast<int>(owner_of_cost(c0 + pc.nb - 1, cur.T, cur.C) - cf + 1);
       // a piece before the walk's last: hand it to the merge warp (each
       // warp's slot stores, ordered by __syncwarp, are released by its
       // arrival) and go on with the next piece

@@ -43,6 +43,7 @@ struct DecodeArgs {
   int slot_floats;   // balanced: floats per partial slot
   int warps_per_head;  // set by the launcher
   int stages;          // set by the launcher
+  int piece_cost;      // balanced: a sequence's fixed cost in blocks (set by the launcher)
   int kv_fp8;          // pools hold E4M3 bytes (head_dim 128) with per-kv-head scales
   const float* k_scales;  // E4M3: [Hkv] dequantization scales of K and V
   const float* v_scales;
