@@ -511,6 +511,15 @@ __device__ __forceinline__ void prefill_cta(const CUtensorMap& tm_q, const CUten
       };
       bool ok = wait_or_abort<kPair>(bar_q, 0, abort_flag, a);
       int js = 0, jp = 0;  // next score tile / next PV product to issue
+      // ring positions of js and jp, kept as counters (no division per tile)
+      int s_buf = 0, s_kslot = 0, s_kphase = 0, p_buf = 0, p_phase = 0, p_vslot = 0, p_vphase = 0;
+      // Descriptors of the operands' first k-step: a k-step's descriptor is
+      // the base's plus its byte offset / 16 (the start-address field, whose
+      // sum stays below 2^14 in a 227 KB shared memory), so the issue loop
+      // adds a constant per product instead of building each descriptor.
+      const uint64_t dq = smem_desc(sbase + P::kQOff, 16, 1024);
+      const uint64_t dk0 = smem_desc(sbase + P::kKOff, 16, 1024);
+      const uint64_t dv0 = smem_desc(sbase + P::kVOff, kHalf, 1024);
       IdleClock clk(a.wait_ns);
       while (ok && jp < nkt) {
         bool progressed = false;
@@ -520,36 +529,48 @@ __device__ __forceinline__ void prefill_cta(const CUtensorMap& tm_q, const CUten
         // cannot overwrite P before that product has read it (waiting for
         // the product to complete drained the pipe every tile)
         if (js < nkt && (js < kNS || jp > js - kNS) &&
-            bar_test<kPair>(bar_k_full + 8 * (js % kNK), (js / kNK) & 1)) {
+            bar_test<kPair>(bar_k_full + 8 * s_kslot, s_kphase)) {
           // operands are TMA loads, ordered by their barrier: no tcgen05 fence
-          const uint32_t kt = sbase + P::kKOff + (js % kNK) * P::kKSlot;
+          const uint64_t dk = dk0 + static_cast<uint64_t>((s_kslot * P::kKSlot) >> 4);
+          const uint32_t dst = tmem + s_buf * 128;
 #pragma unroll
           for (int ks = 0; ks < 8; ++ks)
-            tc_mma_f16<kPair>(tmem + (js % kNS) * 128,
-                              smem_desc(sbase + P::kQOff + (ks >> 2) * kHalf + (ks & 3) * 32, 16,
-                                        1024),
-                              smem_desc(kt + (ks >> 2) * P::kKHalf + (ks & 3) * 32, 16, 1024),
-                              idesc_s, ks > 0);
-          commit(bar_s_full + 8 * (js % kNS));
-          if constexpr (!kFreeByS<kPair>) commit(bar_k_empty + 8 * (js % kNK));
+            tc_mma_f16<kPair>(dst, dq + (((ks >> 2) * kHalf + (ks & 3) * 32) >> 4),
+                              dk + (((ks >> 2) * P::kKHalf + (ks & 3) * 32) >> 4), idesc_s,
+                              ks > 0);
+          commit(bar_s_full + 8 * s_buf);
+          if constexpr (!kFreeByS<kPair>) commit(bar_k_empty + 8 * s_kslot);
           ++js;
+          s_buf = s_buf + 1 == kNS ? 0 : s_buf + 1;
+          if (++s_kslot == kNK) {
+            s_kslot = 0;
+            s_kphase ^= 1;
+          }
           progressed = true;
         }
         // O += P_jp V_jp once the softmax wrote P_jp and V_jp is ready
-        if (jp < js && bar_test<kPair>(bar_p_full + 8 * (jp % kNS), (jp / kNS) & 1) &&
-            bar_test<kPair>(bar_v_ready + 8 * (jp % kNV), (jp / kNV) & 1)) {
+        if (jp < js && bar_test<kPair>(bar_p_full + 8 * p_buf, p_phase) &&
+            bar_test<kPair>(bar_v_ready + 8 * p_vslot, p_vphase)) {
           if (kPair == 2 && jp == tail_tile) fence_acq_rel_cluster();  // the peer's zeroed rows
           tc_fence_after();
-          const uint32_t vt = sbase + P::kVOff + (jp % kNV) * P::kVSlot;
+          const uint64_t dv = dv0 + static_cast<uint64_t>((p_vslot * P::kVSlot) >> 4);
+          const uint32_t ta = tmem + p_buf * 128;
 #pragma unroll
           for (int ks = 0; ks < 8; ++ks)
-            tc_mma_f16_tmem_a<kPair>(tmem + kTmemO,
-                                     tmem + (jp % kNS) * 128 + (ks >> 2) * 64 + (ks & 3) * 8,
-                                     smem_desc(vt + ks * kBlockBytes, kHalf, 1024), idesc_o,
+            tc_mma_f16_tmem_a<kPair>(tmem + kTmemO, ta + (ks >> 2) * 64 + (ks & 3) * 8,
+                                     dv + ((ks * kBlockBytes) >> 4), idesc_o,
                                      (jp > 0 || ks > 0) ? 1u : 0u);
-          commit(bar_o_done + 8 * (jp % kNS));
-          if constexpr (!kFreeByPV<kPair>) commit(bar_v_empty + 8 * (jp % kNV));
+          commit(bar_o_done + 8 * p_buf);
+          if constexpr (!kFreeByPV<kPair>) commit(bar_v_empty + 8 * p_vslot);
           ++jp;
+          if (++p_buf == kNS) {
+            p_buf = 0;
+            p_phase ^= 1;
+          }
+          if (++p_vslot == kNV) {
+            p_vslot = 0;
+            p_vphase ^= 1;
+          }
           progressed = true;
         }
         if (progressed) {
