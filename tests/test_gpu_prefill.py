@@ -327,3 +327,41 @@ def test_hybrid_rejects_bad_arguments_before_launching(pa, cuda_device):
     assert e.value.status == pa.PA_ERR_INVALID
     torch.cuda.synchronize()
     assert pa.pa_device_error_flags() == 0
+
+
+HYBRID_SHAPES = [
+    # (chunk_tokens, chunk_start, num_decode, dec_lo, dec_hi, Hq, Hkv, seed)
+    (96, 200, 20, 1, 300, 16, 8, 1),     # group 2, decodes from one token up
+    (130, 0, 50, 16, 700, 32, 4, 2),     # group 8, chunk from position 0, a ragged tile
+    (1, 5000, 300, 100, 2000, 8, 8, 3),  # group 1, a one-token chunk beside many decodes
+    (256, 64, 7, 2000, 9000, 32, 8, 4),  # group 4, few long decodes: pieces split across CTAs
+]
+
+
+@pytest.mark.parametrize("ct,cs,nd,lo,hi,Hq,Hkv,seed", HYBRID_SHAPES)
+def test_hybrid_one_launch_shapes_match_oracle(pa, cuda_device, ct, cs, nd, lo, hi, Hq, Hkv,
+                                               seed):
+    """The one-launch hybrid kernel (decode CTAs and prefill CTA pairs in one
+    grid) on other shapes than the Sarathi batch, NaN in every unused slot:
+    both results match the oracle, at the default chunk share and at a
+    narrow one."""
+    w = W.sarathi_hybrid(seed=900 + seed, poison=True, chunk_tokens=ct, chunk_start=cs,
+                         num_decode=nd, dec_lo=lo, dec_hi=hi, Hq=Hq, Hkv=Hkv, D=128)
+    kc, vc = oracle_scattered(w)
+    ref_c, ref_c_lse = oracle.prefill(w.chunk_q, kc, vc, w.block_tables[:1], w.cu_q_lens,
+                                      w.q_start_pos, w.seq_lens[:1], w.scale)
+    ref_d, ref_d_lse = oracle.decode(w.decode_q, kc, vc, w.decode_block_tables,
+                                     w.decode_seq_lens, w.scale)
+    dw = DeviceWorkload(w, cuda_device)
+    dw.scatter(pa)
+    ws = _hybrid_ws(pa, w, cuda_device)
+    for chunk_sms in (0, 8):
+        out_c, out_d, lse_c, lse_d = _hybrid_call(pa, dw, ws, chunk_sms)
+        torch.cuda.synchronize()
+        what = f"hybrid G={Hq // Hkv} chunk {ct}@{cs} decodes {nd}, chunk_sms {chunk_sms}"
+        assert_close(out_c, ref_c, what + " chunk")
+        assert_close(lse_c.cpu().numpy(), ref_c_lse, what + " chunk lse")
+        assert_close(out_d, ref_d, what + " decodes")
+        assert_close(lse_d.cpu().numpy(), ref_d_lse, what + " decodes lse")
+    assert int(ws[:256].count_nonzero()) == 0
+    assert pa.pa_device_error_flags() == 0
