@@ -54,7 +54,7 @@ bool decode_supported(int head_dim, int num_kv_heads, int num_q_heads, int mode,
 // Balanced split: a sequence's fixed cost in blocks -- about the time its
 // piece takes outside the block loop (query fragments, partial result, merge
 // ticket) over the time of one block of streaming.
-static int piece_cost(bool kv_fp8) { return kv_fp8 ? 4 : 2; }
+static int piece_cost(bool kv_fp8) { return kv_fp8 ? 4 : 1; }
 
 size_t decode_smem_bytes(DecodeArgs& a, int head_dim) {
   const int pre = a.mode == kModeBalanced ? balanced_pre_ints(a.num_seqs) : 0;
