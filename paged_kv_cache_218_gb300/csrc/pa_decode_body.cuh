@@ -6,10 +6,18 @@
 // section 2 PagedAttention: the kernel gathers K/V from non-contiguous
 // 16-token blocks named by the block table).  Design:
 //
-//  * Persistent CTAs, one per SM: 8 consumer warps + 1 producer warp.
+//  * Persistent CTAs, at most one per SM: 8 consumer warps, 1 producer warp
+//    and 1 merge warp (which takes the merge tickets of the balanced split's
+//    mid-walk partial pieces).
 //  * Work is a list of (sequence, block range) pieces covering *all* kv heads
 //    of each block, so one physical block -- 16 tokens x Hkv heads x D,
 //    contiguous in the pool -- is streamed as a whole (DRAM-page friendly).
+//    The balanced split cuts the batch's blocks into one contiguous range per
+//    CTA on a cost coordinate where each sequence adds a fixed cost, so a
+//    range that starts sequences (pieces) gets fewer blocks.
+//  * Variants: KV8 reads E4M3 pools (converted to f16 in registers); AP
+//    writes each sequence's new token into its slot and into the landed
+//    stage (the scatter fused into the decode step).
 //  * The producer walks the CTA's pieces, prefetches block-table rows 32
 //    entries at a time, and lands each block in a ring of shared-memory
 //    stages with TMA tensor loads: for K and for V, one box per 64-column

@@ -50,7 +50,8 @@
 //    shared by the two half-row owners, p = 2^(x - m) rounded to bf16 and
 //    stored back into tensor memory (tcgen05.st) over the first half of the
 //    score columns it came from, where the PV product reads it as its A
-//    operand; a score buffer takes new scores once that PV product is done.
+//    operand; a score buffer takes new scores once that PV product is
+//    issued (the tensor core runs one thread's products in issue order).
 //    The running maximum only moves (and O in tensor memory is only
 //    rescaled) when the row maximum grows by more than 2^8, which keeps every
 //    p below 256 and the fp32 accumulators far from overflow; the final
