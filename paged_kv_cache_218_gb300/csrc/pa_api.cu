@@ -73,9 +73,30 @@ bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p
 // rows == kPool2D: the pool as a 2-D tensor (Hkv * D columns, tokens), box =
 // 64 columns x 16 tokens: one head's half of a block, as the 3-D box with
 // rows = 16 but cheaper for the TMA unit.
+// rows == kPoolKeyTile (bf16, D = 128): the pool as a 4-D tensor (64 columns,
+// 8 tokens, 2 * Hkv column chunks of 64, num_blocks * 2 groups of 8 tokens),
+// box 64 x 8 x 2 x 2: one head's whole block in one load, landing as
+// [token group][64-column half][8 tokens][64 columns].  Every 8-token group
+// of a 64-column half then sits 2 KB after the previous one, block after
+// block, a uniform stride for a K-major operand descriptor.
 constexpr int kPool2D = 1 << 20;
+constexpr int kPoolKeyTile = kPool2D + 1;
 int encode_pool_map_uncached(CUtensorMap* m, const void* pool, int64_t num_blocks, int Hkv, int D,
                              int rows, int elem) {
+  if (rows == kPoolKeyTile) {
+    if (D != 128 || elem != 2) return PA_ERR_UNSUPPORTED;
+    const cuuint64_t row_bytes = static_cast<cuuint64_t>(Hkv) * D * elem;
+    cuuint64_t dims4[4] = {64, 8, 2 * static_cast<cuuint64_t>(Hkv),
+                           static_cast<cuuint64_t>(num_blocks) * 2};
+    cuuint64_t strides4[3] = {row_bytes, 128, 8 * row_bytes};
+    cuuint32_t box4[4] = {64, 8, 2, 2};
+    cuuint32_t estr4[4] = {1, 1, 1, 1};
+    CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(pool), dims4,
+                          strides4, box4, estr4, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                          CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? PA_OK : PA_ERR_CUDA;
+  }
   if (rows == kPool2D) {
     cuuint64_t dims2[2] = {static_cast<cuuint64_t>(Hkv) * D,
                            static_cast<cuuint64_t>(num_blocks) * kBlockSize};
@@ -976,7 +997,7 @@ static int prefill_impl(void* out, const void* q, const void* k_cache, const voi
   a.scale_log2 = scale * 1.4426950408889634f;
   CUtensorMap tm_q, tm_k, tm_v;
   if (encode_q_map(&tm_q, q, total_q_tokens, num_q_heads, head_dim, group, tokens_per_tile) ||
-      encode_pool_map(&tm_k, k_cache, num_blocks, num_kv_heads, head_dim, kPool2D) ||
+      encode_pool_map(&tm_k, k_cache, num_blocks, num_kv_heads, head_dim, kPoolKeyTile) ||
       encode_pool_map(&tm_v, v_cache, num_blocks, num_kv_heads, head_dim, kPool2D))
     return PA_ERR_CUDA;
   const int64_t tiles = static_cast<int64_t>(a.tiles_per_chunk) * num_chunks * num_kv_heads;

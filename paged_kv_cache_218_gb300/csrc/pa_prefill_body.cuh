@@ -29,21 +29,26 @@
 //  * In a hybrid batch (pa_hybrid_attention) the same pairs run in the launch
 //    of the decodes, on the SMs the decode's CTAs leave free.
 //  * Warp roles.  Warp 9 loads Q once, then the K tiles; warp 10 the V
-//    tiles (128 keys each, assembled from 16-token paged blocks by TMA boxes
-//    of a 2-D view of the pool, 128-byte swizzle) in rings of three, and
+//    tiles (128 keys each, assembled from 16-token paged blocks by TMA
+//    boxes, 128-byte swizzle) in rings of three, and
 //    reports each landed V tile to the MMA issuer after zeroing the slots of
 //    a sequence's last block that lie past its length.  A K slot is free
 //    once the scores of its tile are done, a V slot once its PV product is.
 //    Each loader reads its block ids 32 tiles at a time into shared memory.
-//    Warp 8 issues the tensor-core work from one thread (of the even CTA of a
+//    A K box is a whole block of one head (both 64-column halves, 4 KB: a
+//    4-D view of the pool that splits the block's 16 tokens into two groups
+//    of 8 around the half), a V box the CTA's 64-column half of a block (2
+//    KB, a 2-D view): 4 + 8 boxes per tile and CTA of a pair.
+//    Warp 8 issues the score products from one thread (of the even CTA of a
 //    pair): S = Q K^T into one of three tensor-memory score buffers
-//    (tcgen05.mma, N = 128, K = 16, bf16 in, fp32 accumulate) and O += P V
-//    into a fourth region.  Warps 0-7 run the softmax: two warps per
-//    tensor-memory lane quadrant, each owning 64 of a row's 128 score columns.
+//    (tcgen05.mma, N = 128, K = 16, bf16 in, fp32 accumulate); warp 11 the
+//    products O += P V into a fourth region.  Warps 0-7 run the softmax:
+//    two warps per tensor-memory lane quadrant, each owning 64 of a row's
+//    128 score columns.
 //  * Three score buffers.  Scores of a tile can be computed as soon as its K
 //    tile lands (while the softmax still works on the two before it), so a K
 //    tile leaves its ring slot soon after it arrives.
-//  * Pipelining.  Loader and MMA issuer poll their barriers and issue
+//  * Pipelining.  Loaders and MMA issuers poll their barriers and issue
 //    whatever is ready, so scores of the next tiles are computed while the
 //    softmax works on tile j and PV of tile j-1 runs meanwhile.
 //  * Softmax per row: tcgen05.ld of its scores, causal mask, row maximum
@@ -51,7 +56,7 @@
 //    stored back into tensor memory (tcgen05.st) over the first half of the
 //    score columns it came from, where the PV product reads it as its A
 //    operand; a score buffer takes new scores once that PV product is
-//    issued (the tensor core runs one thread's products in issue order).
+//    complete.
 //    The running maximum only moves (and O in tensor memory is only
 //    rescaled) when the row maximum grows by more than 2^8, which keeps every
 //    p below 256 and the fp32 accumulators far from overflow; the final
@@ -75,26 +80,31 @@ namespace {
 
 static_assert(kMaxCluster == 2, "tile counts are bounded with kMaxCluster");
 constexpr int kSoftmaxWarps = 8;
-constexpr int kMmaWarp = 8;
+constexpr int kMmaWarp = 8;     // issues the score products S = Q K^T
 constexpr int kLoadKWarp = 9;   // Q and K tiles
 constexpr int kLoadVWarp = 10;  // V tiles, and their reports to the MMA issuer
-constexpr int kThreads = 11 * 32;
+constexpr int kPvWarp = 11;     // issues the PV products O += P V
+constexpr int kThreads = 12 * 32;
 constexpr int kTileKeys = 128;
 constexpr int kHalf = 128 * 128;  // a 64-column half of a 128-row operand: 128 rows x 128 B
 constexpr int kBlockBytes = kBlockSize * 128;  // one paged block's 64-column half: 16 rows x 128 B
+// K slot layout: block b of the slot at 4 KB * b, as [8-token group g][64-column
+// half h][8 tokens][128 B]: key 8 * (2b + g) + r of half h at 2 KB * (2b + g) +
+// 1 KB * h + 128 B * r, so a half's 8-key groups are 2 KB apart throughout
+constexpr int kKGroupStride = 2048;
+constexpr int kKHalfOffset = 1024;
 constexpr int kIdBatch = 32;      // tiles whose block ids the loader reads at once
 constexpr int kIdRing = 2 * kIdBatch;  // tiles whose block ids are kept in shared memory
 constexpr int kMaxRing = 4;       // barrier slots per K / V ring
 
-// Shared-memory plan of one CTA.  kPair 1: whole K / V tiles (two 64-column
-// halves of 128 keys); kPair 2: this CTA's half of each (64 keys x 128
-// columns of K, 128 keys x 64 columns of V).
+// Shared-memory plan of one CTA.  kPair 1: whole K / V tiles (128 keys x 128
+// columns); kPair 2: this CTA's half of each (64 keys x 128 columns of K,
+// 128 keys x 64 columns of V).
 template <int kPair>
 struct Plan {
   static constexpr int kNK = kPair == 2 ? 3 : 2;  // K tiles in flight
   static constexpr int kNV = kPair == 2 ? 3 : 2;  // V tiles in flight
   static constexpr int kKSlot = 2 * kHalf / kPair;
-  static constexpr int kKHalf = kKSlot / 2;       // one 64-column half of a K slot
   static constexpr int kVSlot = 2 * kHalf / kPair;
   static constexpr int kQOff = 0;
   static constexpr int kKOff = kQOff + 2 * kHalf;
@@ -352,7 +362,7 @@ __device__ __forceinline__ void prefill_cta(const CUtensorMap& tm_q, const CUten
     };
     if (warp == kLoadKWarp) {
       // loads of this CTA completing on the issuer's barrier `bar`: Q (3-D
-      // map) and K boxes of the 2-D pool map
+      // map) and K boxes of the 4-D pool map
       auto load_q = [&](uint32_t dst, int x, int y, int z, uint32_t bar) {
         if constexpr (kPair == 2) {
           if (!issuer) {
@@ -362,14 +372,14 @@ __device__ __forceinline__ void prefill_cta(const CUtensorMap& tm_q, const CUten
         }
         tma_load_3d(dst, &tm_q, x, y, z, bar, pol);
       };
-      auto load_k = [&](uint32_t dst, int x, int y, uint32_t bar) {
+      auto load_k = [&](uint32_t dst, int chunk, int group8, uint32_t bar) {
         if constexpr (kPair == 2) {
           if (!issuer) {
-            tma_load_2d_pair(dst, &tm_k, x, y, mapa_shared(bar, 0), pol);
+            tma_load_4d_pair(dst, &tm_k, 0, 0, chunk, group8, mapa_shared(bar, 0), pol);
             return;
           }
         }
-        tma_load_2d(dst, &tm_k, x, y, bar, pol);
+        tma_load_4d(dst, &tm_k, 0, 0, chunk, group8, bar, pol);
       };
       // a stalled test launch issues no load: every wait runs out with no
       // copy in flight
@@ -382,9 +392,9 @@ __device__ __forceinline__ void prefill_cta(const CUtensorMap& tm_q, const CUten
       }
       // K tile j = paged blocks 8j .. 8j+7 (id -1 past the visible keys: a box
       // outside the pool, which reads zeros); CTA r of a pair takes keys
-      // 64r .. 64r+63 (blocks 4r .. 4r+3); one box per lane: (block li,
-      // 64-column half h).  The issuer's barrier counts the pair's whole tile.
-      const int li = lane >> 1, h = lane & 1;
+      // 64r .. 64r+63 (blocks 4r .. 4r+3); one box per lane: block `lane`,
+      // both halves of head kvh (column chunks 2 kvh, 2 kvh + 1; token groups
+      // 2 id, 2 id + 1).  The issuer's barrier counts the pair's whole tile.
       int jk = a.stall_loads ? nkt : 0;
       while (jk < nkt && !*abort_flag) {
         bool progressed = false;
@@ -405,10 +415,10 @@ __device__ __forceinline__ void prefill_cta(const CUtensorMap& tm_q, const CUten
           const uint32_t bar = bar_k_full + 8 * slot;
           if (lane == 0 && issuer) mbar_arrive_expect_tx(bar, 2 * kHalf);
           __syncwarp();
-          if (li < 8 / kPair) {
-            const int id = ids_smem[(jk % kIdRing) * 8 + li + (kPair == 2 ? 4 * rank : 0)];
-            load_k(sbase + P::kKOff + slot * P::kKSlot + h * P::kKHalf + li * kBlockBytes,
-                   kvh * 128 + h * 64, id * kBlockSize, bar);
+          if (lane < 8 / kPair) {
+            const int id = ids_smem[(jk % kIdRing) * 8 + lane + (kPair == 2 ? 4 * rank : 0)];
+            load_k(sbase + P::kKOff + slot * P::kKSlot + lane * 2 * kBlockBytes, 2 * kvh, 2 * id,
+                   bar);
           }
           __syncwarp();
           ++jk;
@@ -501,87 +511,105 @@ __device__ __forceinline__ void prefill_cta(const CUtensorMap& tm_q, const CUten
                                ((nkt - 1 - sl) / kNV) & 1, abort_flag, a);
     }
     __syncwarp();
-  } else if (warp == kMmaWarp) {
+  } else if (warp == kMmaWarp || warp == kPvWarp) {
     // ------------------------------------------------------------ tensor-core issue
+    // Two issuing threads of the even CTA, one per product: each blocks in
+    // its own MMA issues and commits while the other's products keep the
+    // tensor pipe fed (one thread issuing both left the pipe idle during its
+    // commits and barrier polls, which set the pace of a tile).  A commit
+    // tracks the products of the thread that makes it.
     if (lane == 0 && issuer) {
-      const uint32_t idesc_s = instr_desc(0, 128 * kPair), idesc_o = instr_desc(1, 128 * kPair);
       // a completion reaches this CTA's barrier and, for a pair, the peer's
       auto commit = [&](uint32_t bar) {
         tc_commit<kPair>(bar);
         if constexpr (kPair == 2) tc_commit<kPair>(mapa_shared(bar, 1));
       };
-      bool ok = wait_or_abort<kPair>(bar_q, 0, abort_flag, a);
-      int js = 0, jp = 0;  // next score tile / next PV product to issue
-      // ring positions of js and jp, kept as counters (no division per tile)
-      int s_buf = 0, s_kslot = 0, s_kphase = 0, p_buf = 0, p_phase = 0, p_vslot = 0, p_vphase = 0;
-      // Descriptors of the operands' first k-step: a k-step's descriptor is
-      // the base's plus its byte offset / 16 (the start-address field, whose
-      // sum stays below 2^14 in a 227 KB shared memory), so the issue loop
-      // adds a constant per product instead of building each descriptor.
-      const uint64_t dq = smem_desc(sbase + P::kQOff, 16, 1024);
-      const uint64_t dk0 = smem_desc(sbase + P::kKOff, 16, 1024);
-      const uint64_t dv0 = smem_desc(sbase + P::kVOff, kHalf, 1024);
       IdleClock clk(a.wait_ns);
-      while (ok && jp < nkt) {
-        bool progressed = false;
-        // S(js) = Q K_js^T into score buffer js % 3, once K_js landed and PV
-        // of tile js-3, which reads its P from that buffer, is issued: the
-        // tensor core runs one thread's MMAs in issue order, so the scores
-        // cannot overwrite P before that product has read it (waiting for
-        // the product to complete drained the pipe every tile)
-        if (js < nkt && (js < kNS || jp > js - kNS) &&
-            bar_test<kPair>(bar_k_full + 8 * s_kslot, s_kphase)) {
-          // operands are TMA loads, ordered by their barrier: no tcgen05 fence
-          const uint64_t dk = dk0 + static_cast<uint64_t>((s_kslot * P::kKSlot) >> 4);
-          const uint32_t dst = tmem + s_buf * 128;
-#pragma unroll
-          for (int ks = 0; ks < 8; ++ks)
-            tc_mma_f16<kPair>(dst, dq + (((ks >> 2) * kHalf + (ks & 3) * 32) >> 4),
-                              dk + (((ks >> 2) * P::kKHalf + (ks & 3) * 32) >> 4), idesc_s,
-                              ks > 0);
-          commit(bar_s_full + 8 * s_buf);
-          if constexpr (!kFreeByS<kPair>) commit(bar_k_empty + 8 * s_kslot);
-          ++js;
-          s_buf = s_buf + 1 == kNS ? 0 : s_buf + 1;
-          if (++s_kslot == kNK) {
-            s_kslot = 0;
-            s_kphase ^= 1;
-          }
-          progressed = true;
+      auto give_up = [&]() {
+        if (!*abort_flag) {
+          *abort_flag = 1;
+          atomicOr(a.err, PA_DEVERR_TIMEOUT);
         }
-        // O += P_jp V_jp once the softmax wrote P_jp and V_jp is ready
-        if (jp < js && bar_test<kPair>(bar_p_full + 8 * p_buf, p_phase) &&
-            bar_test<kPair>(bar_v_ready + 8 * p_vslot, p_vphase)) {
-          if (kPair == 2 && jp == tail_tile) fence_acq_rel_cluster();  // the peer's zeroed rows
-          tc_fence_after();
-          const uint64_t dv = dv0 + static_cast<uint64_t>((p_vslot * P::kVSlot) >> 4);
-          const uint32_t ta = tmem + p_buf * 128;
+      };
+      if (warp == kMmaWarp) {
+        const uint32_t idesc_s = instr_desc(0, 128 * kPair);
+        bool ok = wait_or_abort<kPair>(bar_q, 0, abort_flag, a);
+        // Descriptors of the operands' first k-step: a k-step's descriptor
+        // is the base's plus its byte offset / 16 (the start-address field,
+        // whose sum stays below 2^14 in a 227 KB shared memory), so the
+        // issue loop adds a constant per product instead of building each.
+        const uint64_t dq = smem_desc(sbase + P::kQOff, 16, 1024);
+        const uint64_t dk0 = smem_desc(sbase + P::kKOff, 16, kKGroupStride);
+        // ring positions of js, kept as counters (no division per tile);
+        // s_round = js / kNS
+        int js = 0, s_buf = 0, s_round = 0, s_kslot = 0, s_kphase = 0;
+        while (ok && js < nkt) {
+          // S(js) = Q K_js^T into score buffer js % 3 once K_js landed and
+          // PV of tile js-3, which reads its P from that buffer, completed
+          if (bar_test<kPair>(bar_k_full + 8 * s_kslot, s_kphase) &&
+              (js < kNS || bar_test<kPair>(bar_o_done + 8 * s_buf, (s_round + 1) & 1))) {
+            // the K operand is a TMA load, ordered by its barrier; the
+            // buffer's last reader is a product of the other thread
+            if (js >= kNS) tc_fence_after();
+            const uint64_t dk = dk0 + static_cast<uint64_t>((s_kslot * P::kKSlot) >> 4);
+            const uint32_t dst = tmem + s_buf * 128;
 #pragma unroll
-          for (int ks = 0; ks < 8; ++ks)
-            tc_mma_f16_tmem_a<kPair>(tmem + kTmemO, ta + (ks >> 2) * 64 + (ks & 3) * 8,
-                                     dv + ((ks * kBlockBytes) >> 4), idesc_o,
-                                     (jp > 0 || ks > 0) ? 1u : 0u);
-          commit(bar_o_done + 8 * p_buf);
-          if constexpr (!kFreeByPV<kPair>) commit(bar_v_empty + 8 * p_vslot);
-          ++jp;
-          if (++p_buf == kNS) {
-            p_buf = 0;
-            p_phase ^= 1;
+            for (int ks = 0; ks < 8; ++ks)
+              tc_mma_f16<kPair>(dst, dq + (((ks >> 2) * kHalf + (ks & 3) * 32) >> 4),
+                                dk + (((ks >> 2) * kKHalfOffset + (ks & 3) * 32) >> 4), idesc_s,
+                                ks > 0);
+            commit(bar_s_full + 8 * s_buf);
+            if constexpr (!kFreeByS<kPair>) commit(bar_k_empty + 8 * s_kslot);
+            ++js;
+            if (++s_buf == kNS) {
+              s_buf = 0;
+              ++s_round;
+            }
+            if (++s_kslot == kNK) {
+              s_kslot = 0;
+              s_kphase ^= 1;
+            }
+            clk.progress();
+          } else if (*abort_flag || clk.expired()) {
+            give_up();
+            ok = false;
           }
-          if (++p_vslot == kNV) {
-            p_vslot = 0;
-            p_vphase ^= 1;
-          }
-          progressed = true;
         }
-        if (progressed) {
-          clk.progress();
-        } else if (*abort_flag || clk.expired()) {
-          if (!*abort_flag) {
-            *abort_flag = 1;
-            atomicOr(a.err, PA_DEVERR_TIMEOUT);
+      } else {
+        const uint32_t idesc_o = instr_desc(1, 128 * kPair);
+        const uint64_t dv0 = smem_desc(sbase + P::kVOff, kHalf, 1024);
+        int jp = 0, p_buf = 0, p_phase = 0, p_vslot = 0, p_vphase = 0;
+        bool ok = true;
+        while (ok && jp < nkt) {
+          // O += P_jp V_jp once the softmax wrote P_jp (so S(jp) is done)
+          // and V_jp is ready
+          if (bar_test<kPair>(bar_p_full + 8 * p_buf, p_phase) &&
+              bar_test<kPair>(bar_v_ready + 8 * p_vslot, p_vphase)) {
+            if (kPair == 2 && jp == tail_tile) fence_acq_rel_cluster();  // the peer's zeroed rows
+            tc_fence_after();
+            const uint64_t dv = dv0 + static_cast<uint64_t>((p_vslot * P::kVSlot) >> 4);
+            const uint32_t ta = tmem + p_buf * 128;
+#pragma unroll
+            for (int ks = 0; ks < 8; ++ks)
+              tc_mma_f16_tmem_a<kPair>(tmem + kTmemO, ta + (ks >> 2) * 64 + (ks & 3) * 8,
+                                       dv + ((ks * kBlockBytes) >> 4), idesc_o,
+                                       (jp > 0 || ks > 0) ? 1u : 0u);
+            commit(bar_o_done + 8 * p_buf);
+            if constexpr (!kFreeByPV<kPair>) commit(bar_v_empty + 8 * p_vslot);
+            ++jp;
+            if (++p_buf == kNS) {
+              p_buf = 0;
+              p_phase ^= 1;
+            }
+            if (++p_vslot == kNV) {
+              p_vslot = 0;
+              p_vphase ^= 1;
+            }
+            clk.progress();
+          } else if (*abort_flag || clk.expired()) {
+            give_up();
+            ok = false;
           }
-          ok = false;
         }
       }
     }
