@@ -250,64 +250,9 @@ __device__ __forceinline__ void prefill_cta(const CUtensorMap& tm_q, const CUten
   const int m = mg * kPair + rank;
   const bool issuer = rank == 0;     // issues the (pair's) tensor-core work
 
-  // launched as a programmatic dependent of the previous kernel (the scatter
-  // of this step's K/V): nothing before this line touches global memory
-  griddep_wait();
-  // the next kernel on the stream may start launching; it waits for this grid
-  griddep_launch_dependents();
-
-  // ---- chunk metadata (uniform over the CTA, and over a pair)
-  const int q0 = a.cu_q_lens[c], q1 = a.cu_q_lens[c + 1];
-  const int p0 = a.q_start_pos[c], n = a.seq_lens[c];
-  const int qlen = q1 - q0;
-  if (q0 < 0 || q1 > a.total_q || qlen < 0 || p0 < 0 || p0 + qlen > n ||
-      n > a.max_blocks * kBlockSize) {
-    if (tid == 0 && m == 0 && kvh == 0) atomicOr(a.err, PA_DEVERR_CHUNK);
-    return;
-  }
-  const int t0 = m * tpt;
-  const int tc0 = mg * kPair * tpt;  // first query token of the pair
-  if (tc0 >= qlen) return;  // the whole pair is past the chunk
-  const int tv = qlen - t0 < tpt ? qlen - t0 : tpt;  // valid tokens here (<= 0: none)
-  // keys [0, kmax) are visible to some row of the pair; both CTAs walk the
-  // same tiles (their own rows mask what they may not see)
-  const int kmax = p0 + min(qlen, tc0 + kPair * tpt);
-  const int nkt = (kmax + kTileKeys - 1) / kTileKeys;
-  const int nb_vis = (kmax + kBlockSize - 1) / kBlockSize;
-  // the K/V tile holding the sequence's last block when that block is only
-  // partly filled (its slots past seq_len are zeroed before PV), else -1
-  const int tail_tile = ((n & (kBlockSize - 1)) != 0 && (n - 1) / kBlockSize < nb_vis)
-                            ? (n - 1) / kBlockSize / 8
-                            : -1;
-  // Each loader warp reads block ids kIdBatch tiles at a time (eight loads
-  // in flight per lane) into its own shared-memory ring: read one tile at a
-  // time, ahead of its loads, the table's latency set the pace of the whole
-  // pipeline.
-  // Blocks past the visible keys get id -1, which TMA reads as zeros.
-  auto fetch_ids = [&](int t_first) {
-    const long long row = static_cast<long long>(c) * a.max_blocks;
-    const int jb0 = t_first * 8;
-    int v[8];
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      const int jb = jb0 + lane + 32 * i;
-      v[i] = jb < nb_vis ? a.block_tables[row + jb] : -1;
-    }
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      const int jb = jb0 + lane + 32 * i;
-      int id = v[i];
-      if (jb < nb_vis && (id < 0 || id >= a.num_blocks)) {
-        atomicOr(a.err, PA_DEVERR_BLOCK_ID);
-        id = -1;
-      }
-      ids_smem[jb % (kIdRing * 8)] = id;
-    }
-    __syncwarp();
-  };
-  // the first batch now, so that the table's latency overlaps the set-up
-  if (warp == kLoadKWarp || warp == kLoadVWarp) fetch_ids(0);
-
+  // Barriers and tensor memory are set up before the grid-dependency wait,
+  // while the previous kernel on the stream may still run: none of it
+  // touches global memory.
   if (tid == 0) {
     mbar_init(bar_q, 1);
     for (int k = 0; k < kNK; ++k) {
@@ -338,6 +283,81 @@ __device__ __forceinline__ void prefill_cta(const CUtensorMap& tm_q, const CUten
     __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+
+  // launched as a programmatic dependent of the previous kernel (the scatter
+  // of this step's K/V): nothing before this line touches global memory
+  griddep_wait();
+  // the next kernel on the stream may start launching; it waits for this grid
+  griddep_launch_dependents();
+
+  // Each loader warp reads block ids kIdBatch tiles at a time (eight loads
+  // in flight per lane) into its own shared-memory ring: read one tile at a
+  // time, ahead of its loads, the table's latency set the pace of the whole
+  // pipeline.  read_ids issues the loads of a batch (entries the table row
+  // holds), put_ids stores them: blocks past the visible keys get id -1,
+  // which TMA reads as zeros, and ids outside the pool are flagged and read
+  // as -1 too.
+  const long long id_row = static_cast<long long>(c) * a.max_blocks;
+  auto read_ids = [&](int t_first, int lim, int (&v)[8]) {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int jb = t_first * 8 + lane + 32 * i;
+      v[i] = jb < lim ? a.block_tables[id_row + jb] : -1;
+    }
+  };
+  auto put_ids = [&](int t_first, int nb_vis, const int (&v)[8]) {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int jb = t_first * 8 + lane + 32 * i;
+      int id = jb < nb_vis ? v[i] : -1;
+      if (jb < nb_vis && (id < 0 || id >= a.num_blocks)) {
+        atomicOr(a.err, PA_DEVERR_BLOCK_ID);
+        id = -1;
+      }
+      ids_smem[jb % (kIdRing * 8)] = id;
+    }
+    __syncwarp();
+  };
+  // The loaders' first batch is requested together with the chunk's
+  // metadata (the whole of the table row's first entries, which any chunk
+  // may read), so the two round trips overlap.
+  int ids0[8];
+  if (warp == kLoadKWarp || warp == kLoadVWarp) read_ids(0, a.max_blocks, ids0);
+
+  // ---- chunk metadata (uniform over the CTA, and over a pair)
+  const int q0 = a.cu_q_lens[c], q1 = a.cu_q_lens[c + 1];
+  const int p0 = a.q_start_pos[c], n = a.seq_lens[c];
+  const int qlen = q1 - q0;
+  if (q0 < 0 || q1 > a.total_q || qlen < 0 || p0 < 0 || p0 + qlen > n ||
+      n > a.max_blocks * kBlockSize) {
+    if (tid == 0 && m == 0 && kvh == 0) atomicOr(a.err, PA_DEVERR_CHUNK);
+    if (warp == 0) tmem_dealloc<kPair>(tmem, kTmemCols);  // uniform over the pair
+    return;
+  }
+  const int t0 = m * tpt;
+  const int tc0 = mg * kPair * tpt;  // first query token of the pair
+  if (tc0 >= qlen) {  // the whole pair is past the chunk
+    if (warp == 0) tmem_dealloc<kPair>(tmem, kTmemCols);
+    return;
+  }
+  const int tv = qlen - t0 < tpt ? qlen - t0 : tpt;  // valid tokens here (<= 0: none)
+  // keys [0, kmax) are visible to some row of the pair; both CTAs walk the
+  // same tiles (their own rows mask what they may not see)
+  const int kmax = p0 + min(qlen, tc0 + kPair * tpt);
+  const int nkt = (kmax + kTileKeys - 1) / kTileKeys;
+  const int nb_vis = (kmax + kBlockSize - 1) / kBlockSize;
+  // the K/V tile holding the sequence's last block when that block is only
+  // partly filled (its slots past seq_len are zeroed before PV), else -1
+  const int tail_tile = ((n & (kBlockSize - 1)) != 0 && (n - 1) / kBlockSize < nb_vis)
+                            ? (n - 1) / kBlockSize / 8
+                            : -1;
+  auto fetch_ids = [&](int t_first) {
+    int v[8];
+    read_ids(t_first, nb_vis, v);
+    put_ids(t_first, nb_vis, v);
+  };
+  if (warp == kLoadKWarp || warp == kLoadVWarp) put_ids(0, nb_vis, ids0);
+
 
   if (warp == kLoadKWarp || warp == kLoadVWarp) {
     // ------------------------------------------------------------ loaders
