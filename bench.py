@@ -262,8 +262,11 @@ def run_gpu(args, rank, world, local_rank):
                                                           w.max_blocks_per_seq), dev)
            for _ in range(R)] if hybrid else None
     cow = len(w.cow_pairs) > 0
-    # a decode-only step fuses the slot scatter into the decode (pa_decode_append)
-    launches_per_step = (2 if hybrid else 1) + (1 if P > 0 else 0) + (1 if hybrid else 0) \
+    # a decode-only step fuses the slot scatter into the decode (pa_decode_append),
+    # a hybrid step into its one launch (pa_hybrid_attention_append); eager
+    # hybrid steps run scatter, chunk and decode as three launches
+    use_graphs_cfg = not args.no_graphs
+    launches_per_step = (1 if (use_graphs_cfg or not hybrid) else 3) + (1 if P > 0 else 0) \
         + (1 if cow else 0)
 
     def append(i):
@@ -284,16 +287,18 @@ def run_gpu(args, rank, world, local_rank):
             if ev is not None:
                 ev[1].record(cur)
             return
-        pa.pa_reshape_and_cache(r.key, r.value, r.k_cache, r.v_cache, r.slot_mapping)
         if hybrid and ev is None:
-            # the hybrid batch in one call and one launch: the chunk's tile
-            # pairs beside the decode on the SMs it leaves free
+            # the hybrid batch in one call and one launch: the step's slot
+            # scatter, and the chunk's tile pairs beside the decode on the SMs
+            # it leaves free
             s0, q0, S_ = w.decode_seq0, w.q_decode_row0, w.num_decode_seqs
-            pa.pa_hybrid_attention(r.out_chunk, r.q[:T], r.block_tables[:w.num_chunks], r.cu,
-                                   r.qs, r.seq_lens[:w.num_chunks], max_q, r.out,
-                                   r.q[q0:q0 + S_], r.block_tables[s0:], r.seq_lens[s0:],
-                                   r.k_cache, r.v_cache, w.scale, hws[i % R])
+            pa.pa_hybrid_attention_append(
+                r.out_chunk, r.q[:T], r.key[:T], r.value[:T], r.block_tables[:w.num_chunks],
+                r.cu, r.qs, r.seq_lens[:w.num_chunks], max_q, r.out, r.q[q0:q0 + S_],
+                r.key[T:T + S_], r.value[T:T + S_], r.block_tables[s0:], r.seq_lens[s0:],
+                r.k_cache, r.v_cache, w.scale, hws[i % R])
             return
+        pa.pa_reshape_and_cache(r.key, r.value, r.k_cache, r.v_cache, r.slot_mapping)
         if hybrid:  # timed kernel by kernel (no graphs): chunk and decode on two streams
             s_chunk.wait_stream(cur)
             if cev is not None:
@@ -660,13 +665,14 @@ def run_e2e(args, w, reps, ws, dev, pa, dist, s_chunk, max_q, T, hws):
                                 r.v_cache, v["block_tables"][s0:], v["seq_lens"][s0:], w.scale,
                                 partition_tokens=P, workspace=ws[j])
             return
-        pa.pa_reshape_and_cache(v["key"], v["value"], r.k_cache, r.v_cache, v["slot_mapping"])
-        if hybrid and not args.no_graphs:
-            pa.pa_hybrid_attention(out_chunk, v["q"][:T], v["block_tables"][:C], v["cu"],
-                                   v["qs"], v["seq_lens"][:C], max_q, out, v["q"][q0:q0 + S],
-                                   v["block_tables"][s0:], v["seq_lens"][s0:], r.k_cache,
-                                   r.v_cache, w.scale, hws[j])
+        if hybrid and not args.no_graphs:  # slot scatter fused into the hybrid launch
+            pa.pa_hybrid_attention_append(
+                out_chunk, v["q"][:T], v["key"][:T], v["value"][:T], v["block_tables"][:C],
+                v["cu"], v["qs"], v["seq_lens"][:C], max_q, out, v["q"][q0:q0 + S],
+                v["key"][T:T + S], v["value"][T:T + S], v["block_tables"][s0:],
+                v["seq_lens"][s0:], r.k_cache, r.v_cache, w.scale, hws[j])
             return
+        pa.pa_reshape_and_cache(v["key"], v["value"], r.k_cache, r.v_cache, v["slot_mapping"])
         if hybrid:
             s_chunk.wait_stream(comp)
             pa.pa_prefill_chunk(out_chunk, v["q"][:T], r.k_cache, r.v_cache,
@@ -1054,8 +1060,9 @@ def main():
                    "parallelism": f"replicas x{world}",
                    "launch": (f"CUDA graph per round of {args.replicas} steps ("
                               + ("copy-on-write block copies, " if len(w.cow_pairs) else "")
-                              + ("scatter, then pa_hybrid_attention: one launch, the decode on "
-                                 "its first CTAs, the chunk's CTA pairs on the SMs it leaves free; "
+                              + ("pa_hybrid_attention_append: one launch with the slot scatter "
+                                 "fused in, the decode on its first CTAs, the chunk's CTA pairs on "
+                                 "the SMs it leaves free; "
                                  if w.num_chunks else
                                  "pa_decode_append: the slot scatter fused into the decode; ")
                               + "programmatic dependent launches)") if res["graphs"]
@@ -1110,9 +1117,10 @@ def main():
                 "chunk_alone_ms": res["chunk_ms"],
                 "chunk_hidden_frac": max(0.0, min(1.0, (res["dec_ms"] + res["chunk_ms"] - step_ms)
                                                   / res["chunk_ms"])),
-                "how": "pa_hybrid_attention: one launch whose first CTAs run the decode and "
-                       "whose other CTAs run the chunk's query tiles as tensor-core CTA pairs on "
-                       "the SMs the decode leaves free; step = scatter + that call"}
+                "how": "pa_hybrid_attention_append: one launch whose first CTAs run the decode "
+                       "(each writing its sequences' new tokens) and whose other CTAs run the "
+                       "chunk's query tiles as tensor-core CTA pairs on the SMs the decode leaves "
+                       "free (each writing its tile's new rows); step = that call"}
     if rank == 0:
         line["cpu_baseline"] = cpu_baseline_obj(w, args.cpu_seconds)
         line["host_block_manager"] = block_manager_timing()

@@ -323,6 +323,44 @@ int pa_hybrid_attention(void *out_chunk, const void *q_chunk, const int32_t *chu
                         void *stream);
 
 /*
+ * pa_hybrid_attention_append -- one Sarathi hybrid step with the step's slot
+ * scatter fused in ("03 - Engines Papers", section 3 Sarathi / Sarathi-Serve:
+ * a step carries a prefill chunk and decodes; section 2 PagedAttention: the
+ * step's new K/V go into their slots before attention reads them).  The
+ * result is that of pa_reshape_and_cache of every new row, then
+ * pa_hybrid_attention with the same arguments, in one kernel launch:
+ *   key_chunk / value_chunk  device bf16 [total_q_tokens, *, Hkv, D], row i
+ *              the K / V of query row i of the chunk inputs; chunk c's row
+ *              q0 + t (q0 = cu_q_lens[c]) goes into the slot of position
+ *              q_start_pos[c] + t of chunk c's block table;
+ *   key_decode / value_decode  device bf16 [num_decode_seqs, *, Hkv, D], row
+ *              s the new token of decode s, which goes into the slot of
+ *              position decode_seq_lens[s] - 1 (as pa_decode_append);
+ *   key_token_stride / value_token_stride  elements between consecutive rows
+ *              of both the chunk's and the decodes' arrays (>= Hkv * D, a
+ *              multiple of 8); pointers 16-byte aligned.
+ * The chunk's keys at its own positions are read from key_chunk / value_chunk,
+ * not from the pool the same launch is writing, so every chunk must start a
+ * block: q_start_pos[c] a multiple of 16 (chunks of a multiple of 16 tokens
+ * after whole cached blocks are).  A chunk that does not is skipped and
+ * flagged (PA_DEVERR_CHUNK); use pa_reshape_and_cache + pa_hybrid_attention
+ * for it.  Slots receiving new rows must be owned by their sequence alone
+ * (copy-on-write done before).  Every other argument, the workspace and the
+ * errors as pa_hybrid_attention; with no decodes the launch runs the chunk
+ * alone (workspace unused), with no chunk it is pa_decode_append.
+ */
+int pa_hybrid_attention_append(
+    void *out_chunk, const void *q_chunk, const void *key_chunk, const void *value_chunk,
+    const int32_t *chunk_block_tables, int chunk_max_blocks, const int32_t *cu_q_lens,
+    const int32_t *q_start_pos, const int32_t *chunk_seq_lens, int num_chunks,
+    int total_q_tokens, int max_q_len, float *chunk_lse, void *out_decode, const void *q_decode,
+    const void *key_decode, const void *value_decode, const int32_t *decode_block_tables,
+    int decode_max_blocks, const int32_t *decode_seq_lens, int num_decode_seqs, float *decode_lse,
+    int64_t key_token_stride, int64_t value_token_stride, void *k_cache, void *v_cache,
+    int num_q_heads, int num_kv_heads, int head_dim, int block_size, int64_t num_blocks,
+    float scale, int chunk_sms, void *workspace, size_t workspace_bytes, void *stream);
+
+/*
  * pa_decode_append -- one decode step with the slot scatter fused in:
  * sequence s's new token (row s of key / value, [num_seqs, *, Hkv, D] bf16
  * with token strides in elements) is written into the slot of position

@@ -66,6 +66,9 @@ _SIGS = {
     "pa_hybrid_attention": ([_P, _P, _P, _I, _P, _P, _P, _I, _I, _I, _P,
                              _P, _P, _P, _I, _P, _I, _P,
                              _P, _P, _I, _I, _I, _I, _L, _F, _I, _P, _S, _P], _I),
+    "pa_hybrid_attention_append": ([_P, _P, _P, _P, _P, _I, _P, _P, _P, _I, _I, _I, _P,
+                                    _P, _P, _P, _P, _P, _I, _P, _I, _P, _L, _L,
+                                    _P, _P, _I, _I, _I, _I, _L, _F, _I, _P, _S, _P], _I),
     "pa_test_decode_stalled": ([_P, _P, _P, _P, _P, _I, _P, _I, _I, _I, _I, _I, _L, _F, _I, _P,
                                 _S, ctypes.c_uint, _P], _I),
     "pa_test_prefill_stalled": ([_P, _P, _P, _P, _P, _I, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I,
@@ -388,6 +391,53 @@ def pa_hybrid_attention(out_chunk, q_chunk, chunk_block_tables, cu_q_lens, q_sta
         _ptr(decode_seq_lens), q_decode.shape[0], _ptr(decode_lse),
         _ptr(k_cache), _ptr(v_cache), Hq, Hkv, D, bs, nb, float(scale), int(chunk_sms),
         _ptr(workspace), workspace.numel(), _stream(stream)))
+
+
+def pa_hybrid_attention_append(out_chunk, q_chunk, key_chunk, value_chunk, chunk_block_tables,
+                               cu_q_lens, q_start_pos, chunk_seq_lens, max_q_len, out_decode,
+                               q_decode, key_decode, value_decode, decode_block_tables,
+                               decode_seq_lens, k_cache, v_cache, scale, workspace, chunk_sms=0,
+                               chunk_lse=None, decode_lse=None, stream=None) -> None:
+    """One hybrid step with its slot scatter fused in: the chunk's and the
+    decodes' new K/V rows go into their slots, then pa_hybrid_attention."""
+    _need(out_chunk, "out_chunk", torch.bfloat16, 3)
+    _need(q_chunk, "q_chunk", torch.bfloat16, 3)
+    _need(chunk_block_tables, "chunk_block_tables", torch.int32, 2)
+    _need(cu_q_lens, "cu_q_lens", torch.int32, 1)
+    _need(q_start_pos, "q_start_pos", torch.int32, 1)
+    _need(chunk_seq_lens, "chunk_seq_lens", torch.int32, 1)
+    _need(out_decode, "out_decode", torch.bfloat16, 3)
+    _need(q_decode, "q_decode", torch.bfloat16, 3)
+    _need(decode_block_tables, "decode_block_tables", torch.int32, 2)
+    _need(decode_seq_lens, "decode_seq_lens", torch.int32, 1)
+    _need(k_cache, "k_cache", torch.bfloat16, 4)
+    _need(v_cache, "v_cache", torch.bfloat16, 4)
+    rows = [(key_chunk, "key_chunk"), (value_chunk, "value_chunk"), (key_decode, "key_decode"),
+            (value_decode, "value_decode")]
+    for t, n in rows:
+        _need(t, n, torch.bfloat16, 3, contiguous=False)
+        if t.stride(2) != 1 or t.stride(1) != t.shape[2]:
+            raise ValueError(f"{n} must be contiguous within a token")
+    if key_chunk.stride(0) != key_decode.stride(0) or value_chunk.stride(0) != value_decode.stride(0):
+        raise ValueError("the chunk's and the decodes' rows must share their token strides")
+    if workspace is not None:
+        _need(workspace, "workspace", torch.uint8, 1)
+    if chunk_lse is not None:
+        _need(chunk_lse, "chunk_lse", torch.float32, 2)
+    if decode_lse is not None:
+        _need(decode_lse, "decode_lse", torch.float32, 2)
+    T, Hq, D = q_chunk.shape
+    nb, bs, Hkv, _ = k_cache.shape
+    ws_bytes = 0 if workspace is None else workspace.numel()
+    _check("pa_hybrid_attention_append", _lib.pa_hybrid_attention_append(
+        _ptr(out_chunk), _ptr(q_chunk), _ptr(key_chunk), _ptr(value_chunk),
+        _ptr(chunk_block_tables), chunk_block_tables.shape[1], _ptr(cu_q_lens), _ptr(q_start_pos),
+        _ptr(chunk_seq_lens), q_start_pos.shape[0], T, int(max_q_len), _ptr(chunk_lse),
+        _ptr(out_decode), _ptr(q_decode), _ptr(key_decode), _ptr(value_decode),
+        _ptr(decode_block_tables), decode_block_tables.shape[1], _ptr(decode_seq_lens),
+        q_decode.shape[0], _ptr(decode_lse), key_chunk.stride(0), value_chunk.stride(0),
+        _ptr(k_cache), _ptr(v_cache), Hq, Hkv, D, bs, nb, float(scale), int(chunk_sms),
+        _ptr(workspace), ws_bytes, _stream(stream)))
 
 
 def _host_ptr(a):

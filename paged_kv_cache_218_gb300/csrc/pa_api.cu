@@ -183,6 +183,32 @@ int encode_q_map(CUtensorMap* m, const void* q, int64_t T, int Hq, int D, int he
   return r == CUDA_SUCCESS ? PA_OK : PA_ERR_CUDA;
 }
 
+// A chunk's new K / V rows [T, Hkv, 128] (token strides in elements), read
+// by the prefill in place of the pool's slots they are being written to:
+// K as (64 columns, T tokens, 2 * Hkv column chunks), box 64 x 8 x 2 -- 8
+// tokens of one head's whole row, landing as [64-column half][8 tokens][64
+// columns], one token group of a K block in the prefill's layout; V as
+// (Hkv * 128 columns, T tokens), box 64 x 16, as the pool's 2-D view.
+int encode_new_row_maps(CUtensorMap* nk, CUtensorMap* nv, const void* key, const void* value,
+                        int64_t T, int Hkv, int64_t k_stride, int64_t v_stride) {
+  cuuint64_t kd[3] = {64, static_cast<cuuint64_t>(T), 2 * static_cast<cuuint64_t>(Hkv)};
+  cuuint64_t ks[2] = {static_cast<cuuint64_t>(k_stride) * 2, 128};
+  cuuint32_t kb[3] = {64, 8, 2};
+  cuuint32_t e3[3] = {1, 1, 1};
+  CUresult r = g_encode(nk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(key), kd, ks,
+                        kb, e3, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return PA_ERR_CUDA;
+  cuuint64_t vd[2] = {static_cast<cuuint64_t>(Hkv) * 128, static_cast<cuuint64_t>(T)};
+  cuuint64_t vs[1] = {static_cast<cuuint64_t>(v_stride) * 2};
+  cuuint32_t vb[2] = {64, static_cast<cuuint32_t>(kBlockSize)};
+  cuuint32_t e2[2] = {1, 1};
+  r = g_encode(nv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(value), vd, vs, vb, e2,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? PA_OK : PA_ERR_CUDA;
+}
+
 int check_shape(int Hq, int Hkv, int D, int block_size) {
   if (Hq <= 0 || Hkv <= 0 || D <= 0 || block_size <= 0) return PA_ERR_INVALID;
   if (Hq % Hkv != 0) return PA_ERR_INVALID;
@@ -584,6 +610,7 @@ struct DecodePlan {
 struct PrefillPlan {
   PrefillArgs a;
   CUtensorMap tq, tk, tv;
+  CUtensorMap tnk, tnv;  // the chunks' new rows (append only)
   int tiles;
 };
 
@@ -962,7 +989,9 @@ static int prefill_impl(void* out, const void* q, const void* k_cache, const voi
                         const int32_t* seq_lens, int num_chunks, int total_q_tokens, int max_q_len,
                         int num_q_heads, int num_kv_heads, int head_dim, int block_size,
                         int64_t num_blocks, float scale, float* out_lse, void* stream,
-                        PrefillPlan* plan, int stall_loads = 0, uint64_t wait_ns = 0) {
+                        PrefillPlan* plan, int stall_loads = 0, uint64_t wait_ns = 0,
+                        const void* new_k = nullptr, const void* new_v = nullptr,
+                        int64_t new_k_stride = 0, int64_t new_v_stride = 0) {
   bool done = false;
   if (int rc = prefill_check(out, q, k_cache, v_cache, block_tables, max_blocks_per_seq,
                              cu_q_lens, q_start_pos, seq_lens, num_chunks, total_q_tokens,
@@ -990,6 +1019,12 @@ static int prefill_impl(void* out, const void* q, const void* k_cache, const voi
   a.group = group;
   a.stall_loads = stall_loads;
   a.wait_ns = wait_ns;  // 0: the default limit
+  a.new_k = static_cast<const __nv_bfloat16*>(new_k);
+  a.new_v = static_cast<const __nv_bfloat16*>(new_v);
+  a.new_k_stride = new_k_stride;
+  a.new_v_stride = new_v_stride;
+  a.k_pool = static_cast<__nv_bfloat16*>(const_cast<void*>(k_cache));
+  a.v_pool = static_cast<__nv_bfloat16*>(const_cast<void*>(v_cache));
   const int tokens_per_tile = 128 / group;
   a.tiles_per_chunk = (max_q_len + tokens_per_tile - 1) / tokens_per_tile;
   // whole CTA pairs: an odd count gets one tile more, which has no rows
@@ -1006,9 +1041,15 @@ static int prefill_impl(void* out, const void* q, const void* k_cache, const voi
     plan->tq = tm_q;
     plan->tk = tm_k;
     plan->tv = tm_v;
+    plan->tnk = tm_k;  // not read without new rows
+    plan->tnv = tm_v;
+    if (new_k && encode_new_row_maps(&plan->tnk, &plan->tnv, new_k, new_v, total_q_tokens,
+                                     num_kv_heads, new_k_stride, new_v_stride))
+      return PA_ERR_CUDA;
     plan->tiles = static_cast<int>(tiles);
     return PA_OK;
   }
+  if (new_k) return PA_ERR_INVALID;  // new rows go through the hybrid launch only
   return launch_prefill(a, &tm_q, &tm_k, &tm_v, static_cast<int>(tiles),
                         static_cast<cudaStream_t>(stream)) == cudaSuccess
              ? PA_OK
@@ -1096,8 +1137,84 @@ int pa_hybrid_attention(void* out_chunk, const void* q_chunk, const int32_t* chu
                             block_size, num_blocks, scale, chunk_lse, stream, &pp))
     return rc;
   if (dp.grid != decode_ctas) return PA_ERR_UNSUPPORTED;
-  return launch_hybrid(dp.a, &dp.tk, &dp.tv, pp.a, &pp.tq, &pp.tk, &pp.tv, dp.grid, pp.tiles,
-                       static_cast<cudaStream_t>(stream)) == cudaSuccess
+  return launch_hybrid(dp.a, &dp.tk, &dp.tv, pp.a, &pp.tq, &pp.tk, &pp.tv, &pp.tnk, &pp.tnv,
+                       dp.grid, pp.tiles, static_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? PA_OK
+             : PA_ERR_CUDA;
+}
+
+int pa_hybrid_attention_append(
+    void* out_chunk, const void* q_chunk, const void* key_chunk, const void* value_chunk,
+    const int32_t* chunk_block_tables, int chunk_max_blocks, const int32_t* cu_q_lens,
+    const int32_t* q_start_pos, const int32_t* chunk_seq_lens, int num_chunks,
+    int total_q_tokens, int max_q_len, float* chunk_lse, void* out_decode, const void* q_decode,
+    const void* key_decode, const void* value_decode, const int32_t* decode_block_tables,
+    int decode_max_blocks, const int32_t* decode_seq_lens, int num_decode_seqs, float* decode_lse,
+    int64_t key_token_stride, int64_t value_token_stride, void* k_cache, void* v_cache,
+    int num_q_heads, int num_kv_heads, int head_dim, int block_size, int64_t num_blocks,
+    float scale, int chunk_sms, void* workspace, size_t workspace_bytes, void* stream) {
+  bool no_chunk = false;
+  if (int rc = prefill_check(out_chunk, q_chunk, k_cache, v_cache, chunk_block_tables,
+                             chunk_max_blocks, cu_q_lens, q_start_pos, chunk_seq_lens, num_chunks,
+                             total_q_tokens, max_q_len, num_q_heads, num_kv_heads, head_dim,
+                             block_size, num_blocks, scale, &no_chunk))
+    return rc;
+  if (num_decode_seqs < 0 || chunk_sms < 0) return PA_ERR_INVALID;
+  const int64_t row = static_cast<int64_t>(num_kv_heads) * head_dim;
+  if (key_token_stride < row || value_token_stride < row || key_token_stride % 8 ||
+      value_token_stride % 8)
+    return PA_ERR_INVALID;
+  if (!no_chunk && (!key_chunk || !value_chunk || !aligned(key_chunk, 16) ||
+                    !aligned(value_chunk, 16)))
+    return PA_ERR_INVALID;
+  if (num_decode_seqs > 0 && (!key_decode || !value_decode || !aligned(key_decode, 16) ||
+                              !aligned(value_decode, 16)))
+    return PA_ERR_INVALID;
+  if (no_chunk)
+    return pa_decode_append(out_decode, q_decode, key_decode, value_decode, key_token_stride,
+                            value_token_stride, k_cache, v_cache, decode_block_tables,
+                            decode_max_blocks, decode_seq_lens, num_decode_seqs, num_q_heads,
+                            num_kv_heads, head_dim, block_size, num_blocks, scale, 0, decode_lse,
+                            workspace ? static_cast<char*>(workspace) + 256 : nullptr,
+                            workspace_bytes > 256 ? workspace_bytes - 256 : 0, stream);
+  DeviceInfo* d;
+  if (int rc = current_device_info(&d)) return rc;
+  if (d->num_sms < 4) return PA_ERR_UNSUPPORTED;
+  PrefillPlan pp;
+  if (int rc = prefill_impl(out_chunk, q_chunk, k_cache, v_cache, chunk_block_tables,
+                            chunk_max_blocks, cu_q_lens, q_start_pos, chunk_seq_lens, num_chunks,
+                            total_q_tokens, max_q_len, num_q_heads, num_kv_heads, head_dim,
+                            block_size, num_blocks, scale, chunk_lse, stream, &pp, 0, 0,
+                            key_chunk, value_chunk, key_token_stride, value_token_stride))
+    return rc;
+  DecodePlan dp;
+  int decode_ctas = 0;
+  if (num_decode_seqs > 0) {
+    const size_t need = pa_hybrid_workspace_size(num_decode_seqs, num_q_heads, num_kv_heads,
+                                                 head_dim, decode_max_blocks, block_size);
+    if (need == 0) return PA_ERR_INVALID;
+    if (!workspace || workspace_bytes < need || !aligned(workspace, 256)) return PA_ERR_WORKSPACE;
+    // the SMs of the chunk as in pa_hybrid_attention
+    int cs = chunk_sms > 0 ? chunk_sms : (d->num_sms * 21 + 50) / 100;
+    cs = cs < 1 ? 1 : (cs > d->num_sms - 2 ? d->num_sms - 2 : cs);
+    decode_ctas = (d->num_sms - cs) & ~1;
+    if (int rc = decode_impl(out_decode, q_decode, k_cache, v_cache, nullptr, nullptr, false,
+                             decode_block_tables, decode_max_blocks, decode_seq_lens,
+                             num_decode_seqs, num_q_heads, num_kv_heads, head_dim, block_size,
+                             num_blocks, scale, 0, decode_lse, static_cast<char*>(workspace) + 256,
+                             workspace_bytes - 256, stream, nullptr, nullptr, nullptr,
+                             decode_ctas, 0, 0, key_decode, value_decode, key_token_stride,
+                             value_token_stride, &dp))
+      return rc;
+    if (dp.grid != decode_ctas) return PA_ERR_UNSUPPORTED;
+  } else {
+    // no decodes: every CTA of the launch takes the prefill role
+    dp.a = DecodeArgs{};
+    dp.tk = pp.tk;
+    dp.tv = pp.tv;
+  }
+  return launch_hybrid(dp.a, &dp.tk, &dp.tv, pp.a, &pp.tq, &pp.tk, &pp.tv, &pp.tnk, &pp.tnv,
+                       decode_ctas, pp.tiles, static_cast<cudaStream_t>(stream)) == cudaSuccess
              ? PA_OK
              : PA_ERR_CUDA;
 }

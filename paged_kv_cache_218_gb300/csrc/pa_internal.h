@@ -102,6 +102,16 @@ struct PrefillArgs {
   float scale_log2;
   uint64_t wait_ns;          // limit of every mbarrier wait (normally kWaitLimitNs)
   int stall_loads;           // test launch: the loaders issue no load, every wait runs out
+  // append (pa_hybrid_attention_append; null / 0 otherwise): row i of new_k /
+  // new_v (token strides in elements) is the K / V of the chunk's query row i;
+  // the chunk's keys at positions >= q_start_pos are read from there, and its
+  // rows are written into their pool slots by the CTA of their query tile
+  const __nv_bfloat16* new_k;
+  const __nv_bfloat16* new_v;
+  long long new_k_stride;
+  long long new_v_stride;
+  __nv_bfloat16* k_pool;
+  __nv_bfloat16* v_pool;
 };
 
 struct CascadeArgs {
@@ -154,10 +164,13 @@ cudaError_t launch_cascade_prefix(const CascadeArgs& a, const CUtensorMap* tm_k,
                                   const CUtensorMap* tm_v, cudaStream_t stream);
 // One launch for a hybrid batch: the balanced decode (bf16, head_dim 128) on
 // its first decode_ctas CTAs and the prefill's CTA pairs on the rest.
+// append: the decode role writes its sequences' new tokens (d.new_k) and the
+// prefill role its chunks' (p.new_k), reading the chunks' new keys through
+// nk / nv (maps of p.new_k / p.new_v); otherwise nk / nv are unused.
 cudaError_t launch_hybrid(DecodeArgs d, const CUtensorMap* dk, const CUtensorMap* dv,
                           const PrefillArgs& p, const CUtensorMap* pq, const CUtensorMap* pk,
-                          const CUtensorMap* pv, int decode_ctas, int prefill_ctas,
-                          cudaStream_t stream);
+                          const CUtensorMap* pv, const CUtensorMap* nk, const CUtensorMap* nv,
+                          int decode_ctas, int prefill_ctas, cudaStream_t stream);
 // Shared-memory layout and warp split of a decode launch (pa_decode.cu).
 size_t decode_smem_bytes(DecodeArgs& a, int head_dim);
 

@@ -12,7 +12,8 @@ template <int kPair>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                    const __grid_constant__ CUtensorMap tm_v, const PrefillArgs a) {
-  prefill_cta<kPair>(tm_q, tm_k, tm_v, a, static_cast<int>(blockIdx.x));
+  // no new rows here (a.new_k is null): the new-row maps are not read
+  prefill_cta<kPair>(tm_q, tm_k, tm_v, tm_k, tm_v, a, static_cast<int>(blockIdx.x));
 }
 
 }  // namespace

@@ -210,9 +210,12 @@ __device__ __forceinline__ bool wait_or_abort_warp(uint32_t bar, uint32_t parity
 // even block so that a cluster's CTAs are a pair).  kPair 2: the two CTAs of
 // a cluster run consecutive query tiles as one tcgen05 pair; kPair 1: one CTA
 // per tile, no cluster.  Uses kThreads threads and the dynamic shared memory.
+// tm_nk / tm_nv map the chunk's new K / V rows (a.new_k / a.new_v) when
+// a.new_k is set (append), and are not read otherwise.
 template <int kPair>
 __device__ __forceinline__ void prefill_cta(const CUtensorMap& tm_q, const CUtensorMap& tm_k,
-                                            const CUtensorMap& tm_v, const PrefillArgs& a,
+                                            const CUtensorMap& tm_v, const CUtensorMap& tm_nk,
+                                            const CUtensorMap& tm_nv, const PrefillArgs& a,
                                             const int cta) {
   using P = Plan<kPair>;
   constexpr int kNK = P::kNK, kNV = P::kNV;
@@ -340,6 +343,18 @@ __device__ __forceinline__ void prefill_cta(const CUtensorMap& tm_q, const CUten
     if (warp == 0) tmem_dealloc<kPair>(tmem, kTmemCols);
     return;
   }
+  // Append: the chunk's own keys (positions p0 .. p0+qlen-1) are read from
+  // its new rows, not from the pool, which this launch is still filling with
+  // them; that needs the chunk to start a block (chunks of a multiple of 16
+  // tokens after full cached blocks do).  Blocks jb_new and later of the
+  // sequence are new.
+  const bool append = a.new_k != nullptr;
+  if (append && (p0 & (kBlockSize - 1)) != 0) {
+    if (tid == 0 && m == 0 && kvh == 0) atomicOr(a.err, PA_DEVERR_CHUNK);
+    if (warp == 0) tmem_dealloc<kPair>(tmem, kTmemCols);
+    return;
+  }
+  const int jb_new = append ? p0 / kBlockSize : 0x7fffffff;
   const int tv = qlen - t0 < tpt ? qlen - t0 : tpt;  // valid tokens here (<= 0: none)
   // keys [0, kmax) are visible to some row of the pair; both CTAs walk the
   // same tiles (their own rows mask what they may not see)
@@ -401,11 +416,23 @@ __device__ __forceinline__ void prefill_cta(const CUtensorMap& tm_q, const CUten
         }
         tma_load_4d(dst, &tm_k, 0, 0, chunk, group8, bar, pol);
       };
+      // 8 new rows (from row r) of head kvh's two 64-column halves: one
+      // token group of a K block, [half][8 tokens][64 columns]
+      auto load_nk = [&](uint32_t dst, int r, uint32_t bar) {
+        if constexpr (kPair == 2) {
+          if (!issuer) {
+            tma_load_3d_pair(dst, &tm_nk, 0, r, 2 * kvh, mapa_shared(bar, 0), pol);
+            return;
+          }
+        }
+        tma_load_3d(dst, &tm_nk, 0, r, 2 * kvh, bar, pol);
+      };
       // a stalled test launch issues no load: every wait runs out with no
       // copy in flight
       if (lane == 0 && !a.stall_loads) {
         tma_prefetch_desc(&tm_q);
         tma_prefetch_desc(&tm_k);
+        if (append) tma_prefetch_desc(&tm_nk);
         if (issuer) mbar_arrive_expect_tx(bar_q, kPair * 2 * kHalf);  // both Q tiles of a pair
         for (int h = 0; h < 2; ++h)
           load_q(sbase + P::kQOff + h * kHalf, h * 64, kvh * G, q0 + t0, bar_q);
@@ -436,9 +463,16 @@ __device__ __forceinline__ void prefill_cta(const CUtensorMap& tm_q, const CUten
           if (lane == 0 && issuer) mbar_arrive_expect_tx(bar, 2 * kHalf);
           __syncwarp();
           if (lane < 8 / kPair) {
-            const int id = ids_smem[(jk % kIdRing) * 8 + lane + (kPair == 2 ? 4 * rank : 0)];
-            load_k(sbase + P::kKOff + slot * P::kKSlot + lane * 2 * kBlockBytes, 2 * kvh, 2 * id,
-                   bar);
+            const int b = lane + (kPair == 2 ? 4 * rank : 0);  // block of the tile
+            const int jb = jk * 8 + b;                         // block of the sequence
+            const uint32_t dst = sbase + P::kKOff + slot * P::kKSlot + lane * 2 * kBlockBytes;
+            if (jb >= jb_new && jb < nb_vis) {
+              const int r = q0 + (jb - jb_new) * kBlockSize;
+              load_nk(dst, r, bar);
+              load_nk(dst + kBlockBytes, r + 8, bar);
+            } else {
+              load_k(dst, 2 * kvh, 2 * ids_smem[(jk % kIdRing) * 8 + b], bar);
+            }
           }
           __syncwarp();
           ++jk;
@@ -453,7 +487,10 @@ __device__ __forceinline__ void prefill_cta(const CUtensorMap& tm_q, const CUten
           wait_or_abort<kPair>((kFreeByS<kPair> ? bar_s_full : bar_k_empty) + 8 * sl,
                                ((nkt - 1 - sl) / kNK) & 1, abort_flag, a);
     } else {
-      if (lane == 0) tma_prefetch_desc(&tm_v);
+      if (lane == 0) {
+        tma_prefetch_desc(&tm_v);
+        if (append) tma_prefetch_desc(&tm_nv);
+      }
       // V tile j: this CTA's boxes complete on its own barrier; once landed
       // (and its slots past seq_len zeroed) the tile is reported to the issuer
       int jv = 0, jr = a.stall_loads ? nkt : 0;  // next V tile to load / to report
@@ -479,9 +516,14 @@ __device__ __forceinline__ void prefill_cta(const CUtensorMap& tm_q, const CUten
             // box per lane: (block lane & 7, half lane >> 3)
             if (lane < 16 / kPair) {
               const int b = lane & 7, hh = lane >> 3;
-              const int id = ids_smem[(jv % kIdRing) * 8 + b];
-              tma_load_2d(sbase + P::kVOff + slot * P::kVSlot + hh * kHalf + b * kBlockBytes, &tm_v,
-                          kvh * 128 + (hh + rank) * 64, id * kBlockSize, bar, pol);
+              const int jb = jv * 8 + b;
+              const uint32_t dst = sbase + P::kVOff + slot * P::kVSlot + hh * kHalf + b * kBlockBytes;
+              if (jb >= jb_new && jb < nb_vis)
+                tma_load_2d(dst, &tm_nv, kvh * 128 + (hh + rank) * 64,
+                            q0 + (jb - jb_new) * kBlockSize, bar, pol);
+              else
+                tma_load_2d(dst, &tm_v, kvh * 128 + (hh + rank) * 64,
+                            ids_smem[(jv % kIdRing) * 8 + b] * kBlockSize, bar, pol);
             }
             __syncwarp();
             ++jv;
@@ -636,6 +678,27 @@ __device__ __forceinline__ void prefill_cta(const CUtensorMap& tm_q, const CUten
     __syncwarp();
   } else {
     // ------------------------------------------------------------ softmax warps
+    if (append && tv > 0) {
+      // the slot scatter of this tile's tokens for head kvh, while the first
+      // scores are still on their way: K and V rows of 256 bytes, 16 bytes
+      // per thread and step (no CTA reads these slots in this launch)
+      for (int e = tid; e < tv * 32; e += kSoftmaxWarps * 32) {
+        const int i = e >> 5, which = (e >> 4) & 1, piece = e & 15;
+        const int pos = p0 + t0 + i;
+        const int id = a.block_tables[id_row + pos / kBlockSize];
+        if (id < 0 || id >= a.num_blocks) {
+          atomicOr(a.err, PA_DEVERR_BLOCK_ID);
+          continue;
+        }
+        const long long slot = static_cast<long long>(id) * kBlockSize + (pos & (kBlockSize - 1));
+        const long long row = q0 + t0 + i;
+        const uint4* src = reinterpret_cast<const uint4*>(
+            which ? a.new_v + row * a.new_v_stride : a.new_k + row * a.new_k_stride);
+        uint4* dst = reinterpret_cast<uint4*>((which ? a.v_pool : a.k_pool) +
+                                              (slot * Hkv + kvh) * 128);
+        dst[piece] = __ldg(src + kvh * 16 + piece);
+      }
+    }
     const int qd = warp & 3, hc = warp >> 2;
     const int r = qd * 32 + lane;  // query row = tensor-memory lane
     const uint32_t lane_off = static_cast<uint32_t>(qd * 32) << 16;
