@@ -102,8 +102,10 @@ constexpr int kMaxRing = 4;       // barrier slots per K / V ring
 // 128 keys x 64 columns of V).
 template <int kPair>
 struct Plan {
-  static constexpr int kNK = kPair == 2 ? 3 : 2;  // K tiles in flight
-  static constexpr int kNV = kPair == 2 ? 3 : 2;  // V tiles in flight
+  // four K and four V tiles in flight for pairs (about 1 % faster than
+  // three, whose slots the score-full / PV-done barriers free)
+  static constexpr int kNK = kPair == 2 ? 4 : 2;  // K tiles in flight
+  static constexpr int kNV = kPair == 2 ? 4 : 2;  // V tiles in flight
   static constexpr int kKSlot = 2 * kHalf / kPair;
   static constexpr int kVSlot = 2 * kHalf / kPair;
   static constexpr int kQOff = 0;
