@@ -24,8 +24,10 @@
 //    receives half the K/V bytes per product that a lone CTA does: a K/V
 //    tile's intake, not the tensor pipe, set the pace of a lone CTA.  Each
 //    CTA loads its own halves with plain TMA tensor loads (no load is shared
-//    between SMs); the odd CTA's K and Q loads complete on the even CTA's
-//    barriers, its V loads on its own, which it then reports to the even CTA.
+//    between SMs); the odd CTA's loads complete on the even CTA's barriers,
+//    except the V tile holding a sequence's partly filled last block, which
+//    lands on the odd CTA's own barrier, has its rows past seq_len zeroed and
+//    is then reported to the even CTA.
 //  * In a hybrid batch (pa_hybrid_attention) the same pairs run in the launch
 //    of the decodes, on the SMs the decode's CTAs leave free.
 //  * Warp roles.  Warp 9 loads Q once, then the K tiles; warp 10 the V
@@ -160,6 +162,16 @@ __host__ __device__ constexpr uint32_t instr_desc(uint32_t b_mn, uint32_t m) {
          | (b_mn << 16)         // B major-ness
          | ((128u >> 3) << 17)  // N / 8
          | ((m >> 4) << 24);    // M / 16
+}
+
+// One arrival on an mbarrier of the other CTA of the pair that also expects
+// `bytes` more transaction bytes (the bytes of this CTA's loads that complete
+// on that barrier).
+__device__ __forceinline__ void mbar_arrive_expect_tx_remote(uint32_t cluster_addr,
+                                                             uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cluster.b64 _, [%0], %1;" ::"r"(cluster_addr),
+               "r"(bytes)
+               : "memory");
 }
 
 // Barrier waits.  A pair's barriers also receive the other CTA's arrivals,
@@ -495,8 +507,15 @@ __device__ __forceinline__ void prefill_cta(const CUtensorMap& tm_q, const CUten
       }
       // V tile j: this CTA's boxes complete on its own barrier; once landed
       // (and its slots past seq_len zeroed) the tile is reported to the issuer
-      int jv = 0, jr = a.stall_loads ? nkt : 0;  // next V tile to load / to report
-      while (jr < nkt && !*abort_flag) {
+      // V tile j: the boxes of both CTAs of a pair complete straight on the
+      // issuer's ready barrier (each CTA one arrival that expects its own
+      // bytes), as K's do -- except the tile holding the sequence's last block
+      // when that block is only partly filled: it lands on this CTA's own
+      // barrier first, its slots past seq_len are zeroed, and then it is
+      // reported to the issuer
+      int jv = a.stall_loads ? nkt : 0;  // next V tile to load
+      int tail_slot = -1;                // the tail tile's slot while its report is pending
+      while ((jv < nkt || tail_slot >= 0) && !*abort_flag) {
         bool progressed = false;
         if (jf < nkt && jv + kIdBatch / 2 >= jf) {
           fetch_ids(jf);
@@ -511,8 +530,17 @@ __device__ __forceinline__ void prefill_cta(const CUtensorMap& tm_q, const CUten
                             ? bar_test<kPair>(bar_o_done + 8 * slot, ((jv / kNV) - 1) & 1)
                             : bar_test<kPair>(bar_v_empty + 8 * slot, ((jv / kNV) - 1) & 1);
           if (__shfl_sync(0xffffffffu, free_slot ? 1 : 0, 0)) {
-            const uint32_t bar = bar_v_full + 8 * slot;
-            if (lane == 0) mbar_arrive_expect_tx(bar, P::kVSlot);
+            const bool tail = tail_tile == jv;
+            const bool remote = kPair == 2 && !issuer && !tail;
+            const uint32_t bar = tail ? bar_v_full + 8 * slot
+                                      : (remote ? mapa_shared(bar_v_ready + 8 * slot, 0)
+                                                : bar_v_ready + 8 * slot);
+            if (lane == 0) {
+              if (remote)
+                mbar_arrive_expect_tx_remote(bar, P::kVSlot);
+              else
+                mbar_arrive_expect_tx(bar, P::kVSlot);
+            }
             __syncwarp();
             // CTA r of a pair takes columns 64r .. 64r+63 of every key; one
             // box per lane: (block lane & 7, half lane >> 3)
@@ -520,50 +548,50 @@ __device__ __forceinline__ void prefill_cta(const CUtensorMap& tm_q, const CUten
               const int b = lane & 7, hh = lane >> 3;
               const int jb = jv * 8 + b;
               const uint32_t dst = sbase + P::kVOff + slot * P::kVSlot + hh * kHalf + b * kBlockBytes;
-              if (jb >= jb_new && jb < nb_vis)
-                tma_load_2d(dst, &tm_nv, kvh * 128 + (hh + rank) * 64,
-                            q0 + (jb - jb_new) * kBlockSize, bar, pol);
-              else
-                tma_load_2d(dst, &tm_v, kvh * 128 + (hh + rank) * 64,
-                            ids_smem[(jv % kIdRing) * 8 + b] * kBlockSize, bar, pol);
+              const bool fresh = jb >= jb_new && jb < nb_vis;
+              const CUtensorMap* map = fresh ? &tm_nv : &tm_v;
+              const int y = fresh ? q0 + (jb - jb_new) * kBlockSize
+                                  : ids_smem[(jv % kIdRing) * 8 + b] * kBlockSize;
+              if constexpr (kPair == 2) {
+                if (remote) {
+                  tma_load_2d_pair(dst, map, kvh * 128 + (hh + rank) * 64, y, bar, pol);
+                } else {
+                  tma_load_2d(dst, map, kvh * 128 + (hh + rank) * 64, y, bar, pol);
+                }
+              } else {
+                tma_load_2d(dst, map, kvh * 128 + (hh + rank) * 64, y, bar, pol);
+              }
             }
             __syncwarp();
+            if (tail) tail_slot = slot;
             ++jv;
             progressed = true;
           }
         }
-        if (jr < jv) {
-          const int slot = jr % kNV;
+        if (tail_slot >= 0) {
           bool landed = false;
-          if (lane == 0) landed = bar_test<kPair>(bar_v_full + 8 * slot, (jr / kNV) & 1);
+          if (lane == 0) landed = bar_test<kPair>(bar_v_full + 8 * tail_slot, 0);  // its one use
           if (__shfl_sync(0xffffffffu, landed ? 1 : 0, 0)) {
-            // the sequence's last block may end inside this tile: its slots
-            // past seq_len hold no token and must not reach the PV product
-            const bool tail = tail_tile == jr;
-            if (tail) {
-              const int jl = (n - 1) / kBlockSize;
-              const uint32_t vt = sbase + P::kVOff + slot * P::kVSlot;
-              const int first = n - jl * kBlockSize;  // rows first..15 of block jl % 8
-              const int per_row = 8 * (2 / kPair);    // 16-byte chunks of a key row here
-              for (int e = lane; e < (kBlockSize - first) * per_row; e += 32) {
-                const int row = first + e / per_row, hh = (e / 8) % (2 / kPair), ch = e & 7;
-                st_shared_zero16(vt + hh * kHalf + ((jl & 7) * kBlockSize + row) * 128 + (ch << 4));
-              }
-              fence_proxy_async_smem();
+            // the sequence's last block ends inside this tile: its slots past
+            // seq_len hold no token and must not reach the PV product
+            const int jl = (n - 1) / kBlockSize;
+            const uint32_t vt = sbase + P::kVOff + tail_slot * P::kVSlot;
+            const int first = n - jl * kBlockSize;  // rows first..15 of block jl % 8
+            const int per_row = 8 * (2 / kPair);    // 16-byte chunks of a key row here
+            for (int e = lane; e < (kBlockSize - first) * per_row; e += 32) {
+              const int row = first + e / per_row, hh = (e / 8) % (2 / kPair), ch = e & 7;
+              st_shared_zero16(vt + hh * kHalf + ((jl & 7) * kBlockSize + row) * 128 + (ch << 4));
             }
+            fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0) {
-              if (kPair == 2 && !issuer) {
-                // the zeroed rows are generic stores the pair's MMA will read
-                if (tail)
-                  mbar_arrive_remote_release(mapa_shared(bar_v_ready + 8 * slot, 0));
-                else
-                  mbar_arrive_remote(mapa_shared(bar_v_ready + 8 * slot, 0));
-              } else {
-                mbar_arrive(bar_v_ready + 8 * slot);
-              }
+              // the zeroed rows are generic stores the pair's MMA will read
+              if (kPair == 2 && !issuer)
+                mbar_arrive_remote_release(mapa_shared(bar_v_ready + 8 * tail_slot, 0));
+              else
+                mbar_arrive(bar_v_ready + 8 * tail_slot);
             }
-            ++jr;
+            tail_slot = -1;
             progressed = true;
           }
         }
@@ -585,8 +613,8 @@ __device__ __forceinline__ void prefill_cta(const CUtensorMap& tm_q, const CUten
     if (lane == 0 && issuer) {
       // a completion reaches this CTA's barrier and, for a pair, the peer's
       auto commit = [&](uint32_t bar) {
+        if constexpr (kPair == 2) tc_commit<kPair>(mapa_shared(bar, 1));  // the peer's first
         tc_commit<kPair>(bar);
-        if constexpr (kPair == 2) tc_commit<kPair>(mapa_shared(bar, 1));
       };
       IdleClock clk(a.wait_ns);
       auto give_up = [&]() {
