@@ -225,3 +225,47 @@ def test_fused_step_rejects_bad_arguments_before_launching(pa, cuda_device):
     assert e.value.status == pa.PA_ERR_WORKSPACE
     torch.cuda.synchronize()
     assert pa.pa_device_error_flags() == 0
+
+
+def test_fused_step_several_chunks_without_decodes(pa, cuda_device):
+    """Three chunks (one of them ragged, all starting a block), no decodes:
+    the launch writes every chunk's new rows and attends each chunk's own keys
+    from them; bit for bit pa_reshape_and_cache + pa_prefill_chunk, and the
+    oracle elementwise."""
+    w = W.prefill_batch([(0, 40), (32, 72), (160, 130)], Hq=16, Hkv=4, D=128, seed=964,
+                        poison=True)
+    dev = cuda_device
+    kc_ref, vc_ref = oracle_scattered(w)
+    C = w.num_chunks
+    T = int(w.cu_q_lens[C])
+    ref, ref_lse = oracle.prefill(w.q[:T], kc_ref, vc_ref, w.block_tables[:C], w.cu_q_lens,
+                                  w.q_start_pos, w.seq_lens[:C], w.scale)
+    kc0, vc0 = _poisoned_pools(w)
+    kc, vc = bits_to_dev(kc0, dev), bits_to_dev(vc0, dev)
+    q, key, value = (bits_to_dev(a, dev) for a in (w.q, w.key, w.value))
+    bt = torch.from_numpy(w.block_tables).to(dev)
+    sl = torch.from_numpy(w.seq_lens).to(dev)
+    cu = torch.from_numpy(w.cu_q_lens).to(dev)
+    qs = torch.from_numpy(w.q_start_pos).to(dev)
+    max_q = int(np.max(np.diff(w.cu_q_lens)))
+    Hq, D = w.num_q_heads, w.head_dim
+    out = torch.full((T, Hq, D), float("nan"), dtype=torch.bfloat16, device=dev)
+    lse = torch.full((T, Hq), float("nan"), dtype=torch.float32, device=dev)
+    none = torch.empty((0, Hq, D), dtype=torch.bfloat16, device=dev)
+    pa.pa_hybrid_attention_append(out, q[:T], key[:T], value[:T], bt[:C], cu, qs, sl[:C], max_q,
+                                  none, none, key[:0], value[:0], bt[:0], sl[:0], kc, vc, w.scale,
+                                  None, chunk_lse=lse)
+    # the two-launch form on the same inputs
+    dw = DeviceWorkload(w, dev)
+    dw.scatter(pa)
+    out2 = torch.empty_like(out)
+    lse2 = torch.empty_like(lse)
+    pa.pa_prefill_chunk(out2, dw.q[:T], dw.k_cache, dw.v_cache, dw.block_tables[:C], cu, qs,
+                        dw.seq_lens[:C], max_q, w.scale, out_lse=lse2)
+    torch.cuda.synchronize()
+    assert np.array_equal(dev_to_bits(kc), kc_ref) and np.array_equal(dev_to_bits(vc), vc_ref)
+    assert np.array_equal(dev_to_bits(out), dev_to_bits(out2))
+    assert torch.equal(lse, lse2)
+    assert_close(out, ref, "fused chunks")
+    assert_close(lse.cpu().numpy(), ref_lse, "fused chunks lse")
+    assert pa.pa_device_error_flags() == 0
