@@ -269,3 +269,28 @@ def test_fused_step_several_chunks_without_decodes(pa, cuda_device):
     assert_close(out, ref, "fused chunks")
     assert_close(lse.cpu().numpy(), ref_lse, "fused chunks lse")
     assert pa.pa_device_error_flags() == 0
+
+
+def test_fused_step_strided_rows(pa, cuda_device):
+    """New K / V rows with a token stride above Hkv * D (rows of a fused QKV
+    buffer): the same bits as with contiguous rows."""
+    w = W.sarathi_hybrid(seed=965, poison=True, chunk_tokens=96, chunk_start=48, num_decode=10,
+                         dec_lo=30, dec_hi=700, Hq=16, Hkv=4, D=128)
+    dev = cuda_device
+    rows, Hkv, D = w.key.shape
+    pad = 3 * 128  # the rest of a fused row
+    wide_k = torch.zeros((rows, Hkv * D + pad), dtype=torch.bfloat16, device=dev)
+    wide_v = torch.zeros_like(wide_k)
+    wide_k[:, :Hkv * D] = bits_to_dev(w.key, dev).view(rows, Hkv * D)
+    wide_v[:, :Hkv * D] = bits_to_dev(w.value, dev).view(rows, Hkv * D)
+    key = wide_k.as_strided((rows, Hkv, D), (Hkv * D + pad, D, 1))
+    value = wide_v.as_strided((rows, Hkv, D), (Hkv * D + pad, D, 1))
+    sc, sd, slc, sld, sk, sv, _ = _fused(pa, w, dev, key=key, value=value)
+    fc, fd, flc, fld, fk, fv, _ = _fused(pa, w, dev)
+    torch.cuda.synchronize()
+    for x, y in ((sc, fc), (sd, fd), (sk, fk), (sv, fv)):
+        assert np.array_equal(dev_to_bits(x), dev_to_bits(y))
+    assert torch.equal(slc, flc) and torch.equal(sld, fld)
+    kc_ref, _ = oracle_scattered(w)
+    assert np.array_equal(dev_to_bits(sk), kc_ref)
+    assert pa.pa_device_error_flags() == 0
