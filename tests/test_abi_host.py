@@ -129,6 +129,34 @@ def test_hybrid_checks_arguments_before_launching(lib):
     assert call(oc=None) == -1
 
 
+def test_hybrid_append_checks_arguments_before_launching(lib):
+    f = lib.pa_hybrid_attention_append
+    P, I, L = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64
+    f.argtypes = [P, P, P, P, P, I, P, P, P, I, I, I, P, P, P, P, P, P, I, P, I, P, L, L,
+                  P, P, I, I, I, I, L, ctypes.c_float, I, P, ctypes.c_size_t, P]
+    f.restype = I
+
+    def call(**kw):
+        a = dict(oc=P(256), qc=P(256), kc=P(256), vc=P(256), cbt=P(256), cmb=4, cu=P(256),
+                 qs=P(256), csl=P(256), C=1, T=32, mq=32, clse=None, od=P(256), qd=P(256),
+                 kd=P(256), vd=P(256), dbt=P(256), dmb=4, dsl=P(256), S=2, dlse=None,
+                 kst=256, vst=256, k=P(256), v=P(256), Hq=8, Hkv=2, D=128, bs=16, nb=10,
+                 scale=0.1, cs=0, ws=P(256), wsb=1 << 30, st=None)
+        a.update(kw)
+        return f(*a.values())
+
+    assert call(D=64) == -2              # the chunk's tensor-core path needs head_dim 128
+    assert call(scale=0.0) == -1
+    assert call(cs=-1) == -1
+    assert call(S=-1) == -1
+    assert call(kst=255) == -1           # a token stride below Hkv * D
+    assert call(vst=260) == -1           # not a multiple of 8 elements
+    assert call(kc=None) == -1           # the chunk's new rows are missing
+    assert call(vc=P(264)) == -1         # misaligned
+    assert call(kd=None) == -1           # the decodes' new rows are missing
+    assert call(oc=None) == -1
+
+
 def _decode_args(**kw):
     P = ctypes.c_void_p
     a = dict(out=P(16), q=P(16), k=P(16), v=P(16), bt=P(16), mb=4, sl=P(16), S=2, Hq=8, Hkv=2,
