@@ -100,6 +100,8 @@ SHAPES = [
     (130, 0, 50, 16, 700, 32, 4, 2),        # group 8, chunk from position 0, a ragged tile
     (1, 4992, 300, 100, 2000, 8, 8, 3),     # group 1, a one-token chunk beside many decodes
     (250, 64, 7, 2000, 9000, 32, 8, 4),     # group 4, few long decodes, a ragged last block
+    (64, 32, 5, 10, 400, 8, 1, 5),          # one kv head, group 8
+    (48, 16, 6, 10, 300, 4, 2, 6),          # two kv heads, group 2
 ]
 
 
