@@ -164,6 +164,26 @@ __host__ __device__ constexpr uint32_t instr_desc(uint32_t b_mn, uint32_t m) {
          | ((m >> 4) << 24);    // M / 16
 }
 
+// 64 consecutive fp32 columns of this thread's tensor-memory lane (32x32b
+// shape) together with their maximum, which the load itself reduces
+// (tcgen05.ld.red, sm_103a), waited.
+__device__ __forceinline__ void tmem_ld64_max(uint32_t taddr, uint32_t (&r)[64], float& mx) {
+  asm volatile(
+      "tcgen05.ld.red.sync.aligned.32x32b.x64.max.f32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32, %33, %34, %35, %36, %37, %38, %39, %40, %41, %42, %43, %44, %45, %46, %47, %48, %49, %50, %51, %52, %53, %54, %55, %56, %57, %58, %59, %60, %61, %62, %63}, %64, [%65];\n\t"
+      "tcgen05.wait::ld.sync.aligned;"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+        "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+        "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31]),
+        "=r"(r[32]), "=r"(r[33]), "=r"(r[34]), "=r"(r[35]), "=r"(r[36]), "=r"(r[37]), "=r"(r[38]), "=r"(r[39]),
+        "=r"(r[40]), "=r"(r[41]), "=r"(r[42]), "=r"(r[43]), "=r"(r[44]), "=r"(r[45]), "=r"(r[46]), "=r"(r[47]),
+        "=r"(r[48]), "=r"(r[49]), "=r"(r[50]), "=r"(r[51]), "=r"(r[52]), "=r"(r[53]), "=r"(r[54]), "=r"(r[55]),
+        "=r"(r[56]), "=r"(r[57]), "=r"(r[58]), "=r"(r[59]), "=r"(r[60]), "=r"(r[61]), "=r"(r[62]), "=r"(r[63]),
+        "=f"(mx)
+      : "r"(taddr)
+      : "memory");
+}
+
 // One arrival on an mbarrier of the other CTA of the pair that also expects
 // `bytes` more transaction bytes (the bytes of this CTA's loads that complete
 // on that barrier).
@@ -741,26 +761,27 @@ __device__ __forceinline__ void prefill_cta(const CUtensorMap& tm_q, const CUten
       const int b3 = j % kNS;     // score buffer
       wait_or_abort_warp<kPair>(bar_s_full + 8 * b3, (j / kNS) & 1, abort_flag, a);
       tc_fence_after();
-      tmem_ld64(tmem + lane_off + b3 * 128 + hc * 64, v);
-
       const int kb = j * kTileKeys + hc * 64;
       const int nvis = lim - kb + 1;  // visible columns of this half (may be <= 0 or > 64)
-      // eight independent partial maxima keep the dependency chains short; a
-      // warp whose rows all see the whole half skips the per-element masks
+      // a warp whose rows all see the whole half takes the row maximum from
+      // the tensor-memory load itself and skips the per-element masks; the
+      // others reduce the visible columns with eight independent partial
+      // maxima (short dependency chains)
       const bool full = __all_sync(0xffffffffu, nvis >= 64);
-      float mp[8];
-#pragma unroll
-      for (int k = 0; k < 8; ++k) mp[k] = -INFINITY;
+      float mloc;
       if (full) {
-#pragma unroll
-        for (int i = 0; i < 64; ++i) mp[i & 7] = fmaxf(mp[i & 7], __uint_as_float(v[i]));
+        tmem_ld64_max(tmem + lane_off + b3 * 128 + hc * 64, v, mloc);
       } else {
+        tmem_ld64(tmem + lane_off + b3 * 128 + hc * 64, v);
+        float mp[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) mp[k] = -INFINITY;
 #pragma unroll
         for (int i = 0; i < 64; ++i)
           if (i < nvis) mp[i & 7] = fmaxf(mp[i & 7], __uint_as_float(v[i]));
+        mloc = fmaxf(fmaxf(fmaxf(mp[0], mp[1]), fmaxf(mp[2], mp[3])),
+                     fmaxf(fmaxf(mp[4], mp[5]), fmaxf(mp[6], mp[7])));
       }
-      float mloc = fmaxf(fmaxf(fmaxf(mp[0], mp[1]), fmaxf(mp[2], mp[3])),
-                         fmaxf(fmaxf(mp[4], mp[5]), fmaxf(mp[6], mp[7])));
       mloc = mloc * a.scale_log2;  // scale > 0 keeps the order
       red_max[(b * 2 + hc) * 128 + r] = mloc;
       named_barrier(1 + qd, 64);
