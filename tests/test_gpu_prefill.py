@@ -71,6 +71,43 @@ def test_prefill_chunks_match_oracle(pa, cuda_device, chunks, Hq, Hkv, seed):
     assert pa.pa_device_error_flags() == 0
 
 
+# Positions of a planted dominant key: both ends of every 32-column group of
+# both 64-column halves of key tiles 0 and 1, which every query row of the
+# chunk sees whole (the row maximum comes from the tensor-memory load there),
+# and one key of the chunk itself on the causal diagonal (a masked half,
+# hidden from the chunk's first five rows).
+DOMINANT_KEYS = [0, 31, 32, 63, 64, 95, 96, 127, 128, 159, 160, 191, 192, 223, 224, 255, 261]
+
+
+def _dominant_workload(kpos):
+    """Queries all 1 and one key all 16: its scaled score, 2048 / sqrt(128)
+    (about 261 in log2 units), exceeds every other score of a row by more
+    than 128 in log2 units, so its 2^(s - m) overflows fp32 unless the row
+    maximum m includes it."""
+    w = W.prefill_batch([(256, 32)], Hq=8, Hkv=2, D=128, seed=910)
+    w.q[:] = W.f32_to_bf16_bits(np.float32(1.0))
+    big = W.f32_to_bf16_bits(np.float32(16.0))
+    if kpos < 256:
+        w.k_cache[w.block_tables[0, kpos // 16], kpos % 16] = big
+    else:
+        w.key[kpos - 256] = big
+    return w
+
+
+@pytest.mark.parametrize("kpos", DOMINANT_KEYS)
+def test_prefill_dominant_key_in_every_column(pa, cuda_device, kpos):
+    w = _dominant_workload(kpos)
+    dw = DeviceWorkload(w, cuda_device)
+    dw.scatter(pa)
+    out, lse = _prefill(pa, dw)
+    torch.cuda.synchronize()
+    ref, ref_lse = _oracle_prefill(w)
+    assert torch.isfinite(out).all() and torch.isfinite(lse).all()
+    assert_close(out, ref, f"dominant key at position {kpos}")
+    assert_close(lse.cpu().numpy(), ref_lse, f"dominant key at position {kpos}: lse")
+    assert pa.pa_device_error_flags() == 0
+
+
 @functools.lru_cache(maxsize=None)
 def _hybrid():
     w = W.sarathi_hybrid()

@@ -502,6 +502,40 @@ def test_prefill_is_causal_and_first_position_returns_v0():
     assert not np.array_equal(out[p + 1:37], out2[p + 1:37])
 
 
+def test_prefill_dominant_key_selects_its_value_from_its_position_on():
+    """Queries all 1 and one key all 16 (scaled score 2048 / sqrt(128), about
+    177 above any other in natural-log units): every query row at or after
+    the key's position returns the key's value (the other weights, below
+    e^-170, vanish against the 1e-12 tolerance); the rows before it are
+    exactly those of the batch without that key."""
+    def run(kpos):
+        w = W.prefill_batch([(256, 32)], Hq=8, Hkv=2, D=128, seed=910)
+        w.q[:] = W.f32_to_bf16_bits(np.float32(1.0))
+        base_w = W.prefill_batch([(256, 32)], Hq=8, Hkv=2, D=128, seed=910)
+        base_w.q[:] = w.q
+        big = W.f32_to_bf16_bits(np.float32(16.0))
+        if kpos < 256:
+            w.k_cache[w.block_tables[0, kpos // 16], kpos % 16] = big
+        else:
+            w.key[kpos - 256] = big
+        outs = []
+        for ww in (w, base_w):
+            kc, vc = _scattered(ww)
+            outs.append(oracle.prefill(ww.q, kc, vc, ww.block_tables, ww.cu_q_lens,
+                                       ww.q_start_pos, ww.seq_lens, ww.scale)[0])
+        return w, outs[0], outs[1]
+    for kpos in (0, 127, 200, 261):
+        w, out, base = run(kpos)
+        kc, vc = _scattered(w)
+        blk, off = w.block_tables[0, kpos // 16], kpos % 16
+        first = max(0, kpos - 256)  # first query row (position 256 + i) that sees the key
+        for h in range(8):
+            v = ind.to_f64(vc[blk, off, h // 4])
+            for i in range(first, 32):
+                np.testing.assert_allclose(out[i, h], v, rtol=0, atol=1e-12)
+        assert np.array_equal(out[:first], base[:first])
+
+
 # ---------------------------------------------------------------- KV byte formula
 
 def test_kv_byte_formula_golden():
