@@ -108,6 +108,33 @@ def test_prefill_dominant_key_in_every_column(pa, cuda_device, kpos):
     assert pa.pa_device_error_flags() == 0
 
 
+@pytest.mark.parametrize("chunk,Hq,Hkv", [((1536, 64), 8, 2), ((200, 333), 16, 2)])
+def test_prefill_row_maximum_moving_at_every_tile(pa, cuda_device, chunk, Hq, Hkv):
+    """Queries all 1 and every key of key tile t equal to 0.75 t (bf16-exact):
+    a key of tile t scores 128 * 0.75 t / sqrt(128), about 12.2 t in log2
+    units, so each tile's scores exceed the previous tile's by more than the
+    kernel's rescale threshold and the running maximum, the sum and O are
+    rescaled at every tile."""
+    w = W.prefill_batch([chunk], Hq=Hq, Hkv=Hkv, D=128, seed=930)
+    w.q[:] = W.f32_to_bf16_bits(np.float32(1.0))
+    p0, n = chunk
+    for pos in range(p0 + n):
+        val = W.f32_to_bf16_bits(np.float32(0.75 * (pos // 128)))
+        if pos < p0:
+            w.k_cache[w.block_tables[0, pos // 16], pos % 16] = val
+        else:
+            w.key[pos - p0] = val
+    dw = DeviceWorkload(w, cuda_device)
+    dw.scatter(pa)
+    out, lse = _prefill(pa, dw)
+    torch.cuda.synchronize()
+    ref, ref_lse = _oracle_prefill(w)
+    assert torch.isfinite(out).all()
+    assert_close(out, ref, f"maximum moving every tile {chunk}")
+    assert_close(lse.cpu().numpy(), ref_lse, "maximum moving every tile: lse")
+    assert pa.pa_device_error_flags() == 0
+
+
 @functools.lru_cache(maxsize=None)
 def _hybrid():
     w = W.sarathi_hybrid()
