@@ -189,6 +189,31 @@ def test_decode_edge_shapes(pa, cuda_device, S, lo, hi, Hq, Hkv, D, seed, partit
     assert_close(lse.cpu().numpy(), ref_lse, "edge lse")
 
 
+@pytest.mark.parametrize("partition", [-1, 0, 256])
+def test_decode_scores_climbing_along_the_sequence(pa, cuda_device, partition):
+    """Queries all 1 and every key of positions 128 t .. 128 t + 127 equal to
+    0.75 t (bf16-exact): scores climb by about 12 log2 units per 128 keys,
+    so the running maximum moves at almost every block and the pieces of a
+    split sequence carry log-sum-exps hundreds of units apart for the merge."""
+    w = W.decode_batch(6, 100, 3000, 32, 8, 128, seed=940)
+    w.q[:] = W.f32_to_bf16_bits(np.float32(1.0))
+    for s_ in range(w.num_decode_seqs):
+        n = int(w.seq_lens[s_])
+        for pos in range(n - 1):
+            w.k_cache[w.block_tables[s_, pos // 16], pos % 16] = \
+                W.f32_to_bf16_bits(np.float32(0.75 * (pos // 128)))
+        w.key[s_] = W.f32_to_bf16_bits(np.float32(0.75 * ((n - 1) // 128)))
+    kc, vc = oracle_scattered(w)
+    ref, ref_lse = oracle.decode(w.q, kc, vc, w.block_tables, w.seq_lens, w.scale)
+    dw = DeviceWorkload(w, cuda_device)
+    dw.scatter(pa)
+    out, lse, _ = _decode(pa, dw, partition)
+    assert torch.isfinite(out).all()
+    assert_close(out, ref, f"climbing scores P={partition}")
+    assert_close(lse.cpu().numpy(), ref_lse, f"climbing scores P={partition}: lse")
+    assert pa.pa_device_error_flags() == 0
+
+
 @pytest.mark.parametrize("partition", [-1, 0, 32])
 def test_decode_empty_sequences_give_zero(pa, cuda_device, partition):
     w = W.decode_batch(6, 1, 70, 8, 2, 128, seed=91)
