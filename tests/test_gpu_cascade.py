@@ -60,6 +60,25 @@ def test_cascade_shared_prompt_batch_full_size(pa, cuda_device, partition):
     assert (sb == 128).all()
 
 
+@pytest.mark.parametrize("partition", [0, -1])
+def test_cascade_scores_climbing_along_the_sequence(pa, cuda_device, partition):
+    """Queries all 1 and every key at position p equal to 0.75 (p // 128)
+    (bf16-exact), groups of 8 sharing 512 tokens: scores climb by about 12
+    log2 units per 128 keys, so a member's suffix carries a running maximum
+    far above its prefix's and the suffix decode starts from a prefix (o, lse)
+    whose weight is e^-100 or less."""
+    w = W.cow_mix(num_seqs=40, group=8, prefix_tokens=512, Hq=32, Hkv=8, D=128,
+                  max_len=2048, seed=950)
+    w.q[:] = W.f32_to_bf16_bits(np.float32(1.0))
+    for s_ in range(w.num_decode_seqs):
+        n = int(w.seq_lens[s_])
+        for pos in range(n - 1):
+            w.k_cache[w.block_tables[s_, pos // 16], pos % 16] = \
+                W.f32_to_bf16_bits(np.float32(0.75 * (pos // 128)))
+        w.key[s_] = W.f32_to_bf16_bits(np.float32(0.75 * ((n - 1) // 128)))
+    run(pa, cuda_device, w, 8, partition)
+
+
 SHAPES = [  # num_seqs, group, prefix_tokens, Hq, Hkv, max_len
     (40, 8, 512, 32, 8, 2048),   # 8 members x group 4 = 32 rows
     (30, 3, 96, 16, 2, 600),     # 24 rows, two kv heads

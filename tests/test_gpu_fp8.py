@@ -144,6 +144,23 @@ def test_fp8_queries_far_from_unit_scale(pa, cuda_device, q_mult):
     run_case(pa, Fp8Case(w, cuda_device, q_mult=q_mult), 0)
 
 
+@pytest.mark.parametrize("partition", [0, 256, -1])
+def test_fp8_scores_climbing_along_the_sequence(pa, cuda_device, partition):
+    """Queries all 1 and every key at position p equal to 0.75 (p // 128)
+    before quantization: scores climb by about 12 log2 units per 128 keys,
+    so the running maximum moves at almost every block (two blocks per step
+    on this path) and split pieces carry log-sum-exps far apart."""
+    w = W.decode_batch(6, 100, 3000, 32, 8, 128, seed=960)
+    w.q[:] = W.f32_to_bf16_bits(np.float32(1.0))
+    for s_ in range(w.num_decode_seqs):
+        n = int(w.seq_lens[s_])
+        for pos in range(n - 1):
+            w.k_cache[w.block_tables[s_, pos // 16], pos % 16] = \
+                W.f32_to_bf16_bits(np.float32(0.75 * (pos // 128)))
+        w.key[s_] = W.f32_to_bf16_bits(np.float32(0.75 * ((n - 1) // 128)))
+    run_case(pa, Fp8Case(w, cuda_device), partition)
+
+
 def test_fp8_rejects_head_dim_64(pa, cuda_device):
     w = W.tiny()
     c_k = torch.zeros(w.k_cache.shape, dtype=torch.uint8, device=cuda_device)
