@@ -298,7 +298,7 @@ size_t pa_hybrid_workspace_size(int num_decode_seqs, int num_q_heads, int num_kv
  * chunk's query tiles as tensor-core CTA pairs, which start at once on the SMs
  * the decode leaves free, so the chunk's tensor-core work runs under the
  * decode's HBM streaming instead of after it.  chunk_sms = 0 picks about a
- * fifth of the SMs; values are clamped to [1, num_sms - 2].  The chunk reads
+ * seventh of the SMs (22 of 152); values are clamped to [1, num_sms - 2].  The chunk reads
  * nothing the decode writes; work queued after the call on the stream sees
  * both results.  With no chunk (or no decode) the call is pa_decode (or
  * pa_prefill_chunk) alone.  The decode of this call needs head_dim 128

@@ -949,6 +949,13 @@ int pa_merge_partials(void* out, float* out_lse, const float* part_out, const fl
 }
 
 // Argument checks of a prefill-chunk call (PA_OK: launch it; done: nothing to do).
+// SMs a hybrid step leaves to its chunk by default: about a seventh (22 of
+// 152).  On the Sarathi batch (a 512-query chunk next to 128 decodes) this
+// hides the chunk's tensor work under the decode's HBM streaming; the fused
+// step measured 186.2-186.3 us at 22 SMs, 186.8-187.0 at 24-28 and 187.1 at
+// 32.
+static int default_chunk_sms(int num_sms) { return (num_sms * 29 + 100) / 200; }
+
 static int prefill_check(const void* out, const void* q, const void* k_cache, const void* v_cache,
                          const int32_t* block_tables, int max_blocks_per_seq,
                          const int32_t* cu_q_lens, const int32_t* q_start_pos,
@@ -1114,11 +1121,9 @@ int pa_hybrid_attention(void* out_chunk, const void* q_chunk, const int32_t* chu
   DeviceInfo* d;
   if (int rc = current_device_info(&d)) return rc;
   if (d->num_sms < 4) return PA_ERR_UNSUPPORTED;
-  // SMs left to the chunk: by default about a fifth (32 of 152), which on the
-  // Sarathi batch of a 512-query chunk next to 128 decodes hides the chunk's
-  // tensor work under the decode's HBM streaming.  The decode takes an even
+  // SMs left to the chunk (default_chunk_sms).  The decode takes an even
   // number of CTAs, so that the launch's clusters of two never mix the roles.
-  int cs = chunk_sms > 0 ? chunk_sms : (d->num_sms * 21 + 50) / 100;
+  int cs = chunk_sms > 0 ? chunk_sms : default_chunk_sms(d->num_sms);
   cs = cs < 1 ? 1 : (cs > d->num_sms - 2 ? d->num_sms - 2 : cs);
   const int decode_ctas = (d->num_sms - cs) & ~1;
   // the fused kernel holds the bf16 head_dim-128 decode only; the chunk
@@ -1195,7 +1200,7 @@ int pa_hybrid_attention_append(
     if (need == 0) return PA_ERR_INVALID;
     if (!workspace || workspace_bytes < need || !aligned(workspace, 256)) return PA_ERR_WORKSPACE;
     // the SMs of the chunk as in pa_hybrid_attention
-    int cs = chunk_sms > 0 ? chunk_sms : (d->num_sms * 21 + 50) / 100;
+    int cs = chunk_sms > 0 ? chunk_sms : default_chunk_sms(d->num_sms);
     cs = cs < 1 ? 1 : (cs > d->num_sms - 2 ? d->num_sms - 2 : cs);
     decode_ctas = (d->num_sms - cs) & ~1;
     if (int rc = decode_impl(out_decode, q_decode, k_cache, v_cache, nullptr, nullptr, false,
